@@ -1,0 +1,225 @@
+/*
+ * etc_moe.h -- C ABI of the GB300 Event Tensor MoE library (libetc_moe.so).
+ *
+ * The library runs one Mixture-of-Experts layer (router -> top-k -> per-expert
+ * counts and exp_indptr -> token permute -> GroupGEMM gate/up with SwiGLU ->
+ * GroupGEMM down -> weighted combine) as ONE persistent CUDA kernel whose tiled
+ * tasks are coordinated by an Event Tensor: a device array of counters.  It
+ * also exports the split-K row-sum task graph and a chain of
+ * RMSNorm -> MoE -> residual blocks run in one launch.
+ *
+ * Sources for the operations ("Event Tensor: A Unified Abstraction for
+ * Compiling Dynamic Megakernel", paper summary page and podcast transcript):
+ *   - MoE subgraph, runtime tensors topk and exp_indptr: Figure 2, Figure 5(b).
+ *   - Data-dependent event update (an expert's wait_count is the number of
+ *     tokens routed to it) and data-dependent task triggering (expert i fires
+ *     the GroupGEMM tiles of rows [exp_indptr[i], exp_indptr[i+1])): podcast
+ *     transcript, cues 7 and 9.
+ *   - Symbolic shapes: the token count T is a per-call value; the same kernel
+ *     serves every T with no recompilation and no graph capture: Figure 4,
+ *     podcast cue 5, Table 1 (0 JIT captures).
+ *   - Static scheduling (per-SM task lists, notify/wait on counters) and
+ *     dynamic scheduling (a notify that brings a counter to zero pushes the
+ *     ready task into a shared queue; idle SMs pop): Figures 6-9, podcast
+ *     cue 11.
+ *   - Split-K: partial_sum(i,j) notifies event i (wait_count = number of column
+ *     tiles, map "ij->i"); final_sum(i) waits on event i only ("i->i"):
+ *     Figure 3, podcast cue 3.
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers, 16-byte aligned, contiguous
+ *     row-major with the shapes given below.  bf16 means IEEE bfloat16 stored
+ *     as uint16.  The caller owns all tensors it passes; the library never
+ *     frees them and never keeps them past the call.
+ *   - `stream` is a cudaStream_t passed as void*.  Calls are asynchronous on
+ *     it: nothing is synchronised and nothing is copied to the host.
+ *   - Return 0 (ETC_OK) or a negative ETC_ERR_* code; etc_last_error() then
+ *     holds a message (per calling thread).
+ *   - Device-side waits are bounded in time.  A wait that gives up records a
+ *     timeout in the plan's status, makes every CTA exit cleanly, and leaves
+ *     the CUDA context usable; etc_plan_check() reports it once the stream has
+ *     completed, and etc_plan_reset() makes the plan usable again.
+ */
+#ifndef ETC_MOE_H_
+#define ETC_MOE_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ETC_OK 0
+#define ETC_ERR_INVALID (-1)       /* bad shape, pointer, alignment or T */
+#define ETC_ERR_CUDA (-2)          /* a CUDA runtime call failed */
+#define ETC_ERR_TIMEOUT (-3)       /* a device wait gave up (see etc_plan_check) */
+#define ETC_ERR_UNIMPLEMENTED (-4) /* option not supported by this build */
+#define ETC_ERR_STATE (-5)         /* plan needs etc_plan_reset after a timeout */
+
+typedef enum { ETC_SCHED_STATIC = 0, ETC_SCHED_DYNAMIC = 1 } etc_sched_t;
+
+/* Debug bits for etc_moe_opts.debug_flags. */
+#define ETC_DEBUG_FAULT_EXTRA_WAIT 0x1u /* add 1 to expert debug_arg's wait_count: its
+                                           tiles never become ready, so a wait times out */
+#define ETC_DEBUG_POISON 0x2u           /* fill intermediate buffers with NaN before each call */
+
+typedef struct etc_plan_s* etc_plan_t;
+
+typedef struct {
+  int hidden;        /* H: model width; multiple of 128 */
+  int n_experts;     /* E: 8..256, multiple of 8 */
+  int top_k;         /* k: 1..min(E,16) */
+  int inter;         /* I: expert intermediate width; multiple of 64 */
+  int t_max;         /* largest token count a call may pass (>= 1) */
+  int sched;         /* etc_sched_t */
+  int n_blocks;      /* 1 for etc_moe_forward; 1..4 for etc_chain_forward */
+  float rms_eps;     /* RMSNorm epsilon of the chain (0 -> 1e-6) */
+  const float* router_bias;          /* device fp32 [E] added to the logits, or NULL */
+  unsigned long long wait_timeout_ns; /* device wait limit (0 -> 2 s) */
+  unsigned debug_flags;              /* ETC_DEBUG_* */
+  int debug_arg;                     /* expert id for ETC_DEBUG_FAULT_EXTRA_WAIT */
+  int out_dtype;                     /* ETC_OUT_F32 (default) or ETC_OUT_BF16 */
+} etc_moe_opts;
+
+/* Element type of `out` (etc_moe_opts.out_dtype). */
+#define ETC_OUT_F32 0  /* the fp32 combine sum, unrounded */
+#define ETC_OUT_BF16 1 /* the same sum rounded to bf16 */
+
+/*
+ * Creates a plan for one weight shape: validates the options, allocates the
+ * workspace (event counters, task queue, routing buffers, permuted
+ * activations sized for t_max), builds the TMA descriptors of the workspace,
+ * and sizes the persistent grid (one CTA per SM, all co-resident).  Nothing
+ * in the plan depends on T.  The plan belongs to the current CUDA device.
+ * Returns ETC_ERR_INVALID for unsupported shapes, ETC_ERR_CUDA if allocation
+ * fails.  Free with etc_plan_destroy.
+ */
+int etc_moe_plan(etc_plan_t* plan, const etc_moe_opts* opts);
+
+/*
+ * One MoE layer, out = sum_j w[t,j] * FFN_{ids[t,j]}(x[t]), in ONE kernel
+ * launch on `stream`.
+ *   x          bf16 [T, H]
+ *   gate_w     bf16 [H, E]       router weight (logits = x gate_w + bias)
+ *   w_gate_up  bf16 [E, 2I, H]   rows 0..I-1 gate, rows I..2I-1 up (K-major)
+ *   w_down     bf16 [E, H, I]    (K-major)
+ *   out        fp32 [T, H] (bf16 [T, H] when opts.out_dtype = ETC_OUT_BF16)
+ * Routing: top-k of the fp32 logits, ties to the lower expert id; weights =
+ * softmax over the k selected logits.  Accumulation is fp32; the SwiGLU
+ * activation is rounded to bf16 (the operand of the second GEMM); the
+ * per-expert outputs stay fp32 until the combine, whose sum is rounded to
+ * bf16 once.  0 <= T <= t_max; T == 0 returns ETC_OK without launching.
+ * Concurrent calls on one plan are undefined: give each stream its own plan.
+ */
+int etc_moe_forward(etc_plan_t plan, void* stream, const void* x, const void* gate_w,
+                    const void* w_gate_up, const void* w_down, int T, void* out);
+
+/*
+ * The same layer computed by the same task code, one kernel launch per stage
+ * (router, top-k, scan, permute, gate/up, down, combine: 7 launches).  The
+ * ablation baseline for the one-launch megakernel.  Same arguments and result.
+ */
+int etc_moe_forward_unfused(etc_plan_t plan, void* stream, const void* x, const void* gate_w,
+                            const void* w_gate_up, const void* w_down, int T, void* out);
+
+/*
+ * Routing from caller-given fp32 logits [T, E] (device): runs the top-k,
+ * count/scan and permute stages of the megakernel on `x` and leaves the
+ * routing in the plan's workspace for etc_moe_debug_routing.  Used to check
+ * the routing bit for bit against a reference fed the same logits.
+ */
+int etc_moe_route_from_logits(etc_plan_t plan, void* stream, const float* logits, const void* x,
+                              int T);
+
+/*
+ * Copies the last call's routing of block `block` from the workspace into
+ * caller buffers (device pointers, each may be NULL), asynchronously on
+ * `stream`:  logits fp32 [T,E] (with bias), topk_ids int32 [T,k], topk_w fp32
+ * [T,k], counts int32 [E], exp_indptr int32 [E+1], pos int32 [T,k] (row of
+ * slot (t,j) in the expert-sorted order).  T is the last call's token count.
+ */
+int etc_moe_debug_routing(etc_plan_t plan, void* stream, int block, void* logits, void* topk_ids,
+                          void* topk_w, void* counts, void* exp_indptr, void* pos);
+
+/*
+ * Copies `bytes` bytes from the start of an intermediate buffer of the last
+ * call into `dst` (device), asynchronously on `stream`.  which: 0 = x_perm
+ * bf16 [T*k, H] (expert-sorted input rows), 1 = act bf16 [T*k, I] (SwiGLU
+ * output), 2 = y_perm fp32 [T*k, H] (per-row expert outputs).  Returns
+ * ETC_ERR_INVALID if `bytes` exceeds the buffer.
+ */
+int etc_moe_debug_buffer(etc_plan_t plan, void* stream, int which, void* dst,
+                         unsigned long long bytes);
+
+/*
+ * Chain of opts.n_blocks blocks  x <- x + MoE_b(RMSNorm_b(x))  in ONE launch.
+ * Arguments are HOST arrays of n_blocks DEVICE pointers:
+ *   norm_w[b] bf16 [H], gate_w[b] bf16 [H,E], router_bias[b] fp32 [E] (the
+ *   array or an entry may be NULL), w_gate_up[b] bf16 [E,2I,H],
+ *   w_down[b] bf16 [E,H,I].  x bf16 [T,H]; out [T,H] of opts.out_dtype.  The
+ *   residual stream between blocks stays fp32 in the workspace.  Each
+ *   block's normalised input is rounded to bf16 (the GEMM operand).  Block
+ *   b+1's work on a token block starts as soon as block
+ *   b has combined that token block.  T may change on every call.
+ */
+int etc_chain_forward(etc_plan_t plan, void* stream, const void* x, const void* const* norm_w,
+                      const void* const* gate_w, const float* const* router_bias,
+                      const void* const* w_gate_up, const void* const* w_down, int T, void* out);
+
+/*
+ * Reads the plan's device status (after the caller has synchronised the
+ * stream of the last call): ETC_OK, or ETC_ERR_TIMEOUT with the site in
+ * etc_last_error().  Does not synchronise anything itself.
+ */
+int etc_plan_check(etc_plan_t plan);
+
+/* Clears the status and all event counters (async on `stream`). */
+int etc_plan_reset(etc_plan_t plan, void* stream);
+
+/*
+ * Statistics of a plan: out[0] = kernel launches issued so far, out[1] =
+ * persistent grid size, out[2] = dynamic shared memory per CTA, out[3] =
+ * epoch (calls so far), out[4] = token-block size, out[5] = max tokens per
+ * expert tile.  n = number of entries wanted (<= 8).
+ */
+int etc_plan_stats(etc_plan_t plan, long long* out, int n);
+
+void etc_plan_destroy(etc_plan_t plan);
+
+/*
+ * Split-K row sum in one launch: B[i,j] = sum of A[i, j*tile : (j+1)*tile]
+ * (tile = n_cols / n_split), C[i] = sum_{j} B[i,j] in j order, after event i
+ * has received its n_split notifies.
+ *   A fp32 [n_rows, n_cols] device, 16-byte aligned; C fp32 [n_rows] device.
+ *   n_cols % n_split == 0, (n_cols / n_split) % 4 == 0, tile <= 16384,
+ *   1 <= n_split <= 64.  n_rows == 0 returns ETC_OK without launching.
+ *   sched: ETC_SCHED_STATIC or ETC_SCHED_DYNAMIC.
+ * B and the per-row counters live in a scratch buffer the library allocates
+ * on first use per device and grows as needed (freed at process exit).
+ * Calls on one device must be ordered on one stream: overlapping calls share
+ * that scratch.
+ */
+int etc_splitk_rowsum(void* stream, const float* A, long long n_rows, long long n_cols,
+                      int n_split, float* C, int sched);
+
+/*
+ * etc_splitk_rowsum with a wait limit (0 -> 2 s) and fault injection:
+ * debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT makes row debug_arg wait for one
+ * notify more than it gets, so its final sum times out.
+ */
+int etc_splitk_rowsum_ex(void* stream, const float* A, long long n_rows, long long n_cols,
+                         int n_split, float* C, int sched, unsigned long long wait_timeout_ns,
+                         unsigned debug_flags, long long debug_arg);
+
+/* Status of the last split-K calls on the current device (after a sync). */
+int etc_splitk_check(void);
+
+/* Number of kernels launched by the library so far in this process. */
+long long etc_launch_count(void);
+
+/* Message of the last error on this thread ("" if none). */
+const char* etc_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ETC_MOE_H_ */

@@ -1,0 +1,161 @@
+// etc_internal.h -- structures shared by the host side and the kernels of the
+// Event Tensor MoE library.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace etc {
+
+// ---------------------------------------------------------------------------
+// Megakernel geometry
+// ---------------------------------------------------------------------------
+constexpr int kThreads = 384;       // 12 warps per CTA, one CTA per SM
+constexpr int kWarpSched = 0;       // lane 0: task scheduler (static walk or queue pop)
+constexpr int kWarpTma = 1;         // lane 0: TMA producer
+constexpr int kWarpMma = 2;         // lane 0: tcgen05 issuer; warp owns TMEM
+constexpr int kWorkerWarp0 = 4;     // warps 4..11: epilogue + SIMT tasks
+constexpr int kNumWorkers = 256;
+constexpr int kStages = 4;          // smem operand stages
+constexpr int kRing = 8;            // smem task ring depth
+constexpr int kTB = 32;             // tokens per router/top-k/permute/combine task
+constexpr int kBT = 128;            // max rows (tokens) per expert chunk = max MMA N
+constexpr int kBK = 64;             // K elements per stage (one 128-byte swizzle row)
+constexpr int kGuRows = 64;         // gate rows (and up rows) per gate/up tile
+constexpr int kDnRows = 128;        // output columns of H per down tile
+constexpr int kAccCols = 128;       // TMEM columns per accumulator buffer
+constexpr int kTmemCols = 256;      // two accumulator buffers
+constexpr int kMaxBlocks = 4;       // chain depth per launch
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 16;
+constexpr int kStageABytes = 128 * kBK * 2;   // 16 KB: 128 weight rows
+constexpr int kStageBBytes = kBT * kBK * 2;   // 16 KB: up to 128 token rows
+constexpr int kStageBytes = kStageABytes + kStageBBytes;
+constexpr int kSimtBytes = 48 * 1024;
+constexpr int kEpiHalfBytes = 8 * 1024;       // U (4 KB fp32) + S (4 KB bf16) per half
+constexpr int kCtrlBytes = 2048;
+constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kSimtBytes +
+                           2 * kEpiHalfBytes + kCtrlBytes;
+constexpr int kRouterKStep = 32;    // K elements per router smem stage
+
+enum TaskType : int {
+  TK_NONE = 0,
+  TK_NORM = 1,
+  TK_ROUTER = 2,
+  TK_TOPK = 3,
+  TK_SCAN = 4,
+  TK_PERM = 5,
+  TK_GU = 6,
+  TK_DN = 7,
+  TK_COMB = 8,
+  TK_TERM = 15,
+};
+
+// Device error codes (DevStatus::code).
+enum DevErr : int {
+  DERR_NONE = 0,
+  DERR_TIMEOUT_EVENT = 1,
+  DERR_TIMEOUT_QUEUE = 2,
+  DERR_TIMEOUT_MBAR = 3,
+  DERR_QUEUE_OVERFLOW = 4,
+  DERR_BAD_TASK = 5,
+};
+
+struct DevStatus {
+  int code;   // first error wins
+  int where;  // site id (task type or internal wait id)
+  int aux;    // event index
+  int cta;
+};
+
+// 32-bit task descriptor: type[31:28] blk[27:25] a[24:8] b[7:0].
+__host__ __device__ inline uint32_t task_enc(int type, int blk, int a, int b) {
+  return (static_cast<uint32_t>(type) << 28) | (static_cast<uint32_t>(blk) << 25) |
+         (static_cast<uint32_t>(a) << 8) | static_cast<uint32_t>(b);
+}
+__host__ __device__ inline int task_type(uint32_t d) { return static_cast<int>(d >> 28); }
+__host__ __device__ inline int task_blk(uint32_t d) { return static_cast<int>((d >> 25) & 7); }
+__host__ __device__ inline int task_a(uint32_t d) { return static_cast<int>((d >> 8) & 0x1FFFF); }
+__host__ __device__ inline int task_b(uint32_t d) { return static_cast<int>(d & 0xFF); }
+
+// Per-block workspace (the chain keeps one per block).
+struct BlockWs {
+  float* partial;      // [NC_max, T_pad, E] router partial logits per H-chunk
+  float* logits;       // [T_max, E] final fp32 logits (with bias)
+  int* ids;            // [T_max, k]
+  float* wts;          // [T_max, k]
+  int* pos;            // [T_max, k] row of slot (t, j) in expert-sorted order
+  int* row_token;      // [R_max] token of each expert-sorted row
+  int* blk_cnt;        // [nb_max, E] per-token-block expert histogram
+  int* blk_off;        // [nb_max, E] first row of (token block, expert)
+  int* counts;         // [E]
+  int* exp_indptr;     // [E+1]
+  int* chunk_indptr;   // [E+1]
+  int* chunk_expert;   // [C_max]
+  int* chunk_row0;     // [C_max]
+  int* chunk_rows;     // [C_max]
+  int* meta;           // [8] 0: n_chunks 1: n_gu 2: n_dn
+  // Event tensor counters
+  int* ev_rblk;        // [nb_max] router partials landed per token block (count up to NC)
+  int* ev_route;       // [1] top-k tasks done (count up to nb)
+  unsigned* plan_flag; // [1] epoch once counts / exp_indptr / event inits are published
+  int* ev_expert;      // [E] count-down from counts[e] (permuted rows still missing)
+  int* ev_act;         // [C_max] count-down from gate/up tiles per chunk
+  int* ev_down;        // [C_max] count-down from down tiles per chunk
+  int* ev_tok;         // [nb_max] count-down from expert rows per token block
+  unsigned* norm_flag; // [nb_max] epoch once the token block is normalised (chain)
+  unsigned* comb_flag; // [nb_max] epoch once the token block is combined (chain)
+};
+
+struct Workspace {
+  BlockWs blk[kMaxBlocks];
+  __nv_bfloat16* x_perm;  // [R_max, H]
+  __nv_bfloat16* act;     // [R_max, I]
+  float* y_perm;          // [R_max, H] fp32 per-row expert outputs
+  __nv_bfloat16* xn;      // [T_max, H] normalised input rounded to bf16 (chain)
+  __nv_bfloat16* xn_lo;   // [T_max, H] bf16 of what that rounding dropped (router only)
+  float* resid;           // [n_blocks-1, T_max, H] fp32 residual stream between blocks
+  unsigned long long* qslots[2];  // dynamic queue, one per epoch parity
+  int* qhead[2];
+  int* qtail[2];
+  int* qtotal;            // tasks of the whole call, known after the last scan
+  unsigned* qtotal_flag;
+  int* qacc;
+  DevStatus* status;      // device copy, polled by spinning CTAs
+  DevStatus* status_host; // host-mapped mirror written on error
+  int qcap;
+};
+
+struct MegaParams {
+  CUtensorMap tm_wgu[kMaxBlocks];  // [E*2I, H] box 64x64, 128B swizzle
+  CUtensorMap tm_wd[kMaxBlocks];   // [E*H, I]  box 64x64
+  CUtensorMap tm_xperm;            // [R_max, H] box 16x64
+  CUtensorMap tm_act;              // [R_max, I] box 16x64
+  Workspace ws;
+  const __nv_bfloat16* x;
+  void* out;     // fp32 [T, H], or bf16 when out_bf16
+  int out_bf16;
+  const __nv_bfloat16* gate_w[kMaxBlocks];
+  const float* bias[kMaxBlocks];
+  const __nv_bfloat16* norm_w[kMaxBlocks];
+  const float* logits_in;  // non-null: routing from given logits (router stage skipped)
+  int H, E, k, I, T_max;
+  int n_blocks;
+  int use_norm;  // chain: RMSNorm before and residual after each block
+  float eps;
+  int T, nb, NC, HC, n_router, T_pad;
+  int NT_gu, NT_dn;
+  unsigned epoch;
+  int mode;  // 0 static, 1 dynamic
+  int stage_lo, stage_hi;
+  unsigned long long timeout_ns;
+  int debug_flags, debug_arg;
+};
+
+// Host-side launch helpers implemented next to the kernels.
+cudaError_t launch_megakernel(const MegaParams& p, int grid, cudaStream_t stream);
+cudaError_t megakernel_configure();
+
+}  // namespace etc

@@ -1,0 +1,521 @@
+// moe_api.cu -- plans, workspace and the C ABI of the MoE megakernel.
+//
+// A plan is created once per weight shape; every per-call quantity (T, the
+// token-block count, the router's H split, the call's epoch) is a kernel
+// argument, so one compiled kernel serves every token count without
+// recompilation or graph capture ("Event Tensor: A Unified Abstraction for
+// Compiling Dynamic Megakernel", Figure 4: the symbolic-shape template is
+// instantiated per call).
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "../../include/etc_moe.h"
+#include "etc_host.h"
+#include "etc_internal.h"
+
+namespace etc {
+int megakernel_occupancy();
+}
+
+using namespace etc;
+
+struct etc_plan_s {
+  int device = 0;
+  etc_moe_opts opts{};
+  int H = 0, E = 0, k = 0, I = 0, T_max = 0, n_blocks = 1;
+  int grid = 0;
+  int nb_max = 0, C_max = 0, R_max = 0;
+  long long partial_max = 0;  // max NC * T_pad over T
+  std::vector<void*> allocs;
+  void* ctrl = nullptr;       // counters, flags, queue heads: cleared by reset
+  size_t ctrl_bytes = 0;
+  Workspace ws{};
+  CUtensorMap tm_xperm{}, tm_act{};
+  const void* cached_wgu[kMaxBlocks] = {};
+  const void* cached_wd[kMaxBlocks] = {};
+  CUtensorMap tm_wgu[kMaxBlocks]{}, tm_wd[kMaxBlocks]{};
+  unsigned epoch = 0;
+  long long launches = 0;
+  int last_T = 0;
+};
+
+namespace {
+
+// Router H-split for a call: enough (token block, H-chunk) tasks to cover the
+// grid, each chunk a multiple of 32 rows of H.
+int choose_nc(int T, int H, int grid) {
+  const int nb = (T + kTB - 1) / kTB;
+  int nc = 1;
+  while (nb * nc < grid && nc < 32 && (H / (nc * 2)) % kRouterKStep == 0 && H / (nc * 2) >= 64)
+    nc *= 2;
+  return nc;
+}
+
+int alloc_dev(etc_plan_t p, void** out, size_t bytes) {
+  void* d = nullptr;
+  cudaError_t e = cudaMalloc(&d, std::max<size_t>(bytes, 256));
+  if (e != cudaSuccess)
+    return set_error(ETC_ERR_CUDA, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+  p->allocs.push_back(d);
+  *out = d;
+  return ETC_OK;
+}
+
+// Bump allocator over one device buffer (256-byte aligned pieces).
+struct Bump {
+  char* base;
+  size_t off;
+  template <class T>
+  T* take(size_t n) {
+    off = (off + 255) & ~static_cast<size_t>(255);
+    T* r = reinterpret_cast<T*>(base ? base + off : nullptr);
+    off += n * sizeof(T);
+    return r;
+  }
+};
+
+void carve_block(Bump& data, Bump& ctrl, BlockWs& b, const etc_plan_s& p) {
+  const size_t E = p.E, k = p.k, T = p.T_max, nb = p.nb_max, C = p.C_max, R = p.R_max;
+  b.partial = data.take<float>(p.partial_max * E);
+  b.logits = data.take<float>(T * E);
+  b.ids = data.take<int>(T * k);
+  b.wts = data.take<float>(T * k);
+  b.pos = data.take<int>(T * k);
+  b.row_token = data.take<int>(R);
+  b.blk_cnt = data.take<int>(nb * E);
+  b.blk_off = data.take<int>(nb * E);
+  b.counts = data.take<int>(E);
+  b.exp_indptr = data.take<int>(E + 1);
+  b.chunk_indptr = data.take<int>(E + 1);
+  b.chunk_expert = data.take<int>(C);
+  b.chunk_row0 = data.take<int>(C);
+  b.chunk_rows = data.take<int>(C);
+  b.meta = data.take<int>(8);
+  b.ev_rblk = ctrl.take<int>(nb);
+  b.ev_route = ctrl.take<int>(1);
+  b.plan_flag = ctrl.take<unsigned>(1);
+  b.ev_expert = ctrl.take<int>(E);
+  b.ev_act = ctrl.take<int>(C);
+  b.ev_down = ctrl.take<int>(C);
+  b.ev_tok = ctrl.take<int>(nb);
+  b.norm_flag = ctrl.take<unsigned>(nb);
+  b.comb_flag = ctrl.take<unsigned>(nb);
+}
+
+void carve_globals(Bump& ctrl, Workspace& w) {
+  for (int i = 0; i < 2; ++i) {
+    w.qhead[i] = ctrl.take<int>(1);
+    w.qtail[i] = ctrl.take<int>(1);
+  }
+  w.qtotal = ctrl.take<int>(1);
+  w.qtotal_flag = ctrl.take<unsigned>(1);
+  w.qacc = ctrl.take<int>(1);
+  w.status = ctrl.take<DevStatus>(1);
+}
+
+int validate_opts(const etc_moe_opts* o) {
+  if (!o) return set_error(ETC_ERR_INVALID, "opts is NULL");
+  if (o->hidden <= 0 || o->hidden % 128 != 0)
+    return set_error(ETC_ERR_INVALID, "hidden=%d must be a positive multiple of 128", o->hidden);
+  if (o->n_experts < 8 || o->n_experts > kMaxE || o->n_experts % 8 != 0)
+    return set_error(ETC_ERR_INVALID, "n_experts=%d must be a multiple of 8 in [8, %d]",
+                     o->n_experts, kMaxE);
+  if (o->top_k < 1 || o->top_k > std::min(o->n_experts, kMaxK))
+    return set_error(ETC_ERR_INVALID, "top_k=%d must be in [1, min(E, %d)]", o->top_k, kMaxK);
+  if (o->inter <= 0 || o->inter % 64 != 0)
+    return set_error(ETC_ERR_INVALID, "inter=%d must be a positive multiple of 64", o->inter);
+  if (o->t_max < 1 || static_cast<long long>(o->t_max) * o->top_k > (1 << 24))
+    return set_error(ETC_ERR_INVALID, "t_max=%d out of range", o->t_max);
+  if (o->sched != ETC_SCHED_STATIC && o->sched != ETC_SCHED_DYNAMIC)
+    return set_error(ETC_ERR_INVALID, "sched=%d unknown", o->sched);
+  if (o->n_blocks < 1 || o->n_blocks > kMaxBlocks)
+    return set_error(ETC_ERR_INVALID, "n_blocks=%d must be in [1, %d]", o->n_blocks, kMaxBlocks);
+  if (o->router_bias && !aligned16(o->router_bias))
+    return set_error(ETC_ERR_INVALID, "router_bias must be 16-byte aligned");
+  if (o->out_dtype != ETC_OUT_F32 && o->out_dtype != ETC_OUT_BF16)
+    return set_error(ETC_ERR_INVALID, "out_dtype=%d unknown", o->out_dtype);
+  return ETC_OK;
+}
+
+int status_of(etc_plan_t p) {
+  volatile DevStatus* h = p->ws.status_host;
+  if (h->code == 0) return ETC_OK;
+  return set_error(ETC_ERR_TIMEOUT,
+                   "device wait timed out (code %d, task type/site %d, index %d, cta %d); "
+                   "call etc_plan_reset",
+                   h->code, h->where, h->aux, h->cta);
+}
+
+int weight_maps(etc_plan_t p, int b, const void* wgu, const void* wd) {
+  if (p->cached_wgu[b] != wgu) {
+    CUresult r = encode_tensor_map_2d_bf16(&p->tm_wgu[b], wgu, p->H,
+                                           static_cast<unsigned long long>(p->E) * 2 * p->I, kBK, 64);
+    if (r != CUDA_SUCCESS) return set_error(ETC_ERR_CUDA, "tensor map (w_gate_up) failed: %d", r);
+    p->cached_wgu[b] = wgu;
+  }
+  if (p->cached_wd[b] != wd) {
+    CUresult r = encode_tensor_map_2d_bf16(&p->tm_wd[b], wd, p->I,
+                                           static_cast<unsigned long long>(p->E) * p->H, kBK, 64);
+    if (r != CUDA_SUCCESS) return set_error(ETC_ERR_CUDA, "tensor map (w_down) failed: %d", r);
+    p->cached_wd[b] = wd;
+  }
+  return ETC_OK;
+}
+
+struct CallArgs {
+  const void* x = nullptr;
+  void* out = nullptr;
+  int T = 0;
+  int n_blocks = 1;
+  int use_norm = 0;
+  const void* gate_w[kMaxBlocks] = {};
+  const float* bias[kMaxBlocks] = {};
+  const void* norm_w[kMaxBlocks] = {};
+  const void* wgu[kMaxBlocks] = {};
+  const void* wd[kMaxBlocks] = {};
+  const float* logits_in = nullptr;
+};
+
+// One call: validation, params, then either one launch (stages lo..hi) or,
+// for the unfused ablation, one launch per stage.
+int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int stage_lo,
+             int stage_hi, int mode) {
+  if (!p) return set_error(ETC_ERR_INVALID, "plan is NULL");
+  if (a.T < 0 || a.T > p->T_max)
+    return set_error(ETC_ERR_INVALID, "T=%d outside [0, t_max=%d]", a.T, p->T_max);
+  if (a.T == 0) return ETC_OK;
+  if (a.n_blocks > p->n_blocks)
+    return set_error(ETC_ERR_INVALID, "plan holds %d blocks, call wants %d", p->n_blocks, a.n_blocks);
+  if (!a.x || !aligned16(a.x) || (stage_hi >= TK_COMB && (!a.out || !aligned16(a.out))))
+    return set_error(ETC_ERR_INVALID, "x/out must be 16-byte aligned device pointers");
+  for (int b = 0; b < a.n_blocks; ++b) {
+    if (!a.logits_in && (!a.gate_w[b] || !aligned16(a.gate_w[b])))
+      return set_error(ETC_ERR_INVALID, "gate_w[%d] must be a 16-byte aligned device pointer", b);
+    if (stage_hi >= TK_GU && (!a.wgu[b] || !a.wd[b] || !aligned16(a.wgu[b]) || !aligned16(a.wd[b])))
+      return set_error(ETC_ERR_INVALID, "expert weights of block %d must be 16-byte aligned", b);
+    if (a.use_norm && (!a.norm_w[b] || !aligned16(a.norm_w[b])))
+      return set_error(ETC_ERR_INVALID, "norm_w[%d] must be a 16-byte aligned device pointer", b);
+    if (a.bias[b] && !aligned16(a.bias[b]))
+      return set_error(ETC_ERR_INVALID, "router_bias[%d] must be 16-byte aligned", b);
+  }
+  int st = status_of(p);
+  if (st != ETC_OK) return set_error(ETC_ERR_STATE, "%s", last_error());
+  int dev = 0;
+  ETC_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != p->device)
+    return set_error(ETC_ERR_INVALID, "plan belongs to device %d, current device is %d", p->device, dev);
+
+  MegaParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  for (int b = 0; b < a.n_blocks; ++b) {
+    if (stage_hi >= TK_GU) {
+      int r = weight_maps(p, b, a.wgu[b], a.wd[b]);
+      if (r != ETC_OK) return r;
+    }
+    prm.tm_wgu[b] = p->tm_wgu[b];
+    prm.tm_wd[b] = p->tm_wd[b];
+    prm.gate_w[b] = static_cast<const __nv_bfloat16*>(a.gate_w[b]);
+    prm.bias[b] = a.bias[b];
+    prm.norm_w[b] = static_cast<const __nv_bfloat16*>(a.norm_w[b]);
+  }
+  prm.tm_xperm = p->tm_xperm;
+  prm.tm_act = p->tm_act;
+  prm.ws = p->ws;
+  prm.x = static_cast<const __nv_bfloat16*>(a.x);
+  prm.out = a.out;
+  prm.out_bf16 = p->opts.out_dtype == ETC_OUT_BF16 ? 1 : 0;
+  prm.logits_in = a.logits_in;
+  prm.H = p->H;
+  prm.E = p->E;
+  prm.k = p->k;
+  prm.I = p->I;
+  prm.T_max = p->T_max;
+  prm.n_blocks = a.n_blocks;
+  prm.use_norm = a.use_norm;
+  prm.eps = p->opts.rms_eps > 0.f ? p->opts.rms_eps : 1e-6f;
+  prm.T = a.T;
+  prm.nb = (a.T + kTB - 1) / kTB;
+  prm.NC = choose_nc(a.T, p->H, p->grid);
+  prm.HC = p->H / prm.NC;
+  prm.n_router = prm.nb * prm.NC;
+  prm.T_pad = prm.nb * kTB;
+  prm.NT_gu = p->I / kGuRows;
+  prm.NT_dn = p->H / kDnRows;
+  if (++p->epoch == 0) p->epoch = 1;
+  prm.epoch = p->epoch;
+  prm.mode = mode;
+  prm.timeout_ns = p->opts.wait_timeout_ns ? p->opts.wait_timeout_ns : 2000000000ull;
+  prm.debug_flags = static_cast<int>(p->opts.debug_flags);
+  prm.debug_arg = p->opts.debug_arg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (p->opts.debug_flags & ETC_DEBUG_POISON) {
+    const size_t rows = static_cast<size_t>(p->R_max);
+    ETC_CUDA_TRY(cudaMemsetAsync(p->ws.x_perm, 0xFF, rows * p->H * 2, s));
+    ETC_CUDA_TRY(cudaMemsetAsync(p->ws.act, 0xFF, rows * p->I * 2, s));
+    ETC_CUDA_TRY(cudaMemsetAsync(p->ws.y_perm, 0xFF, rows * p->H * 4, s));
+  }
+  if (!unfused) {
+    prm.stage_lo = stage_lo;
+    prm.stage_hi = stage_hi;
+    ETC_CUDA_TRY(launch_megakernel(prm, p->grid, s));
+    ++p->launches;
+    g_launches.fetch_add(1);
+  } else {
+    for (int stg = TK_ROUTER; stg <= TK_COMB; ++stg) {
+      prm.stage_lo = prm.stage_hi = stg;
+      ETC_CUDA_TRY(launch_megakernel(prm, p->grid, s));
+      ++p->launches;
+      g_launches.fetch_add(1);
+    }
+  }
+  p->last_T = a.T;
+  return ETC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int etc_moe_plan(etc_plan_t* out, const etc_moe_opts* opts) {
+  clear_error();
+  if (!out) return set_error(ETC_ERR_INVALID, "plan pointer is NULL");
+  *out = nullptr;
+  int r = validate_opts(opts);
+  if (r != ETC_OK) return r;
+  etc_plan_t p = new etc_plan_s();
+  p->opts = *opts;
+  p->H = opts->hidden;
+  p->E = opts->n_experts;
+  p->k = opts->top_k;
+  p->I = opts->inter;
+  p->T_max = opts->t_max;
+  p->n_blocks = opts->n_blocks;
+  auto fail = [&](int code) {
+    etc_plan_destroy(p);
+    return code;
+  };
+  if (cudaGetDevice(&p->device) != cudaSuccess) return fail(set_error(ETC_ERR_CUDA, "no CUDA device"));
+  if (megakernel_configure() != cudaSuccess)
+    return fail(set_error(ETC_ERR_CUDA, "cannot configure %d bytes of shared memory", kSmemBytes));
+  const int occ = megakernel_occupancy();
+  if (occ < 1) return fail(set_error(ETC_ERR_CUDA, "megakernel does not fit on an SM"));
+  p->grid = sm_count(p->device);  // one CTA per SM: TMEM and smem sized for that
+  if (p->grid <= 0) return fail(set_error(ETC_ERR_CUDA, "cannot query SM count"));
+
+  p->nb_max = (p->T_max + kTB - 1) / kTB;
+  p->R_max = p->T_max * p->k;
+  p->C_max = (p->R_max + kBT - 1) / kBT + p->E;
+  p->partial_max = 0;
+  for (int nb = 1; nb <= p->nb_max; ++nb) {  // the router split depends on T only through nb
+    const int T = std::min(nb * kTB, p->T_max);
+    p->partial_max = std::max<long long>(p->partial_max,
+                                         static_cast<long long>(choose_nc(T, p->H, p->grid)) * nb * kTB);
+  }
+  {
+    const int nb = p->nb_max;
+    const long long n_router_max = std::max<long long>(p->partial_max / kTB, nb);
+    const long long per_block = nb /*norm*/ + n_router_max + nb + 1 + nb +
+                                static_cast<long long>(p->C_max) * (p->I / kGuRows + p->H / kDnRows) + nb;
+    p->ws.qcap = static_cast<int>(per_block * p->n_blocks + 64);
+  }
+
+  // Data region (no clearing needed) and control region (cleared on reset).
+  Bump dsz{nullptr, 0}, csz{nullptr, 0};
+  {
+    BlockWs tmp{};
+    Workspace wtmp{};
+    for (int b = 0; b < p->n_blocks; ++b) carve_block(dsz, csz, tmp, *p);
+    carve_globals(csz, wtmp);
+  }
+  void* data = nullptr;
+  if ((r = alloc_dev(p, &data, dsz.off + 256)) != ETC_OK) return fail(r);
+  if ((r = alloc_dev(p, &p->ctrl, csz.off + 256)) != ETC_OK) return fail(r);
+  p->ctrl_bytes = csz.off + 256;
+  Bump d{static_cast<char*>(data), 0}, c{static_cast<char*>(p->ctrl), 0};
+  for (int b = 0; b < p->n_blocks; ++b) carve_block(d, c, p->ws.blk[b], *p);
+  carve_globals(c, p->ws);
+  if (cudaMemset(p->ctrl, 0, p->ctrl_bytes) != cudaSuccess)
+    return fail(set_error(ETC_ERR_CUDA, "cudaMemset failed"));
+
+  void* m = nullptr;
+  const size_t R = static_cast<size_t>(p->R_max);
+  if ((r = alloc_dev(p, &m, R * p->H * 2)) != ETC_OK) return fail(r);
+  p->ws.x_perm = static_cast<__nv_bfloat16*>(m);
+  if ((r = alloc_dev(p, &m, R * p->I * 2)) != ETC_OK) return fail(r);
+  p->ws.act = static_cast<__nv_bfloat16*>(m);
+  if ((r = alloc_dev(p, &m, R * p->H * 4)) != ETC_OK) return fail(r);
+  p->ws.y_perm = static_cast<float*>(m);
+  if (p->n_blocks > 1) {
+    if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 2)) != ETC_OK) return fail(r);
+    p->ws.xn = static_cast<__nv_bfloat16*>(m);
+    if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 2)) != ETC_OK) return fail(r);
+    p->ws.xn_lo = static_cast<__nv_bfloat16*>(m);
+    if ((r = alloc_dev(p, &m, static_cast<size_t>(p->n_blocks - 1) * p->T_max * p->H * 4)) != ETC_OK)
+      return fail(r);
+    p->ws.resid = static_cast<float*>(m);
+  }
+  for (int i = 0; i < 2; ++i) {
+    if ((r = alloc_dev(p, &m, static_cast<size_t>(p->ws.qcap) * 8)) != ETC_OK) return fail(r);
+    p->ws.qslots[i] = static_cast<unsigned long long*>(m);
+    if (cudaMemset(m, 0, static_cast<size_t>(p->ws.qcap) * 8) != cudaSuccess)
+      return fail(set_error(ETC_ERR_CUDA, "cudaMemset failed"));
+  }
+  DevStatus* hs = nullptr;
+  if (cudaHostAlloc(&hs, sizeof(DevStatus), cudaHostAllocMapped) != cudaSuccess)
+    return fail(set_error(ETC_ERR_CUDA, "cudaHostAlloc failed"));
+  std::memset(hs, 0, sizeof *hs);
+  p->ws.status_host = hs;
+
+  if (encode_tensor_map_2d_bf16(&p->tm_xperm, p->ws.x_perm, p->H, R, kBK, 16) != CUDA_SUCCESS ||
+      encode_tensor_map_2d_bf16(&p->tm_act, p->ws.act, p->I, R, kBK, 16) != CUDA_SUCCESS)
+    return fail(set_error(ETC_ERR_CUDA, "tensor map encoding of the workspace failed"));
+  *out = p;
+  return ETC_OK;
+}
+
+void etc_plan_destroy(etc_plan_t p) {
+  if (!p) return;
+  cudaDeviceSynchronize();
+  for (void* d : p->allocs) cudaFree(d);
+  if (p->ws.status_host) cudaFreeHost(p->ws.status_host);
+  delete p;
+}
+
+int etc_moe_forward(etc_plan_t p, void* stream, const void* x, const void* gate_w,
+                    const void* w_gate_up, const void* w_down, int T, void* out) {
+  clear_error();
+  if (!p) return set_error(ETC_ERR_INVALID, "plan is NULL");
+  CallArgs a;
+  a.x = x;
+  a.out = out;
+  a.T = T;
+  a.gate_w[0] = gate_w;
+  a.bias[0] = p->opts.router_bias;
+  a.wgu[0] = w_gate_up;
+  a.wd[0] = w_down;
+  return run_call(p, stream, a, false, TK_NORM, TK_COMB, p->opts.sched);
+}
+
+int etc_moe_forward_unfused(etc_plan_t p, void* stream, const void* x, const void* gate_w,
+                            const void* w_gate_up, const void* w_down, int T, void* out) {
+  clear_error();
+  if (!p) return set_error(ETC_ERR_INVALID, "plan is NULL");
+  CallArgs a;
+  a.x = x;
+  a.out = out;
+  a.T = T;
+  a.gate_w[0] = gate_w;
+  a.bias[0] = p->opts.router_bias;
+  a.wgu[0] = w_gate_up;
+  a.wd[0] = w_down;
+  return run_call(p, stream, a, true, TK_ROUTER, TK_COMB, ETC_SCHED_STATIC);
+}
+
+int etc_moe_route_from_logits(etc_plan_t p, void* stream, const float* logits, const void* x,
+                              int T) {
+  clear_error();
+  if (!p) return set_error(ETC_ERR_INVALID, "plan is NULL");
+  if (!logits) return set_error(ETC_ERR_INVALID, "logits is NULL");
+  CallArgs a;
+  a.x = x;
+  a.T = T;
+  a.logits_in = logits;
+  return run_call(p, stream, a, false, TK_ROUTER, TK_PERM, ETC_SCHED_STATIC);
+}
+
+int etc_chain_forward(etc_plan_t p, void* stream, const void* x, const void* const* norm_w,
+                      const void* const* gate_w, const float* const* router_bias,
+                      const void* const* w_gate_up, const void* const* w_down, int T, void* out) {
+  clear_error();
+  if (!p) return set_error(ETC_ERR_INVALID, "plan is NULL");
+  if (!norm_w || !gate_w || !w_gate_up || !w_down)
+    return set_error(ETC_ERR_INVALID, "weight pointer arrays must not be NULL");
+  CallArgs a;
+  a.x = x;
+  a.out = out;
+  a.T = T;
+  a.n_blocks = p->n_blocks;
+  a.use_norm = 1;
+  for (int b = 0; b < p->n_blocks; ++b) {
+    a.norm_w[b] = norm_w[b];
+    a.gate_w[b] = gate_w[b];
+    a.bias[b] = router_bias ? router_bias[b] : nullptr;
+    a.wgu[b] = w_gate_up[b];
+    a.wd[b] = w_down[b];
+  }
+  return run_call(p, stream, a, false, TK_NORM, TK_COMB, p->opts.sched);
+}
+
+int etc_moe_debug_routing(etc_plan_t p, void* stream, int block, void* logits, void* topk_ids,
+                          void* topk_w, void* counts, void* exp_indptr, void* pos) {
+  clear_error();
+  if (!p) return set_error(ETC_ERR_INVALID, "plan is NULL");
+  if (block < 0 || block >= p->n_blocks) return set_error(ETC_ERR_INVALID, "bad block %d", block);
+  const BlockWs& b = p->ws.blk[block];
+  const size_t T = p->last_T;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaMemcpyKind kind = cudaMemcpyDeviceToDevice;
+  if (logits) ETC_CUDA_TRY(cudaMemcpyAsync(logits, b.logits, T * p->E * 4, kind, s));
+  if (topk_ids) ETC_CUDA_TRY(cudaMemcpyAsync(topk_ids, b.ids, T * p->k * 4, kind, s));
+  if (topk_w) ETC_CUDA_TRY(cudaMemcpyAsync(topk_w, b.wts, T * p->k * 4, kind, s));
+  if (counts) ETC_CUDA_TRY(cudaMemcpyAsync(counts, b.counts, p->E * 4, kind, s));
+  if (exp_indptr) ETC_CUDA_TRY(cudaMemcpyAsync(exp_indptr, b.exp_indptr, (p->E + 1) * 4, kind, s));
+  if (pos) ETC_CUDA_TRY(cudaMemcpyAsync(pos, b.pos, T * p->k * 4, kind, s));
+  return ETC_OK;
+}
+
+int etc_moe_debug_buffer(etc_plan_t p, void* stream, int which, void* dst,
+                         unsigned long long bytes) {
+  clear_error();
+  if (!p || !dst) return set_error(ETC_ERR_INVALID, "NULL argument");
+  const unsigned long long R = static_cast<unsigned long long>(p->R_max);
+  const void* src = nullptr;
+  unsigned long long cap = 0;
+  if (which == 0) {
+    src = p->ws.x_perm;
+    cap = R * p->H * 2;
+  } else if (which == 1) {
+    src = p->ws.act;
+    cap = R * p->I * 2;
+  } else if (which == 2) {
+    src = p->ws.y_perm;
+    cap = R * p->H * 4;
+  } else {
+    return set_error(ETC_ERR_INVALID, "unknown buffer %d", which);
+  }
+  if (bytes > cap) return set_error(ETC_ERR_INVALID, "buffer %d holds %llu bytes", which, cap);
+  ETC_CUDA_TRY(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice,
+                               static_cast<cudaStream_t>(stream)));
+  return ETC_OK;
+}
+
+int etc_plan_check(etc_plan_t p) {
+  clear_error();
+  if (!p) return set_error(ETC_ERR_INVALID, "plan is NULL");
+  return status_of(p);
+}
+
+int etc_plan_reset(etc_plan_t p, void* stream) {
+  clear_error();
+  if (!p) return set_error(ETC_ERR_INVALID, "plan is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ETC_CUDA_TRY(cudaMemsetAsync(p->ctrl, 0, p->ctrl_bytes, s));
+  ETC_CUDA_TRY(cudaStreamSynchronize(s));
+  std::memset(const_cast<DevStatus*>(p->ws.status_host), 0, sizeof(DevStatus));
+  // The epoch keeps counting: queue slots written by earlier calls carry
+  // older epochs and can never be mistaken for this call's.
+  return ETC_OK;
+}
+
+int etc_plan_stats(etc_plan_t p, long long* out, int n) {
+  clear_error();
+  if (!p || !out) return set_error(ETC_ERR_INVALID, "NULL argument");
+  const long long v[8] = {p->launches, p->grid, kSmemBytes, p->epoch, kTB, kBT, p->ws.qcap, p->C_max};
+  for (int i = 0; i < n && i < 8; ++i) out[i] = v[i];
+  return ETC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,1009 @@
+// moe_kernel.cu -- the MoE layer as one persistent megakernel coordinated by
+// an Event Tensor ("Event Tensor: A Unified Abstraction for Compiling Dynamic
+// Megakernel", Figure 2 and Figure 5(b); podcast cues 7, 9 and 11).
+//
+// Tasks (one per tile) and the events between them:
+//
+//   NORM(b,tb)      chain only: RMSNorm of token block tb -> xn   flag norm_flag[tb]
+//   ROUTER(b,tb,c)  partial logits of token block tb over H-chunk c     -> ev_rblk[tb] (+1)
+//   TOPK(b,tb)      sums the NC partials, top-k, softmax over the top-k,
+//                   per-block expert histogram                          -> ev_route (+1)
+//   SCAN(b)         counts, exp_indptr, per-block row offsets, expert
+//                   chunks; DATA-DEPENDENT EVENT UPDATE: ev_expert[e] :=
+//                   counts[e]; publishes the plan                      flag plan_flag
+//   PERM(b,tb)      writes x_perm rows [exp_indptr[e] + rank]           -> ev_expert[e] (-n)
+//   GU(b,ch,n)      gate/up tile: 64 gate + 64 up weight rows x chunk
+//                   tokens, SwiGLU -> act                               -> ev_act[ch] (-1)
+//   DN(b,ch,n)      down tile: 128 output columns x chunk tokens -> y   -> ev_down[ch] (-1);
+//                   the tile that brings ev_down[ch] to zero notifies the
+//                   token blocks of the chunk's rows                    -> ev_tok[tb] (-rows)
+//   COMB(b,tb)      out[t] = sum_j w[t,j] y[pos[t,j]] (+ residual)     flag comb_flag[tb]
+//
+// DATA-DEPENDENT TASK TRIGGERING: expert e owns the rows
+// [exp_indptr[e], exp_indptr[e+1]) and fires exactly the GU tiles of the
+// chunks covering them (ceil(counts[e]/128) chunks); an expert with no tokens
+// fires none.
+//
+// Static scheduling: every CTA walks a fixed, stage-ordered list of task
+// slots computed from (T, blockIdx) and from the published chunk count,
+// spinning on each task's input event before handing it to its roles.
+// Dynamic scheduling: the notify that brings an event to zero pushes the
+// consumer tasks into a global queue at once (early push); CTAs pop.
+//
+// Inside a CTA (one per SM, 12 warps):
+//   warp 0   scheduler (lane 0): walks or pops tasks, waits on their events,
+//            writes them into a shared-memory ring
+//   warp 1   TMA producer (lane 0): weight and token tiles -> smem stages
+//   warp 2   tcgen05 issuer (lane 0); the warp owns 256 TMEM columns
+//   warps 4-11  workers: TMEM epilogues of the GEMM tiles and every SIMT task
+//
+// GEMM tiles are "swap-AB": the MMA's M = 128 weight rows, its N = the
+// chunk's token rows rounded up to 16 (16..128).  Decode-sized chunks (a few
+// tokens per expert) therefore waste at most 15 columns, and the weight
+// stream is what the tile pays for.
+#include <cstdio>
+
+#include "../../include/etc_moe.h"
+#include "etc_event.cuh"
+
+namespace etc {
+
+struct Task {
+  int type, blk, a, b;
+  int e, row0, rows, pad;
+};
+
+struct Ctrl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t rfull[kRing];
+  uint64_t rempty[kRing];
+  Task ring[kRing];
+  Task wtask[2];     // workers' broadcast of the current task (double-buffered)
+  uint32_t tmem_base;
+  int wflag[2];      // workers' broadcast flags
+};
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
+
+constexpr int kRingConsumers = 3;  // TMA lane, MMA lane, worker thread 0
+
+__device__ __forceinline__ QueueView queue_of(const MegaParams& p) {
+  QueueView q;
+  const int par = p.epoch & 1;
+  q.slots = p.ws.qslots[par];
+  q.head = p.ws.qhead[par];
+  q.tail = p.ws.qtail[par];
+  q.cap = p.ws.qcap;
+  q.n_seed = p.use_norm ? p.nb : p.n_router;
+  q.epoch = p.epoch;
+  return q;
+}
+
+__device__ __forceinline__ bool dynamic_mode(const MegaParams& p) { return p.mode == ETC_SCHED_DYNAMIC; }
+
+// Eight consecutive values of block blk's input row `tok` (columns 8c..8c+7):
+// the caller's bf16 x for block 0, the fp32 residual stream after that.
+__device__ __forceinline__ void load_block_input8(const MegaParams& p, int blk, int tok, int c,
+                                                  float (&f)[8]);
+
+// ---------------------------------------------------------------------------
+// small helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
+  uint4 v;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return v;
+}
+
+__device__ __forceinline__ void load_block_input8(const MegaParams& p, int blk, int tok, int c,
+                                                  float (&f)[8]) {
+  if (blk == 0) {
+    bf16x8_to_f32(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(tok) * p.H)[c], f);
+  } else {
+    const float4* r = reinterpret_cast<const float4*>(
+        p.ws.resid + (static_cast<size_t>(blk - 1) * p.T_max + tok) * p.H + 8 * c);
+    const float4 a = r[0], b = r[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+}
+
+// Exclusive prefix sum over the 256 worker threads; `tmp` holds >= 8 ints.
+__device__ __forceinline__ int workers_excl_scan(int v, int* tmp, int wt) {
+  const int lane = wt & 31, w = wt >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[w] = x;
+  named_bar(1, kNumWorkers);
+  int base = 0;
+  for (int i = 0; i < w; ++i) base += tmp[i];
+  named_bar(1, kNumWorkers);
+  return base + x - v;
+}
+
+// ---------------------------------------------------------------------------
+// SIMT tasks (executed by the 256 worker threads)
+// ---------------------------------------------------------------------------
+
+// RMSNorm of token block tb: xn[t] = x[t] / sqrt(mean(x[t]^2) + eps) * g.
+__device__ void task_norm(const MegaParams& p, const Task& t, int wt) {
+  const int blk = t.blk, tb = t.a;
+  const BlockWs& B = p.ws.blk[blk];
+  const __nv_bfloat16* g = p.norm_w[blk];
+  const int ww = wt >> 5, lane = wt & 31, n8 = p.H / 8;
+  for (int r = ww; r < kTB; r += 8) {
+    const int tok = tb * kTB + r;
+    if (tok >= p.T) break;
+    float ss = 0.f;
+    for (int c = lane; c < n8; c += 32) {
+      float f[8];
+      load_block_input8(p, blk, tok, c, f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss += f[i] * f[i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = 1.0f / sqrtf(ss / static_cast<float>(p.H) + p.eps);
+    uint4* dst = reinterpret_cast<uint4*>(p.ws.xn + static_cast<size_t>(tok) * p.H);
+    uint4* dst_lo = reinterpret_cast<uint4*>(p.ws.xn_lo + static_cast<size_t>(tok) * p.H);
+    const uint4* gv = reinterpret_cast<const uint4*>(g);
+    for (int c = lane; c < n8; c += 32) {
+      float f[8], w[8], hi[8];
+      load_block_input8(p, blk, tok, c, f);
+      bf16x8_to_f32(gv[c], w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = f[i] * inv * w[i];
+      const uint4 h = f32_to_bf16x8(f);
+      dst[c] = h;
+      // The router also reads what the bf16 rounding dropped, so that its
+      // logits see the normalised input to about 16 mantissa bits.
+      bf16x8_to_f32(h, hi);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] -= hi[i];
+      dst_lo[c] = f32_to_bf16x8(f);
+    }
+  }
+  __threadfence();
+  named_bar(1, kNumWorkers);
+  if (wt == 0) {
+    st_release(&B.norm_flag[tb], p.epoch);
+    if (dynamic_mode(p)) {
+      const Clock c0{~0ull, p.ws.status, p.ws.status_host};
+      queue_push(queue_of(p), p.NC, [&](int i) { return task_enc(TK_ROUTER, blk, tb, i); }, c0);
+    }
+  }
+}
+
+// Router partial logits of token block tb over H-chunk c, on mma.sync
+// (a [32 x HC] x [HC x E] contraction; logits are fp32).  In the chain the
+// input is the normalised row split as hi + lo bf16 parts (two MMAs).
+__device__ void task_router(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
+  const int blk = t.blk, tb = t.a, ch = t.b;
+  const BlockWs& B = p.ws.blk[blk];
+  if (p.logits_in == nullptr) {
+    const bool split = p.use_norm != 0;
+    const __nv_bfloat16* X = split ? p.ws.xn : p.x;
+    const __nv_bfloat16* Wg = p.gate_w[blk];
+    const int E = p.E, H = p.H, ldw = E + 8, ldx = kRouterKStep + 8;
+    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(simt);       // [2 buf][2 hi/lo][32][40]
+    __nv_bfloat16* wsm = xs + 4 * kTB * ldx;                          // [2][32][E+8]
+    const int h0 = ch * p.HC, nks = p.HC / kRouterKStep;
+    const int ww = wt >> 5, lane = wt & 31;
+    auto load = [&](int ks, int buf) {
+      if (wt < kTB * 4 * (split ? 2 : 1)) {
+        const int part = wt >> 7, r = (wt >> 2) & 31, q = wt & 3;
+        const int tok = tb * kTB + r;
+        const __nv_bfloat16* src = (part ? p.ws.xn_lo : X) +
+            static_cast<size_t>(tok < p.T ? tok : p.T - 1) * H + h0 + ks * kRouterKStep + q * 8;
+        cp_async16(xs + ((buf * 2 + part) * kTB + r) * ldx + q * 8, src, tok < p.T ? 16 : 0);
+      }
+      const int per_row = E / 8;
+      for (int i = wt; i < kRouterKStep * per_row; i += kNumWorkers) {
+        const int r = i / per_row, q = i - r * per_row;
+        const __nv_bfloat16* src = Wg + static_cast<size_t>(h0 + ks * kRouterKStep + r) * E + q * 8;
+        cp_async16(wsm + (buf * kRouterKStep + r) * ldw + q * 8, src, 16);
+      }
+      cp_async_commit();
+    };
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    const int mt = ww & 1, ng = ww >> 1, n8 = E / 8;
+    load(0, 0);
+    for (int ks = 0; ks < nks; ++ks) {
+      if (ks + 1 < nks) {
+        load(ks + 1, (ks + 1) & 1);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      named_bar(1, kNumWorkers);
+      const int buf = ks & 1;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        uint32_t a0, a1, a2, a3, l0 = 0, l1 = 0, l2 = 0, l3 = 0;
+        ldmatrix_x4(smem_u32(xs + (buf * 2 * kTB + mt * 16 + (lane & 15)) * ldx + kk * 16 + (lane >> 4) * 8),
+                    a0, a1, a2, a3);
+        if (split)
+          ldmatrix_x4(smem_u32(xs + ((buf * 2 + 1) * kTB + mt * 16 + (lane & 15)) * ldx + kk * 16 +
+                               (lane >> 4) * 8),
+                      l0, l1, l2, l3);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int j = ng + 4 * i;
+          if (j < n8) {
+            uint32_t b0, b1;
+            ldmatrix_x2_trans(smem_u32(wsm + (buf * kRouterKStep + kk * 16 + (lane & 15)) * ldw + j * 8),
+                              b0, b1);
+            mma_bf16_16816(acc[i], a0, a1, a2, a3, b0, b1);
+            if (split) mma_bf16_16816(acc[i], l0, l1, l2, l3, b0, b1);
+          }
+        }
+      }
+      named_bar(1, kNumWorkers);
+    }
+    const int g = lane >> 2, tq = lane & 3;
+    float* part = B.partial + static_cast<size_t>(ch) * p.T_pad * E;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int j = ng + 4 * i;
+      if (j < n8) {
+        const int e = j * 8 + 2 * tq;
+        const int t0 = tb * kTB + mt * 16 + g;
+        if (t0 < p.T) {
+          part[static_cast<size_t>(t0) * E + e] = acc[i][0];
+          part[static_cast<size_t>(t0) * E + e + 1] = acc[i][1];
+        }
+        if (t0 + 8 < p.T) {
+          part[static_cast<size_t>(t0 + 8) * E + e] = acc[i][2];
+          part[static_cast<size_t>(t0 + 8) * E + e + 1] = acc[i][3];
+        }
+      }
+    }
+  }
+  __threadfence();
+  named_bar(1, kNumWorkers);
+  if (wt == 0) {
+    const int arrived = atom_add_acq_rel(&B.ev_rblk[tb], 1) + 1;
+    if (arrived == p.NC && dynamic_mode(p)) {
+      const Clock c0{~0ull, p.ws.status, p.ws.status_host};
+      queue_push(queue_of(p), 1, [&](int) { return task_enc(TK_TOPK, blk, tb, 0); }, c0);
+    }
+  }
+}
+
+// Top-k over the summed logits of token block tb; ties go to the lower id;
+// weights are the softmax over the k selected logits.
+__device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
+  const int blk = t.blk, tb = t.a;
+  const BlockWs& B = p.ws.blk[blk];
+  const int E = p.E, k = p.k, ww = wt >> 5, lane = wt & 31;
+  int* s_cnt = reinterpret_cast<int*>(simt);
+  for (int i = wt; i < E; i += kNumWorkers) s_cnt[i] = 0;
+  named_bar(1, kNumWorkers);
+  const float* bias = p.bias[blk];
+  for (int r = ww; r < kTB; r += 8) {
+    const int tok = tb * kTB + r;
+    if (tok >= p.T) break;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = 32 * i + lane;
+      v[i] = -INFINITY;
+      if (e < E) {
+        float s;
+        if (p.logits_in) {
+          s = p.logits_in[static_cast<size_t>(tok) * E + e];
+        } else {
+          s = 0.f;
+          for (int c = 0; c < p.NC; ++c)
+            s += B.partial[(static_cast<size_t>(c) * p.T_pad + tok) * E + e];
+          if (bias) s += bias[e];
+        }
+        B.logits[static_cast<size_t>(tok) * E + e] = s;
+        v[i] = s;
+      }
+    }
+    unsigned taken = 0;
+    float my_v = -INFINITY;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = 32 * i + lane;
+        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        my_v = bv;
+        my_id = bi;
+      }
+    }
+    const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
+    const float ex = lane < k ? expf(my_v - v0) : 0.f;
+    float z = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    if (lane < k) {
+      B.ids[tok * k + lane] = my_id;
+      B.wts[tok * k + lane] = ex / z;
+      atomicAdd(&s_cnt[my_id], 1);
+    }
+  }
+  named_bar(1, kNumWorkers);
+  for (int i = wt; i < E; i += kNumWorkers) B.blk_cnt[tb * E + i] = s_cnt[i];
+  __threadfence();
+  named_bar(1, kNumWorkers);
+  if (wt == 0) {
+    st_relaxed(&B.ev_rblk[tb], 0);  // consumed: re-armed for the next call
+    const int arrived = atom_add_acq_rel(B.ev_route, 1) + 1;
+    if (arrived == p.nb && dynamic_mode(p)) {
+      const Clock c0{~0ull, p.ws.status, p.ws.status_host};
+      queue_push(queue_of(p), 1, [&](int) { return task_enc(TK_SCAN, blk, 0, 0); }, c0);
+    }
+  }
+}
+
+// counts / exp_indptr / per-block offsets / expert chunks / event inits.
+__device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
+  const int blk = t.blk;
+  const BlockWs& B = p.ws.blk[blk];
+  const int E = p.E, nb = p.nb;
+  int* tmp = reinterpret_cast<int*>(simt);
+  int cnt = 0;
+  if (wt < E)
+    for (int tb = 0; tb < nb; ++tb) cnt += B.blk_cnt[tb * E + wt];
+  const int nch = (cnt + kBT - 1) / kBT;
+  const int row0 = workers_excl_scan(cnt, tmp, wt);
+  const int ch0 = workers_excl_scan(nch, tmp + 16, wt);
+  if (wt < E) {
+    B.counts[wt] = cnt;
+    B.exp_indptr[wt] = row0;
+    B.chunk_indptr[wt] = ch0;
+    if (wt == E - 1) {
+      B.exp_indptr[E] = row0 + cnt;
+      B.chunk_indptr[E] = ch0 + nch;
+      B.meta[0] = ch0 + nch;
+      B.meta[1] = (ch0 + nch) * p.NT_gu;
+      B.meta[2] = (ch0 + nch) * p.NT_dn;
+    }
+    int run = row0;
+    for (int tb = 0; tb < nb; ++tb) {
+      B.blk_off[tb * E + wt] = run;
+      run += B.blk_cnt[tb * E + wt];
+    }
+    for (int c = 0; c < nch; ++c) {
+      const int chn = ch0 + c;
+      B.chunk_expert[chn] = wt;
+      B.chunk_row0[chn] = row0 + c * kBT;
+      B.chunk_rows[chn] = min(kBT, cnt - c * kBT);
+      B.ev_act[chn] = p.NT_gu;
+      B.ev_down[chn] = p.NT_dn;
+    }
+    // Data-dependent event update: expert e waits for its counts[e] rows.
+    const int extra = ((p.debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT) && wt == p.debug_arg) ? 1 : 0;
+    B.ev_expert[wt] = cnt + extra;
+  }
+  for (int tb = wt; tb < nb; tb += kNumWorkers)
+    B.ev_tok[tb] = p.k * (min(p.T, tb * kTB + kTB) - tb * kTB);
+  __threadfence();
+  named_bar(1, kNumWorkers);
+  if (wt == 0) {
+    st_relaxed(B.ev_route, 0);
+    const bool dyn = dynamic_mode(p);
+    if (dyn) {
+      const int n_chunks = B.meta[0];
+      const int blk_tasks = (p.use_norm ? nb : 0) + p.n_router + nb + 1 + nb +
+                            n_chunks * (p.NT_gu + p.NT_dn) + nb;
+      const int acc = (blk == 0 ? 0 : *p.ws.qacc) + blk_tasks;
+      *p.ws.qacc = acc;
+      if (blk == p.n_blocks - 1) *p.ws.qtotal = acc;
+    }
+    // Re-arm the other parity's queue for the next call (whatever its mode).
+    const int other = (p.epoch + 1) & 1;
+    *p.ws.qhead[other] = 0;
+    *p.ws.qtail[other] = 0;
+    __threadfence();
+    st_release(B.plan_flag, p.epoch);
+    if (dyn) {
+      if (blk == p.n_blocks - 1) st_release(p.ws.qtotal_flag, p.epoch);
+      const Clock c0{~0ull, p.ws.status, p.ws.status_host};
+      queue_push(queue_of(p), nb, [&](int i) { return task_enc(TK_PERM, blk, i, 0); }, c0);
+    }
+  }
+}
+
+// Writes the rows of token block tb into x_perm at exp_indptr[e] + rank.
+__device__ void task_perm(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
+  const int blk = t.blk, tb = t.a;
+  const BlockWs& B = p.ws.blk[blk];
+  const int E = p.E, k = p.k, ww = wt >> 5, lane = wt & 31;
+  int* s_run = reinterpret_cast<int*>(simt);
+  int* s_slot = s_run + kMaxE;
+  for (int i = wt; i < E; i += kNumWorkers) s_run[i] = B.blk_off[tb * E + i];
+  named_bar(1, kNumWorkers);
+  const int t0 = tb * kTB, ntok = min(kTB, p.T - t0);
+  if (ww == 0) {
+    // Ranks in ascending token order; one token's k experts are distinct.
+    for (int r = 0; r < ntok; ++r) {
+      const int tok = t0 + r;
+      if (lane < k) {
+        const int e = B.ids[tok * k + lane];
+        const int row = s_run[e];
+        s_run[e] = row + 1;
+        B.pos[tok * k + lane] = row;
+        B.row_token[row] = tok;
+        s_slot[r * k + lane] = row;
+      }
+      __syncwarp();
+    }
+  }
+  named_bar(1, kNumWorkers);
+  const __nv_bfloat16* src = p.use_norm ? p.ws.xn : p.x;
+  const int nslots = ntok * k, n8 = p.H / 8;
+  for (int s = ww; s < nslots; s += 8) {
+    const int tok = t0 + s / k, row = s_slot[s];
+    const uint4* sr = reinterpret_cast<const uint4*>(src + static_cast<size_t>(tok) * p.H);
+    uint4* dr = reinterpret_cast<uint4*>(p.ws.x_perm + static_cast<size_t>(row) * p.H);
+    for (int v = lane; v < n8; v += 32) dr[v] = sr[v];
+  }
+  fence_proxy_async_global();  // x_perm is read next by TMA (async proxy)
+  __threadfence();
+  named_bar(1, kNumWorkers);
+  const Clock c0{~0ull, p.ws.status, p.ws.status_host};
+  for (int e = wt; e < E; e += kNumWorkers) {
+    const int n = B.blk_cnt[tb * E + e];
+    if (n > 0) {
+      const int left = notify(&B.ev_expert[e], n);
+      if (left == 0 && dynamic_mode(p)) {
+        // Expert e is ready: fire the tiles of rows [exp_indptr[e], exp_indptr[e+1]).
+        const int c0i = B.chunk_indptr[e], nch = B.chunk_indptr[e + 1] - c0i;
+        const int NT = p.NT_gu;
+        queue_push(queue_of(p), nch * NT,
+                   [&](int i) { return task_enc(TK_GU, blk, c0i + i / NT, i % NT); }, c0);
+      }
+    }
+  }
+}
+
+// out[t] = sum_j w[t,j] * y[pos[t,j]] (j ascending, fp32) (+ x[t] in the chain).
+__device__ void task_comb(const MegaParams& p, const Task& t, int wt) {
+  const int blk = t.blk, tb = t.a;
+  const BlockWs& B = p.ws.blk[blk];
+  const int k = p.k, ww = wt >> 5, lane = wt & 31, n8 = p.H / 8;
+  const bool last = blk == p.n_blocks - 1;
+  float* resid_out = p.ws.resid + static_cast<size_t>(blk) * p.T_max * p.H;  // when !last
+  for (int r = ww; r < kTB; r += 8) {
+    const int tok = tb * kTB + r;
+    if (tok >= p.T) break;
+    const int pj = lane < k ? B.pos[tok * k + lane] : 0;
+    const float wj = lane < k ? B.wts[tok * k + lane] : 0.f;
+    int prow[kMaxK];
+    float pw[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      prow[j] = __shfl_sync(0xffffffffu, pj, j);
+      pw[j] = __shfl_sync(0xffffffffu, wj, j);
+    }
+    for (int c = lane; c < n8; c += 32) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k) {
+          const float4* yr = reinterpret_cast<const float4*>(
+              p.ws.y_perm + static_cast<size_t>(prow[j]) * p.H + 8 * c);
+          const float4 y0 = yr[0], y1 = yr[1];
+          acc[0] += pw[j] * y0.x;
+          acc[1] += pw[j] * y0.y;
+          acc[2] += pw[j] * y0.z;
+          acc[3] += pw[j] * y0.w;
+          acc[4] += pw[j] * y1.x;
+          acc[5] += pw[j] * y1.y;
+          acc[6] += pw[j] * y1.z;
+          acc[7] += pw[j] * y1.w;
+        }
+      }
+      if (p.use_norm) {
+        float x[8];
+        load_block_input8(p, blk, tok, c, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += x[i];
+      }
+      if (last && p.out_bf16) {
+        reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(tok) * p.H)[c] =
+            f32_to_bf16x8(acc);
+      } else {
+        float* row = last ? static_cast<float*>(p.out) : resid_out;
+        float4* d = reinterpret_cast<float4*>(row + static_cast<size_t>(tok) * p.H + 8 * c);
+        d[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        d[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      }
+    }
+  }
+  __threadfence();
+  named_bar(1, kNumWorkers);
+  if (wt == 0) {
+    if (p.use_norm) st_release(&B.comb_flag[tb], p.epoch);
+    if (dynamic_mode(p) && blk + 1 < p.n_blocks) {
+      const Clock c0{~0ull, p.ws.status, p.ws.status_host};
+      queue_push(queue_of(p), 1, [&](int) { return task_enc(TK_NORM, blk + 1, tb, 0); }, c0);
+    }
+  }
+}
+
+// TMEM epilogue of a GU or DN tile, then its notify.
+__device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, uint8_t* simt,
+                                   const Task& t, uint32_t& gemm_i, const Clock& clk, int wt,
+                                   uint32_t iter) {
+  const int acc = gemm_i & 1;
+  const uint32_t aph = (gemm_i >> 1) & 1;
+  ++gemm_i;
+  int* flag = &c->wflag[iter & 1];
+  if (wt == 0) *flag = mbar_wait(&c->tfull[acc], aph, clk, 230) ? 1 : 0;
+  named_bar(1, kNumWorkers);
+  const bool ok = *flag != 0;
+  tc_fence_after();
+  const int w = warp_id(), q = w & 3, h = (w - kWorkerWarp0) >> 2, lane = lane_id();
+  const int i128 = q * 32 + lane;
+  float* U = reinterpret_cast<float*>(epi + h * kEpiHalfBytes);                     // [2][16][32]
+  __nv_bfloat16* S = reinterpret_cast<__nv_bfloat16*>(epi + h * kEpiHalfBytes + 4096);  // [16][128]
+  const uint32_t tbase = c->tmem_base + acc * kAccCols + (static_cast<uint32_t>(32 * q) << 16);
+  const int ncb = (t.rows + 15) >> 4;
+  const BlockWs& B = p.ws.blk[t.blk];
+  if (ok) {
+    if (t.type == TK_GU) {
+      for (int cb = h; cb < ncb; cb += 2) {
+        float v[16];
+        tmem_ld16(tbase + cb * 16, v);
+        if (q >= 2) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) U[((q - 2) * 16 + i) * 32 + lane] = v[i];
+        }
+        named_bar(2 + h, 128);
+        if (q < 2) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float gte = v[i];
+            const float up = U[(q * 16 + i) * 32 + lane];
+            const float a = gte / (1.0f + __expf(-gte)) * up;
+            S[i * 64 + 32 * q + lane] = __float2bfloat16_rn(a);
+          }
+        }
+        named_bar(2 + h, 128);
+        const int tok = cb * 16 + (i128 >> 3), chunk = i128 & 7;
+        if (tok < t.rows) {
+          const uint4 val = *reinterpret_cast<const uint4*>(S + (i128 >> 3) * 64 + chunk * 8);
+          *reinterpret_cast<uint4*>(p.ws.act + static_cast<size_t>(t.row0 + tok) * p.I +
+                                    t.b * kGuRows + chunk * 8) = val;
+        }
+        named_bar(2 + h, 128);
+      }
+    } else {
+      float* S32 = reinterpret_cast<float*>(epi + h * kEpiHalfBytes);  // [16][128] fp32
+      for (int cb = h; cb < ncb; cb += 2) {
+        float v[16];
+        tmem_ld16(tbase + cb * 16, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) S32[i * 128 + 32 * q + lane] = v[i];
+        named_bar(2 + h, 128);
+#pragma unroll
+        for (int rep = 0; rep < 4; ++rep) {
+          const int idx = i128 + 128 * rep;
+          const int tok = cb * 16 + (idx >> 5), chunk = idx & 31;
+          if (tok < t.rows) {
+            const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
+            *reinterpret_cast<float4*>(p.ws.y_perm + static_cast<size_t>(t.row0 + tok) * p.H +
+                                       t.b * kDnRows + chunk * 4) = val;
+          }
+        }
+        named_bar(2 + h, 128);
+      }
+    }
+  }
+  fence_proxy_async_global();  // act is read next by TMA
+  __threadfence();
+  tc_fence_before();
+  named_bar(1, kNumWorkers);
+  if (wt == 0) mbar_arrive(&c->tempty[acc]);
+  const Clock c0{~0ull, p.ws.status, p.ws.status_host};
+  if (t.type == TK_GU) {
+    if (wt == 0) {
+      const int left = notify(&B.ev_act[t.a], 1);
+      if (left == 0 && dynamic_mode(p))
+        queue_push(queue_of(p), p.NT_dn, [&](int i) { return task_enc(TK_DN, t.blk, t.a, i); }, c0);
+    }
+  } else {
+    int* fin = &c->wflag[(iter & 1) ^ 1];
+    if (wt == 0) *fin = notify(&B.ev_down[t.a], 1) == 0 ? 1 : 0;
+    named_bar(1, kNumWorkers);
+    if (*fin) {
+      // Finisher of the chunk: notify each token block by its number of rows.
+      int* s_tb = reinterpret_cast<int*>(simt);
+      for (int r = wt; r < t.rows; r += kNumWorkers) s_tb[r] = B.row_token[t.row0 + r] / kTB;
+      named_bar(1, kNumWorkers);
+      for (int r = wt; r < t.rows; r += kNumWorkers) {
+        const int tb = s_tb[r];
+        if (r == 0 || s_tb[r - 1] != tb) {
+          int e = r + 1;
+          while (e < t.rows && s_tb[e] == tb) ++e;
+          const int left = notify(&B.ev_tok[tb], e - r);
+          if (left == 0 && dynamic_mode(p))
+            queue_push(queue_of(p), 1, [&](int) { return task_enc(TK_COMB, t.blk, tb, 0); }, c0);
+        }
+      }
+    }
+  }
+}
+
+__device__ void run_workers(const MegaParams& p, Ctrl* c, uint8_t* simt, uint8_t* epi,
+                            const Clock& clk) {
+  const int wt = threadIdx.x - kWorkerWarp0 * 32;
+  uint32_t gemm_i = 0;
+  for (uint32_t ri = 0;; ++ri) {
+    Task* slot = &c->wtask[ri & 1];
+    if (wt == 0) {
+      const int r = ri % kRing;
+      if (mbar_wait(&c->rfull[r], (ri / kRing) & 1, clk, 210)) {
+        *slot = c->ring[r];
+      } else {
+        slot->type = TK_TERM;
+      }
+      mbar_arrive(&c->rempty[r]);
+    }
+    named_bar(1, kNumWorkers);
+    const Task t = *slot;
+    switch (t.type) {
+      case TK_NORM: task_norm(p, t, wt); break;
+      case TK_ROUTER: task_router(p, t, simt, wt); break;
+      case TK_TOPK: task_topk(p, t, simt, wt); break;
+      case TK_SCAN: task_scan(p, t, simt, wt); break;
+      case TK_PERM: task_perm(p, t, simt, wt); break;
+      case TK_GU:
+      case TK_DN: task_gemm_epilogue(p, c, epi, simt, t, gemm_i, clk, wt, ri); break;
+      case TK_COMB: task_comb(p, t, wt); break;
+      default: break;
+    }
+    if (t.type == TK_TERM) break;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA producer and tcgen05 issuer
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool ring_take(Ctrl* c, uint32_t& ri, Task& t, const Clock& clk,
+                                          int where) {
+  const int r = ri % kRing;
+  const bool ok = mbar_wait(&c->rfull[r], (ri / kRing) & 1, clk, where);
+  if (ok) t = c->ring[r];
+  mbar_arrive(&c->rempty[r]);
+  ++ri;
+  return ok;
+}
+
+__device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock& clk) {
+  uint32_t ri = 0, it = 0;
+  for (;;) {
+    Task t;
+    if (!ring_take(c, ri, t, clk, 220) || t.type == TK_TERM) break;
+    if (t.type != TK_GU && t.type != TK_DN) continue;
+    const bool gu = t.type == TK_GU;
+    const CUtensorMap* ta = gu ? &p.tm_wgu[t.blk] : &p.tm_wd[t.blk];
+    const CUtensorMap* tb = gu ? &p.tm_xperm : &p.tm_act;
+    const int KB = (gu ? p.H : p.I) / kBK;
+    const int nb16 = (t.rows + 15) >> 4;
+    int rowA0, rowA1;
+    if (gu) {
+      rowA0 = t.e * 2 * p.I + t.b * kGuRows;  // gate rows
+      rowA1 = rowA0 + p.I;                     // matching up rows
+    } else {
+      rowA0 = t.e * p.H + t.b * kDnRows;
+      rowA1 = rowA0 + 64;
+    }
+    const uint32_t bytes = kStageABytes + nb16 * 16 * kBK * 2;
+    fence_proxy_async_global();
+    for (int kb = 0; kb < KB; ++kb, ++it) {
+      const int s = it % kStages;
+      if (!mbar_wait(&c->empty[s], ((it / kStages) & 1) ^ 1, clk, 221)) return;
+      uint8_t* sa = base + s * kStageBytes;
+      uint8_t* sb = sa + kStageABytes;
+      mbar_arrive_expect_tx(&c->full[s], bytes);
+      tma_load_2d(sa, ta, &c->full[s], kb * kBK, rowA0);
+      tma_load_2d(sa + kStageABytes / 2, ta, &c->full[s], kb * kBK, rowA1);
+      for (int i = 0; i < nb16; ++i)
+        tma_load_2d(sb + i * 16 * kBK * 2, tb, &c->full[s], kb * kBK, t.row0 + 16 * i);
+    }
+  }
+}
+
+__device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock& clk) {
+  uint32_t ri = 0, it = 0, tc = 0;
+  const uint32_t tmem = c->tmem_base;
+  for (;;) {
+    Task t;
+    if (!ring_take(c, ri, t, clk, 240) || t.type == TK_TERM) break;
+    if (t.type != TK_GU && t.type != TK_DN) continue;
+    const int acc = tc & 1;
+    if (!mbar_wait(&c->tempty[acc], ((tc >> 1) & 1) ^ 1, clk, 241)) return;
+    tc_fence_after();
+    const uint32_t d = tmem + acc * kAccCols;
+    const int npad = (t.rows + 15) & ~15;
+    const uint32_t idesc = idesc_bf16_f32(128, npad);
+    const int KB = (t.type == TK_GU ? p.H : p.I) / kBK;
+    for (int kb = 0; kb < KB; ++kb, ++it) {
+      const int s = it % kStages;
+      if (!mbar_wait(&c->full[s], (it / kStages) & 1, clk, 242)) return;
+      tc_fence_after();
+      const uint64_t ad = desc_kmajor_sw128(smem_u32(base + s * kStageBytes));
+      const uint64_t bd = desc_kmajor_sw128(smem_u32(base + s * kStageBytes + kStageABytes));
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk)
+        umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+      umma_commit(&c->empty[s]);  // stage free once these MMAs have read it
+    }
+    umma_commit(&c->tfull[acc]);  // accumulator ready
+    ++tc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Scheduler
+// ---------------------------------------------------------------------------
+struct RingWriter {
+  Ctrl* c;
+  uint32_t i;
+  __device__ bool emit(const Task& t, const Clock& clk) {
+    const int r = i % kRing;
+    if (!mbar_wait(&c->rempty[r], ((i / kRing) & 1) ^ 1, clk, 200)) return false;
+    c->ring[r] = t;
+    mbar_arrive(&c->rfull[r]);
+    ++i;
+    return true;
+  }
+};
+
+__device__ __forceinline__ Task make_task(int type, int blk, int a, int b) {
+  Task t;
+  t.type = type;
+  t.blk = blk;
+  t.a = a;
+  t.b = b;
+  t.e = t.row0 = t.rows = t.pad = 0;
+  return t;
+}
+
+__device__ __forceinline__ void resolve_chunk(const MegaParams& p, Task& t) {
+  const BlockWs& B = p.ws.blk[t.blk];
+  t.e = B.chunk_expert[t.a];
+  t.row0 = B.chunk_row0[t.a];
+  t.rows = B.chunk_rows[t.a];
+}
+
+__device__ void sched_static(const MegaParams& p, Ctrl* c, const Clock& clk) {
+  RingWriter rw{c, 0};
+  const int G = gridDim.x, cta = blockIdx.x;
+  auto in = [&](int stage) { return stage >= p.stage_lo && stage <= p.stage_hi; };
+  bool ok = true;
+  for (int blk = 0; blk < p.n_blocks && ok; ++blk) {
+    const BlockWs& B = p.ws.blk[blk];
+    if (p.use_norm && in(TK_NORM)) {
+      for (int tb = cta; tb < p.nb && ok; tb += G) {
+        if (blk > 0) ok = wait_flag(&p.ws.blk[blk - 1].comb_flag[tb], p.epoch, clk, TK_NORM, tb);
+        ok = ok && rw.emit(make_task(TK_NORM, blk, tb, 0), clk);
+      }
+    }
+    if (in(TK_ROUTER)) {
+      for (int i = cta; i < p.n_router && ok; i += G) {
+        const int tb = i / p.NC;
+        if (p.use_norm) ok = wait_flag(&B.norm_flag[tb], p.epoch, clk, TK_ROUTER, tb);
+        ok = ok && rw.emit(make_task(TK_ROUTER, blk, tb, i % p.NC), clk);
+      }
+    }
+    if (in(TK_TOPK)) {
+      for (int tb = cta; tb < p.nb && ok; tb += G) {
+        ok = wait_geq(&B.ev_rblk[tb], p.NC, clk, TK_TOPK, tb);
+        ok = ok && rw.emit(make_task(TK_TOPK, blk, tb, 0), clk);
+      }
+    }
+    if (in(TK_SCAN) && cta == blk % G && ok) {
+      ok = wait_geq(B.ev_route, p.nb, clk, TK_SCAN, 0);
+      ok = ok && rw.emit(make_task(TK_SCAN, blk, 0, 0), clk);
+    }
+    if (p.stage_hi < TK_PERM || !ok) continue;
+    ok = wait_flag(B.plan_flag, p.epoch, clk, TK_PERM, 0);
+    if (!ok) break;
+    const int n_chunks = ld_acquire(&B.meta[0]);
+    if (in(TK_PERM))
+      for (int tb = cta; tb < p.nb && ok; tb += G) ok = rw.emit(make_task(TK_PERM, blk, tb, 0), clk);
+    if (in(TK_GU)) {
+      const int n = n_chunks * p.NT_gu;
+      for (int g = cta; g < n && ok; g += G) {
+        Task t = make_task(TK_GU, blk, g / p.NT_gu, g % p.NT_gu);
+        resolve_chunk(p, t);
+        ok = wait_zero(&B.ev_expert[t.e], clk, TK_GU, t.e);
+        ok = ok && rw.emit(t, clk);
+      }
+    }
+    if (in(TK_DN)) {
+      const int n = n_chunks * p.NT_dn;
+      for (int d = cta; d < n && ok; d += G) {
+        Task t = make_task(TK_DN, blk, d / p.NT_dn, d % p.NT_dn);
+        ok = wait_zero(&B.ev_act[t.a], clk, TK_DN, t.a);
+        if (ok) resolve_chunk(p, t);
+        ok = ok && rw.emit(t, clk);
+      }
+    }
+    if (in(TK_COMB)) {
+      for (int tb = cta; tb < p.nb && ok; tb += G) {
+        ok = wait_zero(&B.ev_tok[tb], clk, TK_COMB, tb);
+        ok = ok && rw.emit(make_task(TK_COMB, blk, tb, 0), clk);
+      }
+    }
+  }
+  rw.emit(make_task(TK_TERM, 0, 0, 0), clk);
+}
+
+__device__ void sched_dynamic(const MegaParams& p, Ctrl* c, const Clock& clk) {
+  RingWriter rw{c, 0};
+  const QueueView q = queue_of(p);
+  for (;;) {
+    const int idx = atom_add_relaxed(q.head, 1);
+    uint32_t desc = 0;
+    bool have = false;
+    if (idx < q.n_seed) {
+      desc = p.use_norm ? task_enc(TK_NORM, 0, idx, 0)
+                        : task_enc(TK_ROUTER, 0, idx / p.NC, idx % p.NC);
+      have = true;
+    } else {
+      unsigned long long v = 0;
+      const bool got = spin_until(
+          [&] {
+            if (idx < q.cap) {
+              v = ld_acquire(&q.slots[idx]);
+              if (static_cast<unsigned>(v >> 32) == p.epoch) return true;
+            }
+            if (ld_acquire(p.ws.qtotal_flag) == p.epoch && idx >= ld_acquire(p.ws.qtotal)) {
+              v = 0;
+              return true;
+            }
+            return false;
+          },
+          clk, DERR_TIMEOUT_QUEUE, 0, idx);
+      if (!got) break;
+      if (static_cast<unsigned>(v >> 32) == p.epoch) {
+        desc = static_cast<uint32_t>(v);
+        have = true;
+      }
+    }
+    if (!have) break;  // every task of the call has been popped
+    Task t = make_task(task_type(desc), task_blk(desc), task_a(desc), task_b(desc));
+    if (t.type == TK_GU || t.type == TK_DN) resolve_chunk(p, t);
+    if (!rw.emit(t, clk)) break;
+  }
+  rw.emit(make_task(TK_TERM, 0, 0, 0), clk);
+}
+
+// ---------------------------------------------------------------------------
+// Kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_constant__ MegaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* simt = base + kStages * kStageBytes;
+  uint8_t* epi = simt + kSimtBytes;
+  Ctrl* c = reinterpret_cast<Ctrl*>(epi + 2 * kEpiHalfBytes);
+  const Clock clk{globaltimer_ns() + p.timeout_ns, p.ws.status, p.ws.status_host};
+  const int w = warp_id();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&c->full[s], 1);
+      mbar_init(&c->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&c->tfull[a], 1);
+      mbar_init(&c->tempty[a], 1);
+    }
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(&c->rfull[r], 1);
+      mbar_init(&c->rempty[r], kRingConsumers);
+    }
+    mbar_fence_init();
+  }
+  if (w == kWarpTma && lane_id() == 0 && p.stage_hi >= TK_GU) {
+    for (int b = 0; b < p.n_blocks; ++b) {
+      tma_prefetch_desc(&p.tm_wgu[b]);
+      tma_prefetch_desc(&p.tm_wd[b]);
+    }
+    tma_prefetch_desc(&p.tm_xperm);
+    tma_prefetch_desc(&p.tm_act);
+  }
+  if (w == kWarpMma) {
+    tmem_alloc(&c->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (w == kWarpSched) {
+    if (lane_id() == 0) {
+      if (p.mode == ETC_SCHED_DYNAMIC)
+        sched_dynamic(p, c, clk);
+      else
+        sched_static(p, c, clk);
+    }
+  } else if (w == kWarpTma) {
+    if (lane_id() == 0) run_producer(p, c, base, clk);
+  } else if (w == kWarpMma) {
+    if (lane_id() == 0) run_mma(p, c, base, clk);
+  } else if (w >= kWorkerWarp0) {
+    run_workers(p, c, simt, epi, clk);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (w == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(c->tmem_base, kTmemCols);
+  }
+}
+
+cudaError_t megakernel_configure() {
+  return cudaFuncSetAttribute(etc_moe_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemBytes);
+}
+
+cudaError_t launch_megakernel(const MegaParams& p, int grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: spin-waits are safe
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, etc_moe_megakernel, p);
+}
+
+int megakernel_occupancy() {
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, etc_moe_megakernel, kThreads,
+                                                    kSmemBytes) != cudaSuccess)
+    return 0;
+  return occ;
+}
+
+}  // namespace etc
