@@ -212,6 +212,29 @@ int etc_splitk_rowsum_ex(void* stream, const float* A, long long n_rows, long lo
 /* Status of the last split-K calls on the current device (after a sync). */
 int etc_splitk_check(void);
 
+/*
+ * etc_splitk_rowsum for callers that must not allocate device memory: code
+ * running while a CUDA graph is being captured, code inside an allocator or
+ * memory-pool callback that may not re-enter the allocator, and runtimes that
+ * reserve all device memory up front.  Same arguments, result and tolerance
+ * as etc_splitk_rowsum; the paper has no counterpart of this entry point.
+ *
+ * Its scratch (partial sums, per-row counters, queue counters, status) is a
+ * fixed array of about 1.25 MiB compiled into the library: every GPU that
+ * loads the library holds it until the process exits.  Limits:
+ * n_rows <= 65536 and n_rows * n_split <= 262144; larger calls return
+ * ETC_ERR_INVALID (use etc_splitk_rowsum instead).  Nothing is allocated:
+ * no cudaMalloc, cudaFree or allocating library routine; each call clears the
+ * part of the array that must start at zero with an async memset on `stream`.
+ * The first call on a device looks up the array's device address (a one-time
+ * set-up, with that device current); make that first call before any stream
+ * capture.  All calls on a device share the one array, so calls that overlap
+ * on the GPU (other streams, other threads) race: order them on one stream.
+ * A device wait that gives up (2 s) leaves the affected C rows unwritten.
+ */
+int etc_splitk_rowsum_noalloc(void* stream, const float* A, long long n_rows, long long n_cols,
+                              int n_split, float* C, int sched);
+
 /* Number of kernels launched by the library so far in this process. */
 long long etc_launch_count(void);
 

@@ -30,7 +30,7 @@ EXPORTED = [
     "etc_moe_plan", "etc_moe_forward", "etc_moe_forward_unfused", "etc_moe_route_from_logits",
     "etc_moe_debug_routing", "etc_moe_debug_buffer", "etc_chain_forward", "etc_plan_check", "etc_plan_reset",
     "etc_plan_stats", "etc_plan_destroy", "etc_splitk_rowsum", "etc_splitk_rowsum_ex",
-    "etc_splitk_check", "etc_launch_count", "etc_last_error",
+    "etc_splitk_check", "etc_splitk_rowsum_noalloc", "etc_launch_count", "etc_last_error",
 ]
 
 
@@ -83,6 +83,7 @@ def load(build_if_missing: bool = True):
     L.etc_splitk_rowsum.argtypes = [P, P, LL, LL, I, P, I]
     L.etc_splitk_rowsum_ex.argtypes = [P, P, LL, LL, I, P, I, ctypes.c_ulonglong, ctypes.c_uint, LL]
     L.etc_splitk_check.argtypes = []
+    L.etc_splitk_rowsum_noalloc.argtypes = [P, P, LL, LL, I, P, I]
     L.etc_launch_count.restype = LL
     L.etc_last_error.restype = ctypes.c_char_p
     for name in EXPORTED:
@@ -242,3 +243,10 @@ def etc_last_error() -> str:
 
 def etc_plan_destroy(plan: Plan):
     plan.close()
+
+
+def etc_splitk_rowsum_noalloc(A, n_split, C, sched=ETC_SCHED_STATIC, stream=None):
+    """Split-K row sum whose scratch is a fixed array inside the library (no allocation)."""
+    n_rows, n_cols = A.shape
+    return _check(load().etc_splitk_rowsum_noalloc(_stream(stream), _ptr(A), n_rows, n_cols,
+                                                   int(n_split), _ptr(C), int(sched)))

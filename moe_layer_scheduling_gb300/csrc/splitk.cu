@@ -344,3 +344,123 @@ int etc_splitk_check(void) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Split-K row sum that allocates nothing.
+//
+// Some callers cannot call cudaMalloc at the moment they need this operation:
+// code running while a CUDA graph is being captured, code inside an allocator
+// or a memory-pool callback that must not re-enter the allocator, and
+// runtimes that reserve all device memory up front and forbid allocation
+// later.  For them the scratch this kernel needs (the per-row partial sums B,
+// the per-row event counters and the queue counters) lives in one fixed-size
+// array in the library's device image instead of a buffer from cudaMalloc.
+// The array exists on every GPU that loads the library and stays there until
+// the process exits.
+// ---------------------------------------------------------------------------
+namespace etc {
+namespace {
+
+constexpr long long kNoAllocMaxRows = 65536;           // n_rows limit
+constexpr long long kNoAllocMaxPartials = 262144;      // n_rows * n_split limit
+constexpr size_t kNoAllocHeader = 256;                 // status + queue counters
+constexpr size_t kNoAllocBytes =
+    kNoAllocHeader + kNoAllocMaxRows * sizeof(int) + kNoAllocMaxPartials * sizeof(float);
+
+// Layout: [DevStatus | head[2] | pad to 256] [ev: int x 65536] [B: float x 262144]
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+struct NoAllocDevice {
+  unsigned char* base = nullptr;  // device address of g_noalloc_scratch on this device
+  unsigned epoch = 0;
+};
+std::mutex g_na_mu;
+NoAllocDevice g_na[64];
+
+}  // namespace
+}  // namespace etc
+
+extern "C" int etc_splitk_rowsum_noalloc(void* stream, const float* A, long long n_rows,
+                                         long long n_cols, int n_split, float* C, int sched) {
+  using namespace etc;
+  clear_error();
+  if (n_rows < 0 || n_cols <= 0 || n_split < 1 || n_split > 64)
+    return set_error(ETC_ERR_INVALID, "splitk_noalloc: bad sizes n_rows=%lld n_cols=%lld n_split=%d",
+                     n_rows, n_cols, n_split);
+  if (n_cols % n_split != 0 || (n_cols / n_split) % 4 != 0 || n_cols / n_split > 16384)
+    return set_error(ETC_ERR_INVALID,
+                     "splitk_noalloc: tile = n_cols/n_split must be a multiple of 4 and <= 16384");
+  if (n_rows > kNoAllocMaxRows || n_rows * n_split > kNoAllocMaxPartials)
+    return set_error(ETC_ERR_INVALID,
+                     "splitk_noalloc: n_rows=%lld, n_rows*n_split=%lld exceed the fixed scratch "
+                     "(at most %lld rows and %lld partial sums); use etc_splitk_rowsum",
+                     n_rows, n_rows * n_split, kNoAllocMaxRows, kNoAllocMaxPartials);
+  if (sched != ETC_SCHED_STATIC && sched != ETC_SCHED_DYNAMIC)
+    return set_error(ETC_ERR_INVALID, "splitk_noalloc: bad sched %d", sched);
+  if (n_rows == 0) return ETC_OK;
+  if (!A || !C || !aligned16(A))
+    return set_error(ETC_ERR_INVALID,
+                     "splitk_noalloc: A and C must be device pointers, A 16-byte aligned");
+  int dev = 0;
+  ETC_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return set_error(ETC_ERR_INVALID, "splitk_noalloc: device %d", dev);
+
+  std::lock_guard<std::mutex> lk(g_na_mu);
+  NoAllocDevice& nd = g_na[dev];
+  if (!nd.base) {
+    // One-time set-up on this device (the current one): the host-side name of
+    // the array is not a device address, so ask the runtime for it.
+    void* ptr = nullptr;
+    ETC_CUDA_TRY(cudaGetSymbolAddress(&ptr, g_noalloc_scratch));
+    ETC_CUDA_TRY(cudaFuncSetAttribute(splitk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kSkSmemBudget + 1024));
+    nd.base = static_cast<unsigned char*>(ptr);
+  }
+  int* ev = reinterpret_cast<int*>(nd.base + kNoAllocHeader);
+  float* B = reinterpret_cast<float*>(nd.base + kNoAllocHeader + kNoAllocMaxRows * sizeof(int));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Status, queue counters and this call's row counters must start at zero;
+  // the array keeps whatever the previous call left there.
+  ETC_CUDA_TRY(cudaMemsetAsync(nd.base, 0, kNoAllocHeader + n_rows * sizeof(int), s));
+
+  SkParams p{};
+  p.A = A;
+  p.C = C;
+  p.B = B;
+  p.ev = ev;
+  p.head = reinterpret_cast<int*>(nd.base + sizeof(DevStatus));
+  p.n_rows = n_rows;
+  p.n_cols = n_cols;
+  p.n_split = n_split;
+  p.tile = static_cast<int>(n_cols / n_split);
+  const int tile_bytes = p.tile * 4;
+  p.R = std::max(1, std::min(kSkMaxRows, 65536 / tile_bytes));
+  p.stage_bytes = p.R * tile_bytes;
+  p.stages = std::max(2, std::min(kSkMaxStages, kSkSmemBudget / p.stage_bytes));
+  p.n_tasks = ((n_rows + p.R - 1) / p.R) * n_split;
+  if (++nd.epoch == 0) nd.epoch = 1;
+  p.epoch = nd.epoch;
+  p.mode = sched;
+  p.timeout_ns = 2000000000ull;
+  p.status = reinterpret_cast<DevStatus*>(nd.base);
+  p.status_host = nullptr;
+  p.fault_row = -1;
+  const size_t smem =
+      ((sizeof(SkCtrl) + 127) / 128) * 128 + static_cast<size_t>(p.stages) * p.stage_bytes;
+  int occ = 0;
+  ETC_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, splitk_kernel, kSkThreads, smem));
+  if (occ < 1) return set_error(ETC_ERR_CUDA, "splitk_noalloc: kernel does not fit on an SM");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sm_count(dev) * occ);
+  cfg.blockDim = dim3(kSkThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ETC_CUDA_TRY(cudaLaunchKernelEx(&cfg, splitk_kernel, p));
+  g_launches.fetch_add(1);
+  return ETC_OK;
+}

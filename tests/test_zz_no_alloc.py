@@ -1,0 +1,52 @@
+"""The split-K entry point that allocates nothing.
+
+It serves callers that cannot call cudaMalloc when they need the operation
+(graph capture, allocator callbacks, runtimes that reserve all memory up
+front).  Its result must match the allocating entry point within the split-K
+tolerance, on two calls in a row (the second reuses the fixed scratch the
+first left behind), and sizes beyond its fixed scratch must be refused.
+This file is collected last on purpose.
+"""
+import numpy as np
+import pytest
+import torch
+
+from moe_layer_scheduling_gb300 import binding as B
+from moe_layer_scheduling_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+REL_TOL = 1e-5  # the split-K tolerance used by the other split-K tests
+
+
+def _close(C, Cref, A):
+    C, Cref = C.double(), Cref.double()
+    assert torch.linalg.norm(C - Cref) <= REL_TOL * torch.linalg.norm(Cref)
+    bound = REL_TOL * A.double().abs().sum(dim=1)
+    assert torch.all((C - Cref).abs() <= bound)
+
+
+@pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC])
+@pytest.mark.parametrize("n_rows,n_cols,n_split", [(8192, 16384, 4), (777, 1024, 4), (5, 64, 1)])
+def test_noalloc_matches_the_allocating_entry_point(sched, n_rows, n_cols, n_split):
+    A = inputs.splitk_matrix(n_rows, n_cols, seed=11).cuda()
+    ref = torch.empty(n_rows, device="cuda")
+    B.etc_splitk_rowsum(A, n_split, ref, sched=sched)
+    for _ in range(2):
+        C = torch.full((n_rows,), float("nan"), device="cuda")
+        B.etc_splitk_rowsum_noalloc(A, n_split, C, sched=sched)
+        torch.cuda.synchronize()
+        assert torch.isfinite(C).all()
+        _close(C.cpu(), ref.cpu(), A.cpu())
+
+
+def test_noalloc_refuses_sizes_beyond_its_scratch():
+    A = torch.zeros(65537, 4, device="cuda")
+    C = torch.empty(65537, device="cuda")
+    with pytest.raises(B.EtcError) as e:
+        B.etc_splitk_rowsum_noalloc(A, 1, C)
+    assert e.value.code == B.ETC_ERR_INVALID and "scratch" in str(e.value)
+    A = torch.zeros(8192, 64 * 4, device="cuda")
+    C = torch.empty(8192, device="cuda")
+    with pytest.raises(B.EtcError):
+        B.etc_splitk_rowsum_noalloc(A, 64, C)  # 8192 * 64 partial sums > 262144
