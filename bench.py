@@ -238,9 +238,9 @@ def run_ours(args, rank, world):
     sec = max_over_ranks(s.elapsed_time(e) / 1e3 / args.steps, world)
     assert B.etc_plan_check(plan) == B.ETC_OK, B.etc_last_error()
     # keep the GPU loaded ~1.5 s more for the clock record if the timed region was short
-    if t1 - t0 < 1.5:
+    if t1 - t0 < args.clock_window:
         tl = time.time()
-        while time.time() - tl < 1.5:
+        while time.time() - tl < args.clock_window:
             for _ in range(20):
                 step()
             torch.cuda.synchronize()
@@ -469,6 +469,34 @@ def run_reference(args, rank, world):
     }
 
 
+def run_single(args):
+    """One workload only, no extras (used for profiling captures): decode or splitk."""
+    import torch
+
+    from moe_layer_scheduling_gb300 import binding as B
+    from moe_layer_scheduling_gb300 import build as libbuild
+    from moe_layer_scheduling_gb300 import inputs
+    libbuild.build()
+    dev = torch.device("cuda")
+    sched = B.ETC_SCHED_DYNAMIC if args.sched == "dynamic" else B.ETC_SCHED_STATIC
+    if args.workload == "splitk":
+        A = inputs.splitk_matrix(8192, 16384, 0).to(dev)
+        C = torch.empty(8192, device=dev)
+        sec = time_gpu(lambda: B.etc_splitk_rowsum(A, 4, C, sched=sched), args.steps, args.warmup, 1)
+        return {"workload": "splitk_8192x16384_4tiles", "sched": args.sched, "us": sec * 1e6,
+                "gbs": A.numel() * 4 / sec / 1e9}
+    w = inputs.qwen_weights(0)
+    wl = inputs.decode_layer(args.tokens, w)
+    plan = B.etc_moe_plan(H, E, K, I, t_max=args.tokens, sched=sched)
+    x, gw, wgu, wd = wl.x.to(dev), w.gate_w.to(dev), w.w_gate_up.to(dev), w.w_down.to(dev)
+    out = torch.empty(args.tokens, H, device=dev)
+    sec = time_gpu(lambda: B.etc_moe_forward(plan, x, gw, wgu, wd, args.tokens, out), args.steps,
+                   args.warmup, 1)
+    plan.close()
+    return {"workload": wl.name, "sched": args.sched, "us": sec * 1e6,
+            "note": "same weights every step (L2-warm for small T)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -480,10 +508,17 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "splitk"],
+                    help="prefill = the benchmark line; decode/splitk = one workload (profiling)")
+    ap.add_argument("--sched", default="dynamic", choices=["static", "dynamic"])
+    ap.add_argument("--clock-window", type=float, default=1.5,
+                    help="seconds of load kept up for the clock record (0 for profiler runs)")
     args = ap.parse_args()
     rank, world, _ = dist_init()
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.workload != "prefill":
+        line = run_single(args)
     else:
         line = run_ours(args, rank, world)
     if rank == 0 and line is not None:

@@ -60,6 +60,7 @@ typedef enum { ETC_SCHED_STATIC = 0, ETC_SCHED_DYNAMIC = 1 } etc_sched_t;
 #define ETC_DEBUG_FAULT_EXTRA_WAIT 0x1u /* add 1 to expert debug_arg's wait_count: its
                                            tiles never become ready, so a wait times out */
 #define ETC_DEBUG_POISON 0x2u           /* fill intermediate buffers with NaN before each call */
+#define ETC_DEBUG_TRACE 0x4u            /* record every task's dispatch/start/end time and SM */
 
 typedef struct etc_plan_s* etc_plan_t;
 
@@ -104,9 +105,11 @@ int etc_moe_plan(etc_plan_t* plan, const etc_moe_opts* opts);
  *   out        fp32 [T, H] (bf16 [T, H] when opts.out_dtype = ETC_OUT_BF16)
  * Routing: top-k of the fp32 logits, ties to the lower expert id; weights =
  * softmax over the k selected logits.  Accumulation is fp32; the SwiGLU
- * activation is rounded to bf16 (the operand of the second GEMM); the
- * per-expert outputs stay fp32 until the combine, whose sum is rounded to
- * bf16 once.  0 <= T <= t_max; T == 0 returns ETC_OK without launching.
+ * activation is rounded to bf16 (the operand of the second GEMM); each down
+ * tile adds its weighted fp32 outputs into the token rows of `out` with
+ * fp32 reductions in L2 (the order of the k additions per element is not
+ * fixed, so results may differ in the last fp32 bits from run to run).
+ * 0 <= T <= t_max; T == 0 returns ETC_OK without launching.
  * Concurrent calls on one plan are undefined: give each stream its own plan.
  */
 int etc_moe_forward(etc_plan_t plan, void* stream, const void* x, const void* gate_w,
@@ -143,11 +146,22 @@ int etc_moe_debug_routing(etc_plan_t plan, void* stream, int block, void* logits
  * Copies `bytes` bytes from the start of an intermediate buffer of the last
  * call into `dst` (device), asynchronously on `stream`.  which: 0 = x_perm
  * bf16 [T*k, H] (expert-sorted input rows), 1 = act bf16 [T*k, I] (SwiGLU
- * output), 2 = y_perm fp32 [T*k, H] (per-row expert outputs).  Returns
- * ETC_ERR_INVALID if `bytes` exceeds the buffer.
+ * output).  Returns ETC_ERR_INVALID if `bytes` exceeds the buffer.
  */
 int etc_moe_debug_buffer(etc_plan_t plan, void* stream, int which, void* dst,
                          unsigned long long bytes);
+
+/*
+ * Task trace of the last call of a plan created with ETC_DEBUG_TRACE: copies
+ * up to `max_records` records into `dst` (device, uint64 [1 + 4*max_records]),
+ * asynchronously on `stream`.  dst[0] = number of records written by the call;
+ * record i = dst[1+4i .. 4+4i]: (type<<56 | block<<48 | sm<<32 | a<<8 | b),
+ * dispatch time, start time, end time (ns, %globaltimer).  The dispatch time
+ * is when the scheduler handed the task to its CTA (after its input event);
+ * start/end bracket the workers' part of the task.  Returns ETC_ERR_INVALID
+ * if the plan has no trace buffer.
+ */
+int etc_moe_debug_trace(etc_plan_t plan, void* stream, void* dst, int max_records);
 
 /*
  * Chain of opts.n_blocks blocks  x <- x + MoE_b(RMSNorm_b(x))  in ONE launch.

@@ -28,7 +28,8 @@ ETC_OUT_BF16 = 1
 
 EXPORTED = [
     "etc_moe_plan", "etc_moe_forward", "etc_moe_forward_unfused", "etc_moe_route_from_logits",
-    "etc_moe_debug_routing", "etc_moe_debug_buffer", "etc_chain_forward", "etc_plan_check", "etc_plan_reset",
+    "etc_moe_debug_routing", "etc_moe_debug_buffer", "etc_moe_debug_trace", "etc_chain_forward",
+    "etc_plan_check", "etc_plan_reset",
     "etc_plan_stats", "etc_plan_destroy", "etc_splitk_rowsum", "etc_splitk_rowsum_ex",
     "etc_splitk_check", "etc_splitk_rowsum_noalloc", "etc_launch_count", "etc_last_error",
 ]
@@ -74,6 +75,7 @@ def load(build_if_missing: bool = True):
     L.etc_moe_route_from_logits.argtypes = [P, P, P, P, I]
     L.etc_moe_debug_routing.argtypes = [P, P, I, P, P, P, P, P, P]
     L.etc_moe_debug_buffer.argtypes = [P, P, I, P, ctypes.c_ulonglong]
+    L.etc_moe_debug_trace.argtypes = [P, P, P, I]
     L.etc_chain_forward.argtypes = [P, P, P, P, P, P, P, P, I, P]
     L.etc_plan_check.argtypes = [P]
     L.etc_plan_reset.argtypes = [P, P]
@@ -250,3 +252,25 @@ def etc_splitk_rowsum_noalloc(A, n_split, C, sched=ETC_SCHED_STATIC, stream=None
     n_rows, n_cols = A.shape
     return _check(load().etc_splitk_rowsum_noalloc(_stream(stream), _ptr(A), n_rows, n_cols,
                                                    int(n_split), _ptr(C), int(sched)))
+
+
+ETC_DEBUG_TRACE = 0x4
+TASK_NAMES = {1: "norm", 2: "router", 3: "topk", 4: "scan", 5: "perm", 6: "gate_up", 7: "down",
+              8: "combine"}
+
+
+def etc_moe_debug_trace(plan: Plan, max_records: int = 65536, stream=None):
+    """Task trace of the last call as a list of dicts (type, block, sm, a, b, times in ns)."""
+    import torch
+    buf = torch.zeros(1 + 4 * max_records, dtype=torch.int64, device="cuda")
+    _check(load().etc_moe_debug_trace(plan.handle, _stream(stream), _ptr(buf), int(max_records)))
+    torch.cuda.synchronize()
+    v = buf.cpu().numpy().astype("uint64")
+    n = int(min(v[0], max_records))
+    recs = []
+    for i in range(n):
+        w0, t_disp, t0, t1 = (int(x) for x in v[1 + 4 * i: 5 + 4 * i])
+        recs.append(dict(type=TASK_NAMES.get(w0 >> 56, str(w0 >> 56)), block=(w0 >> 48) & 0xFF,
+                         sm=(w0 >> 32) & 0xFFFF, a=(w0 >> 8) & 0xFFFFFF, b=w0 & 0xFF,
+                         t_dispatch=t_disp, t_start=t0, t_end=t1))
+    return recs

@@ -18,7 +18,7 @@ constexpr int kWarpTma = 1;         // lane 0: TMA producer
 constexpr int kWarpMma = 2;         // lane 0: tcgen05 issuer; warp owns TMEM
 constexpr int kWorkerWarp0 = 4;     // warps 4..11: epilogue + SIMT tasks
 constexpr int kNumWorkers = 256;
-constexpr int kStages = 4;          // smem operand stages
+constexpr int kStages = 6;          // smem operand stages
 constexpr int kRing = 8;            // smem task ring depth
 constexpr int kTB = 32;             // tokens per router/top-k/permute/combine task
 constexpr int kBT = 128;            // max rows (tokens) per expert chunk = max MMA N
@@ -33,11 +33,14 @@ constexpr int kMaxK = 16;
 constexpr int kStageABytes = 128 * kBK * 2;   // 16 KB: 128 weight rows
 constexpr int kStageBBytes = kBT * kBK * 2;   // 16 KB: up to 128 token rows
 constexpr int kStageBytes = kStageABytes + kStageBBytes;
-constexpr int kSimtBytes = 48 * 1024;
+// The worker warps run one task at a time, so the SIMT tasks' scratch and the
+// GEMM epilogues' staging share one region.
+constexpr int kSimtBytes = 32 * 1024;
 constexpr int kEpiHalfBytes = 8 * 1024;       // U (4 KB fp32) + S (4 KB bf16) per half
+constexpr int kWorkerBytes = kSimtBytes > 2 * kEpiHalfBytes ? kSimtBytes : 2 * kEpiHalfBytes;
 constexpr int kCtrlBytes = 2048;
-constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kSimtBytes +
-                           2 * kEpiHalfBytes + kCtrlBytes;
+constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kWorkerBytes + kCtrlBytes;
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
 constexpr int kRouterKStep = 32;    // K elements per router smem stage
 
 enum TaskType : int {
@@ -88,6 +91,7 @@ struct BlockWs {
   float* wts;          // [T_max, k]
   int* pos;            // [T_max, k] row of slot (t, j) in expert-sorted order
   int* row_token;      // [R_max] token of each expert-sorted row
+  float* row_w;        // [R_max] routing weight of each expert-sorted row
   int* blk_cnt;        // [nb_max, E] per-token-block expert histogram
   int* blk_off;        // [nb_max, E] first row of (token block, expert)
   int* counts;         // [E]
@@ -113,7 +117,7 @@ struct Workspace {
   BlockWs blk[kMaxBlocks];
   __nv_bfloat16* x_perm;  // [R_max, H]
   __nv_bfloat16* act;     // [R_max, I]
-  float* y_perm;          // [R_max, H] fp32 per-row expert outputs
+  float* acc;             // [T_max, H] fp32 combine accumulator when `out` is bf16
   __nv_bfloat16* xn;      // [T_max, H] normalised input rounded to bf16 (chain)
   __nv_bfloat16* xn_lo;   // [T_max, H] bf16 of what that rounding dropped (router only)
   float* resid;           // [n_blocks-1, T_max, H] fp32 residual stream between blocks
@@ -125,6 +129,8 @@ struct Workspace {
   int* qacc;
   DevStatus* status;      // device copy, polled by spinning CTAs
   DevStatus* status_host; // host-mapped mirror written on error
+  unsigned long long* trace;  // [1 + 4 * trace_cap] task trace (debug), or null
+  int trace_cap;
   int qcap;
 };
 
@@ -133,6 +139,8 @@ struct MegaParams {
   CUtensorMap tm_wd[kMaxBlocks];   // [E*H, I]  box 64x64
   CUtensorMap tm_xperm;            // [R_max, H] box 16x64
   CUtensorMap tm_act;              // [R_max, I] box 16x64
+  CUtensorMap tm_xperm64;          // [R_max, H] box 64x64
+  CUtensorMap tm_act64;            // [R_max, I] box 64x64
   Workspace ws;
   const __nv_bfloat16* x;
   void* out;     // fp32 [T, H], or bf16 when out_bf16

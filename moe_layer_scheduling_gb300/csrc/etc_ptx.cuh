@@ -77,6 +77,12 @@ __device__ __forceinline__ int atom_cas_relaxed(int* p, int cmp, int v) {
                : "=r"(old) : "l"(p), "r"(cmp), "r"(v) : "memory");
   return old;
 }
+// *p += v on four consecutive floats, done in L2 (no return value).
+__device__ __forceinline__ void red_add_v4(float* p, float4 v) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
 // Orders this thread's generic-proxy global accesses with later/earlier
 // async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {

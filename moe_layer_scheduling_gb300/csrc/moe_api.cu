@@ -32,7 +32,7 @@ struct etc_plan_s {
   void* ctrl = nullptr;       // counters, flags, queue heads: cleared by reset
   size_t ctrl_bytes = 0;
   Workspace ws{};
-  CUtensorMap tm_xperm{}, tm_act{};
+  CUtensorMap tm_xperm{}, tm_act{}, tm_xperm64{}, tm_act64{};
   const void* cached_wgu[kMaxBlocks] = {};
   const void* cached_wd[kMaxBlocks] = {};
   CUtensorMap tm_wgu[kMaxBlocks]{}, tm_wd[kMaxBlocks]{};
@@ -84,6 +84,7 @@ void carve_block(Bump& data, Bump& ctrl, BlockWs& b, const etc_plan_s& p) {
   b.wts = data.take<float>(T * k);
   b.pos = data.take<int>(T * k);
   b.row_token = data.take<int>(R);
+  b.row_w = data.take<float>(R);
   b.blk_cnt = data.take<int>(nb * E);
   b.blk_off = data.take<int>(nb * E);
   b.counts = data.take<int>(E);
@@ -222,6 +223,8 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   }
   prm.tm_xperm = p->tm_xperm;
   prm.tm_act = p->tm_act;
+  prm.tm_xperm64 = p->tm_xperm64;
+  prm.tm_act64 = p->tm_act64;
   prm.ws = p->ws;
   prm.x = static_cast<const __nv_bfloat16*>(a.x);
   prm.out = a.out;
@@ -251,11 +254,13 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   prm.debug_arg = p->opts.debug_arg;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+  if (p->ws.trace) ETC_CUDA_TRY(cudaMemsetAsync(p->ws.trace, 0, 8, s));
   if (p->opts.debug_flags & ETC_DEBUG_POISON) {
     const size_t rows = static_cast<size_t>(p->R_max);
     ETC_CUDA_TRY(cudaMemsetAsync(p->ws.x_perm, 0xFF, rows * p->H * 2, s));
     ETC_CUDA_TRY(cudaMemsetAsync(p->ws.act, 0xFF, rows * p->I * 2, s));
-    ETC_CUDA_TRY(cudaMemsetAsync(p->ws.y_perm, 0xFF, rows * p->H * 4, s));
+    if (p->ws.acc)
+      ETC_CUDA_TRY(cudaMemsetAsync(p->ws.acc, 0xFF, static_cast<size_t>(p->T_max) * p->H * 4, s));
   }
   if (!unfused) {
     prm.stage_lo = stage_lo;
@@ -346,8 +351,10 @@ int etc_moe_plan(etc_plan_t* out, const etc_moe_opts* opts) {
   p->ws.x_perm = static_cast<__nv_bfloat16*>(m);
   if ((r = alloc_dev(p, &m, R * p->I * 2)) != ETC_OK) return fail(r);
   p->ws.act = static_cast<__nv_bfloat16*>(m);
-  if ((r = alloc_dev(p, &m, R * p->H * 4)) != ETC_OK) return fail(r);
-  p->ws.y_perm = static_cast<float*>(m);
+  if (opts->out_dtype == ETC_OUT_BF16) {  // fp32 accumulator behind a bf16 output
+    if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 4)) != ETC_OK) return fail(r);
+    p->ws.acc = static_cast<float*>(m);
+  }
   if (p->n_blocks > 1) {
     if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 2)) != ETC_OK) return fail(r);
     p->ws.xn = static_cast<__nv_bfloat16*>(m);
@@ -363,6 +370,12 @@ int etc_moe_plan(etc_plan_t* out, const etc_moe_opts* opts) {
     if (cudaMemset(m, 0, static_cast<size_t>(p->ws.qcap) * 8) != cudaSuccess)
       return fail(set_error(ETC_ERR_CUDA, "cudaMemset failed"));
   }
+  if (opts->debug_flags & ETC_DEBUG_TRACE) {
+    p->ws.trace_cap = p->ws.qcap;
+    if ((r = alloc_dev(p, &m, (1 + 4 * static_cast<size_t>(p->ws.trace_cap)) * 8)) != ETC_OK)
+      return fail(r);
+    p->ws.trace = static_cast<unsigned long long*>(m);
+  }
   DevStatus* hs = nullptr;
   if (cudaHostAlloc(&hs, sizeof(DevStatus), cudaHostAllocMapped) != cudaSuccess)
     return fail(set_error(ETC_ERR_CUDA, "cudaHostAlloc failed"));
@@ -370,7 +383,9 @@ int etc_moe_plan(etc_plan_t* out, const etc_moe_opts* opts) {
   p->ws.status_host = hs;
 
   if (encode_tensor_map_2d_bf16(&p->tm_xperm, p->ws.x_perm, p->H, R, kBK, 16) != CUDA_SUCCESS ||
-      encode_tensor_map_2d_bf16(&p->tm_act, p->ws.act, p->I, R, kBK, 16) != CUDA_SUCCESS)
+      encode_tensor_map_2d_bf16(&p->tm_act, p->ws.act, p->I, R, kBK, 16) != CUDA_SUCCESS ||
+      encode_tensor_map_2d_bf16(&p->tm_xperm64, p->ws.x_perm, p->H, R, kBK, 64) != CUDA_SUCCESS ||
+      encode_tensor_map_2d_bf16(&p->tm_act64, p->ws.act, p->I, R, kBK, 64) != CUDA_SUCCESS)
     return fail(set_error(ETC_ERR_CUDA, "tensor map encoding of the workspace failed"));
   *out = p;
   return ETC_OK;
@@ -480,14 +495,21 @@ int etc_moe_debug_buffer(etc_plan_t p, void* stream, int which, void* dst,
   } else if (which == 1) {
     src = p->ws.act;
     cap = R * p->I * 2;
-  } else if (which == 2) {
-    src = p->ws.y_perm;
-    cap = R * p->H * 4;
   } else {
     return set_error(ETC_ERR_INVALID, "unknown buffer %d", which);
   }
   if (bytes > cap) return set_error(ETC_ERR_INVALID, "buffer %d holds %llu bytes", which, cap);
   ETC_CUDA_TRY(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice,
+                               static_cast<cudaStream_t>(stream)));
+  return ETC_OK;
+}
+
+int etc_moe_debug_trace(etc_plan_t p, void* stream, void* dst, int max_records) {
+  clear_error();
+  if (!p || !dst || max_records < 0) return set_error(ETC_ERR_INVALID, "bad argument");
+  if (!p->ws.trace) return set_error(ETC_ERR_INVALID, "plan was created without ETC_DEBUG_TRACE");
+  const size_t n = 1 + 4 * static_cast<size_t>(std::min(max_records, p->ws.trace_cap));
+  ETC_CUDA_TRY(cudaMemcpyAsync(dst, p->ws.trace, n * 8, cudaMemcpyDeviceToDevice,
                                static_cast<cudaStream_t>(stream)));
   return ETC_OK;
 }

@@ -51,6 +51,7 @@ namespace etc {
 struct Task {
   int type, blk, a, b;
   int e, row0, rows, pad;
+  unsigned long long t_disp;  // when the scheduler handed the task over (trace only)
 };
 
 struct Ctrl {
@@ -111,11 +112,12 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
 __device__ __forceinline__ void load_block_input8(const MegaParams& p, int blk, int tok, int c,
                                                   float (&f)[8]) {
   if (blk == 0) {
-    bf16x8_to_f32(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(tok) * p.H)[c], f);
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(tok) * p.H) + c), f);
   } else {
+    // written earlier in this kernel by another CTA: L2-only load
     const float4* r = reinterpret_cast<const float4*>(
         p.ws.resid + (static_cast<size_t>(blk - 1) * p.T_max + tok) * p.H + 8 * c);
-    const float4 a = r[0], b = r[1];
+    const float4 a = __ldcg(r), b = __ldcg(r + 1);
     f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
     f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
   }
@@ -202,8 +204,11 @@ __device__ void task_router(const MegaParams& p, const Task& t, uint8_t* simt, i
     const __nv_bfloat16* X = split ? p.ws.xn : p.x;
     const __nv_bfloat16* Wg = p.gate_w[blk];
     const int E = p.E, H = p.H, ldw = E + 8, ldx = kRouterKStep + 8;
-    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(simt);       // [2 buf][2 hi/lo][32][40]
-    __nv_bfloat16* wsm = xs + 4 * kTB * ldx;                          // [2][32][E+8]
+    // NS-deep cp.async ring, as deep as the worker scratch allows (1..3).
+    const int stage_bytes = (2 * kTB * ldx + kRouterKStep * ldw) * 2;
+    const int NS = min(3, kSimtBytes / stage_bytes);
+    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(simt);       // [NS][2 hi/lo][32][40]
+    __nv_bfloat16* wsm = xs + NS * 2 * kTB * ldx;                     // [NS][32][E+8]
     const int h0 = ch * p.HC, nks = p.HC / kRouterKStep;
     const int ww = wt >> 5, lane = wt & 31;
     auto load = [&](int ks, int buf) {
@@ -226,16 +231,19 @@ __device__ void task_router(const MegaParams& p, const Task& t, uint8_t* simt, i
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     const int mt = ww & 1, ng = ww >> 1, n8 = E / 8;
-    load(0, 0);
+    for (int s = 0; s < NS - 1; ++s) {
+      if (s < nks) load(s, s);
+      else cp_async_commit();  // keep one group per stage
+    }
     for (int ks = 0; ks < nks; ++ks) {
-      if (ks + 1 < nks) {
-        load(ks + 1, (ks + 1) & 1);
-        cp_async_wait<1>();
-      } else {
-        cp_async_wait<0>();
-      }
+      const int nxt = ks + NS - 1;
+      if (nxt < nks) load(nxt, nxt % NS);
+      else cp_async_commit();
+      if (NS == 3) cp_async_wait<2>();  // stage ks has landed
+      else if (NS == 2) cp_async_wait<1>();
+      else cp_async_wait<0>();
       named_bar(1, kNumWorkers);
-      const int buf = ks & 1;
+      const int buf = ks % NS;
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         uint32_t a0, a1, a2, a3, l0 = 0, l1 = 0, l2 = 0, l3 = 0;
@@ -295,73 +303,91 @@ __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int
   const int blk = t.blk, tb = t.a;
   const BlockWs& B = p.ws.blk[blk];
   const int E = p.E, k = p.k, ww = wt >> 5, lane = wt & 31;
-  int* s_cnt = reinterpret_cast<int*>(simt);
+  int* s_cnt = reinterpret_cast<int*>(simt);                  // [E]
+  float* s_log = reinterpret_cast<float*>(simt + 1024);       // [G][E]
+  const int G = min(kTB, (24 * 1024) / (4 * E));              // tokens per pass
   for (int i = wt; i < E; i += kNumWorkers) s_cnt[i] = 0;
-  named_bar(1, kNumWorkers);
   const float* bias = p.bias[blk];
-  for (int r = ww; r < kTB; r += 8) {
-    const int tok = tb * kTB + r;
-    if (tok >= p.T) break;
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = 32 * i + lane;
-      v[i] = -INFINITY;
-      if (e < E) {
+  const size_t cstride = static_cast<size_t>(p.T_pad) * E;
+  for (int g0 = 0; g0 < kTB; g0 += G) {
+    const int tok0 = tb * kTB + g0;
+    if (tok0 >= p.T) break;
+    // Phase 1, all threads: logits of G tokens x E experts (coalesced; the
+    // NC partials come from other CTAs, hence L2-only loads).
+    for (int idx = wt; idx < G * E; idx += kNumWorkers) {
+      const int r = idx / E, e = idx - r * E, tok = tok0 + r;
+      if (tok < p.T) {
         float s;
         if (p.logits_in) {
-          s = p.logits_in[static_cast<size_t>(tok) * E + e];
+          s = __ldg(p.logits_in + static_cast<size_t>(tok) * E + e);
         } else {
-          s = 0.f;
-          for (int c = 0; c < p.NC; ++c)
-            s += B.partial[(static_cast<size_t>(c) * p.T_pad + tok) * E + e];
-          if (bias) s += bias[e];
+          const float* pp = B.partial + static_cast<size_t>(tok) * E + e;
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+          int c = 0;
+          for (; c + 4 <= p.NC; c += 4) {
+            a0 += __ldcg(pp + c * cstride);
+            a1 += __ldcg(pp + (c + 1) * cstride);
+            a2 += __ldcg(pp + (c + 2) * cstride);
+            a3 += __ldcg(pp + (c + 3) * cstride);
+          }
+          for (; c < p.NC; ++c) a0 += __ldcg(pp + c * cstride);
+          s = (a0 + a1) + (a2 + a3);
+          if (bias) s += __ldg(bias + e);
         }
+        s_log[r * E + e] = s;
         B.logits[static_cast<size_t>(tok) * E + e] = s;
-        v[i] = s;
       }
     }
-    unsigned taken = 0;
-    float my_v = -INFINITY;
-    int my_id = 0;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
+    named_bar(1, kNumWorkers);
+    // Phase 2, one warp per token.
+    for (int r = ww; r < G; r += 8) {
+      const int tok = tok0 + r;
+      if (tok >= p.T) break;
+      float v[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = 32 * i + lane;
-        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-          bv = v[i];
-          bi = e;
+      for (int i = 0; i < 8; ++i) v[i] = 32 * i + lane < E ? s_log[r * E + 32 * i + lane] : -INFINITY;
+      unsigned taken = 0;
+      float my_v = -INFINITY;
+      int my_id = 0;
+      for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int e = 32 * i + lane;
+          if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+            bv = v[i];
+            bi = e;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (ov > bv || (ov == bv && oi < bi)) {
+            bv = ov;
+            bi = oi;
+          }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+          my_v = bv;
+          my_id = bi;
         }
       }
+      const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
+      const float ex = lane < k ? expf(my_v - v0) : 0.f;
+      float z = ex;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == j) {
-        my_v = bv;
-        my_id = bi;
+      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+      if (lane < k) {
+        B.ids[tok * k + lane] = my_id;
+        B.wts[tok * k + lane] = ex / z;
+        atomicAdd(&s_cnt[my_id], 1);
       }
     }
-    const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
-    const float ex = lane < k ? expf(my_v - v0) : 0.f;
-    float z = ex;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    if (lane < k) {
-      B.ids[tok * k + lane] = my_id;
-      B.wts[tok * k + lane] = ex / z;
-      atomicAdd(&s_cnt[my_id], 1);
-    }
+    named_bar(1, kNumWorkers);  // s_log reused by the next pass
   }
-  named_bar(1, kNumWorkers);
   for (int i = wt; i < E; i += kNumWorkers) B.blk_cnt[tb * E + i] = s_cnt[i];
   __threadfence();
   named_bar(1, kNumWorkers);
@@ -376,18 +402,34 @@ __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int
 }
 
 // counts / exp_indptr / per-block offsets / expert chunks / event inits.
+// The token blocks are split over the 8 worker warps; lane l of every warp
+// owns experts l, l+32, ...
 __device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
   const int blk = t.blk;
   const BlockWs& B = p.ws.blk[blk];
-  const int E = p.E, nb = p.nb;
-  int* tmp = reinterpret_cast<int*>(simt);
+  const int E = p.E, nb = p.nb, ww = wt >> 5, lane = wt & 31;
+  int* tmp = reinterpret_cast<int*>(simt);               // scan scratch [32]
+  int* s_part = tmp + 32;                                 // [8][E] per-warp partial counts
+  int* s_row0 = s_part + 8 * kMaxE;                       // [E]
+  const int per = (nb + 7) / 8, tb_lo = min(nb, ww * per), tb_hi = min(nb, tb_lo + per);
+  int part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int tb = tb_lo; tb < tb_hi; ++tb) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (32 * i + lane < E) part[i] += __ldcg(B.blk_cnt + tb * E + 32 * i + lane);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (32 * i + lane < E) s_part[ww * kMaxE + 32 * i + lane] = part[i];
+  named_bar(1, kNumWorkers);
   int cnt = 0;
   if (wt < E)
-    for (int tb = 0; tb < nb; ++tb) cnt += B.blk_cnt[tb * E + wt];
+    for (int w = 0; w < 8; ++w) cnt += s_part[w * kMaxE + wt];
   const int nch = (cnt + kBT - 1) / kBT;
   const int row0 = workers_excl_scan(cnt, tmp, wt);
   const int ch0 = workers_excl_scan(nch, tmp + 16, wt);
   if (wt < E) {
+    s_row0[wt] = row0;
     B.counts[wt] = cnt;
     B.exp_indptr[wt] = row0;
     B.chunk_indptr[wt] = ch0;
@@ -397,11 +439,6 @@ __device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int
       B.meta[0] = ch0 + nch;
       B.meta[1] = (ch0 + nch) * p.NT_gu;
       B.meta[2] = (ch0 + nch) * p.NT_dn;
-    }
-    int run = row0;
-    for (int tb = 0; tb < nb; ++tb) {
-      B.blk_off[tb * E + wt] = run;
-      run += B.blk_cnt[tb * E + wt];
     }
     for (int c = 0; c < nch; ++c) {
       const int chn = ch0 + c;
@@ -414,6 +451,20 @@ __device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int
     // Data-dependent event update: expert e waits for its counts[e] rows.
     const int extra = ((p.debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT) && wt == p.debug_arg) ? 1 : 0;
     B.ev_expert[wt] = cnt + extra;
+  }
+  named_bar(1, kNumWorkers);
+  // First row of (token block, expert): exp_indptr[e] + rows of e in earlier blocks.
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = 32 * i + lane;
+    if (e < E) {
+      int run = s_row0[e];
+      for (int w = 0; w < ww; ++w) run += s_part[w * kMaxE + e];
+      for (int tb = tb_lo; tb < tb_hi; ++tb) {
+        B.blk_off[tb * E + e] = run;
+        run += __ldcg(B.blk_cnt + tb * E + e);
+      }
+    }
   }
   for (int tb = wt; tb < nb; tb += kNumWorkers)
     B.ev_tok[tb] = p.k * (min(p.T, tb * kTB + kTB) - tb * kTB);
@@ -444,51 +495,92 @@ __device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int
   }
 }
 
-// Writes the rows of token block tb into x_perm at exp_indptr[e] + rank.
+// fp32 rows that block blk's combine accumulates into: the residual stream of
+// the next block, the caller's fp32 output, or the accumulator behind a bf16
+// output.
+__device__ __forceinline__ float* acc_rows(const MegaParams& p, int blk) {
+  if (blk < p.n_blocks - 1) return p.ws.resid + static_cast<size_t>(blk) * p.T_max * p.H;
+  return p.out_bf16 ? p.ws.acc : static_cast<float*>(p.out);
+}
+
+// Writes the rows of token block tb into x_perm at exp_indptr[e] + rank,
+// records each row's token and routing weight, and sets the block's combine
+// rows to their starting value (0, or the residual in the chain) before any
+// down tile adds into them.
 __device__ void task_perm(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
   const int blk = t.blk, tb = t.a;
   const BlockWs& B = p.ws.blk[blk];
   const int E = p.E, k = p.k, ww = wt >> 5, lane = wt & 31;
   int* s_run = reinterpret_cast<int*>(simt);
   int* s_slot = s_run + kMaxE;
-  for (int i = wt; i < E; i += kNumWorkers) s_run[i] = B.blk_off[tb * E + i];
+  int* s_ids = s_slot + kTB * kMaxK;
+  const int t0 = tb * kTB, ntok = min(kTB, p.T - t0), nslots = ntok * k;
+  for (int i = wt; i < E; i += kNumWorkers) s_run[i] = __ldcg(B.blk_off + tb * E + i);
+  for (int i = wt; i < nslots; i += kNumWorkers) s_ids[i] = __ldcg(B.ids + t0 * k + i);
   named_bar(1, kNumWorkers);
-  const int t0 = tb * kTB, ntok = min(kTB, p.T - t0);
   if (ww == 0) {
     // Ranks in ascending token order; one token's k experts are distinct.
     for (int r = 0; r < ntok; ++r) {
-      const int tok = t0 + r;
       if (lane < k) {
-        const int e = B.ids[tok * k + lane];
+        const int e = s_ids[r * k + lane];
         const int row = s_run[e];
         s_run[e] = row + 1;
-        B.pos[tok * k + lane] = row;
-        B.row_token[row] = tok;
         s_slot[r * k + lane] = row;
       }
       __syncwarp();
     }
   }
   named_bar(1, kNumWorkers);
+  for (int i = wt; i < nslots; i += kNumWorkers) {
+    const int row = s_slot[i];
+    B.pos[t0 * k + i] = row;
+    B.row_token[row] = t0 + i / k;
+    B.row_w[row] = __ldcg(B.wts + t0 * k + i);
+  }
   const __nv_bfloat16* src = p.use_norm ? p.ws.xn : p.x;
-  const int nslots = ntok * k, n8 = p.H / 8;
+  const int n8 = p.H / 8;
+  // One warp per row; all eight 16-byte loads of a lane are in flight before its stores.
   for (int s = ww; s < nslots; s += 8) {
-    const int tok = t0 + s / k, row = s_slot[s];
-    const uint4* sr = reinterpret_cast<const uint4*>(src + static_cast<size_t>(tok) * p.H);
-    uint4* dr = reinterpret_cast<uint4*>(p.ws.x_perm + static_cast<size_t>(row) * p.H);
-    for (int v = lane; v < n8; v += 32) dr[v] = sr[v];
+    const uint4* sr = reinterpret_cast<const uint4*>(src + static_cast<size_t>(t0 + s / k) * p.H);
+    uint4* dr = reinterpret_cast<uint4*>(p.ws.x_perm + static_cast<size_t>(s_slot[s]) * p.H);
+    for (int v0 = 0; v0 < n8; v0 += 256) {
+      uint4 a[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + lane + 32 * u;
+        if (v < n8) a[u] = __ldcg(sr + v);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + lane + 32 * u;
+        if (v < n8) dr[v] = a[u];
+      }
+    }
+  }
+  // Combine rows of this token block start at 0 (or at the block's input).
+  // (A routing-only call has no output rows.)
+  float* accr = acc_rows(p, blk);
+  for (int r = ww; accr != nullptr && r < ntok; r += 8) {
+    const int tok = t0 + r;
+    float4* d = reinterpret_cast<float4*>(accr + static_cast<size_t>(tok) * p.H);
+    for (int c = lane; c < n8; c += 32) {
+      float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (p.use_norm) load_block_input8(p, blk, tok, c, x);
+      d[2 * c] = make_float4(x[0], x[1], x[2], x[3]);
+      d[2 * c + 1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
   }
   fence_proxy_async_global();  // x_perm is read next by TMA (async proxy)
   __threadfence();
   named_bar(1, kNumWorkers);
   const Clock c0{~0ull, p.ws.status, p.ws.status_host};
   for (int e = wt; e < E; e += kNumWorkers) {
-    const int n = B.blk_cnt[tb * E + e];
+    const int n = __ldcg(B.blk_cnt + tb * E + e);
     if (n > 0) {
       const int left = notify(&B.ev_expert[e], n);
       if (left == 0 && dynamic_mode(p)) {
         // Expert e is ready: fire the tiles of rows [exp_indptr[e], exp_indptr[e+1]).
-        const int c0i = B.chunk_indptr[e], nch = B.chunk_indptr[e + 1] - c0i;
+        const int c0i = __ldcg(B.chunk_indptr + e), nch = __ldcg(B.chunk_indptr + e + 1) - c0i;
         const int NT = p.NT_gu;
         queue_push(queue_of(p), nch * NT,
                    [&](int i) { return task_enc(TK_GU, blk, c0i + i / NT, i % NT); }, c0);
@@ -497,57 +589,23 @@ __device__ void task_perm(const MegaParams& p, const Task& t, uint8_t* simt, int
   }
 }
 
-// out[t] = sum_j w[t,j] * y[pos[t,j]] (j ascending, fp32) (+ x[t] in the chain).
+// Finaliser of token block tb once every down tile touching it has added its
+// weighted expert rows: rounds the rows to bf16 when the output is bf16, and
+// in the chain releases the next block's RMSNorm of tb.
 __device__ void task_comb(const MegaParams& p, const Task& t, int wt) {
   const int blk = t.blk, tb = t.a;
   const BlockWs& B = p.ws.blk[blk];
-  const int k = p.k, ww = wt >> 5, lane = wt & 31, n8 = p.H / 8;
-  const bool last = blk == p.n_blocks - 1;
-  float* resid_out = p.ws.resid + static_cast<size_t>(blk) * p.T_max * p.H;  // when !last
-  for (int r = ww; r < kTB; r += 8) {
-    const int tok = tb * kTB + r;
-    if (tok >= p.T) break;
-    const int pj = lane < k ? B.pos[tok * k + lane] : 0;
-    const float wj = lane < k ? B.wts[tok * k + lane] : 0.f;
-    int prow[kMaxK];
-    float pw[kMaxK];
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      prow[j] = __shfl_sync(0xffffffffu, pj, j);
-      pw[j] = __shfl_sync(0xffffffffu, wj, j);
-    }
-    for (int c = lane; c < n8; c += 32) {
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j < k) {
-          const float4* yr = reinterpret_cast<const float4*>(
-              p.ws.y_perm + static_cast<size_t>(prow[j]) * p.H + 8 * c);
-          const float4 y0 = yr[0], y1 = yr[1];
-          acc[0] += pw[j] * y0.x;
-          acc[1] += pw[j] * y0.y;
-          acc[2] += pw[j] * y0.z;
-          acc[3] += pw[j] * y0.w;
-          acc[4] += pw[j] * y1.x;
-          acc[5] += pw[j] * y1.y;
-          acc[6] += pw[j] * y1.z;
-          acc[7] += pw[j] * y1.w;
-        }
-      }
-      if (p.use_norm) {
-        float x[8];
-        load_block_input8(p, blk, tok, c, x);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += x[i];
-      }
-      if (last && p.out_bf16) {
-        reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(tok) * p.H)[c] =
-            f32_to_bf16x8(acc);
-      } else {
-        float* row = last ? static_cast<float*>(p.out) : resid_out;
-        float4* d = reinterpret_cast<float4*>(row + static_cast<size_t>(tok) * p.H + 8 * c);
-        d[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        d[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  const int ww = wt >> 5, lane = wt & 31, n8 = p.H / 8;
+  if (blk == p.n_blocks - 1 && p.out_bf16) {
+    for (int r = ww; r < kTB; r += 8) {
+      const int tok = tb * kTB + r;
+      if (tok >= p.T) break;
+      const float4* s = reinterpret_cast<const float4*>(p.ws.acc + static_cast<size_t>(tok) * p.H);
+      uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(tok) * p.H);
+      for (int c = lane; c < n8; c += 32) {
+        const float4 a = __ldcg(s + 2 * c), b = __ldcg(s + 2 * c + 1);
+        const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        d[c] = f32_to_bf16x8(f);
       }
     }
   }
@@ -581,6 +639,16 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
   const uint32_t tbase = c->tmem_base + acc * kAccCols + (static_cast<uint32_t>(32 * q) << 16);
   const int ncb = (t.rows + 15) >> 4;
   const BlockWs& B = p.ws.blk[t.blk];
+  // Down tiles: each chunk row's token and routing weight, for the combine.
+  int* s_rtok = reinterpret_cast<int*>(simt + 2 * kEpiHalfBytes);                 // [128]
+  float* s_rw = reinterpret_cast<float*>(simt + 2 * kEpiHalfBytes + 4 * kBT);     // [128]
+  if (t.type == TK_DN) {
+    for (int r = wt; r < t.rows; r += kNumWorkers) {
+      s_rtok[r] = __ldcg(B.row_token + t.row0 + r);
+      s_rw[r] = __ldcg(B.row_w + t.row0 + r);
+    }
+    named_bar(1, kNumWorkers);
+  }
   if (ok) {
     if (t.type == TK_GU) {
       for (int cb = h; cb < ncb; cb += 2) {
@@ -610,7 +678,9 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
         named_bar(2 + h, 128);
       }
     } else {
+      // Weighted combine fused here: out[token] += w * y, 4 columns per red op.
       float* S32 = reinterpret_cast<float*>(epi + h * kEpiHalfBytes);  // [16][128] fp32
+      float* accr = acc_rows(p, t.blk) + t.b * kDnRows;
       for (int cb = h; cb < ncb; cb += 2) {
         float v[16];
         tmem_ld16(tbase + cb * 16, v);
@@ -620,11 +690,12 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
 #pragma unroll
         for (int rep = 0; rep < 4; ++rep) {
           const int idx = i128 + 128 * rep;
-          const int tok = cb * 16 + (idx >> 5), chunk = idx & 31;
-          if (tok < t.rows) {
+          const int r = cb * 16 + (idx >> 5), chunk = idx & 31;
+          if (r < t.rows) {
             const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
-            *reinterpret_cast<float4*>(p.ws.y_perm + static_cast<size_t>(t.row0 + tok) * p.H +
-                                       t.b * kDnRows + chunk * 4) = val;
+            const float wr = s_rw[r];
+            red_add_v4(accr + static_cast<size_t>(s_rtok[r]) * p.H + chunk * 4,
+                       make_float4(wr * val.x, wr * val.y, wr * val.z, wr * val.w));
           }
         }
         named_bar(2 + h, 128);
@@ -648,15 +719,13 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
     if (wt == 0) *fin = notify(&B.ev_down[t.a], 1) == 0 ? 1 : 0;
     named_bar(1, kNumWorkers);
     if (*fin) {
-      // Finisher of the chunk: notify each token block by its number of rows.
-      int* s_tb = reinterpret_cast<int*>(simt);
-      for (int r = wt; r < t.rows; r += kNumWorkers) s_tb[r] = B.row_token[t.row0 + r] / kTB;
-      named_bar(1, kNumWorkers);
+      // Finisher of the chunk: notify each token block by its number of rows
+      // (the chunk's rows are in ascending token order, so blocks form runs).
       for (int r = wt; r < t.rows; r += kNumWorkers) {
-        const int tb = s_tb[r];
-        if (r == 0 || s_tb[r - 1] != tb) {
+        const int tb = s_rtok[r] / kTB;
+        if (r == 0 || s_rtok[r - 1] / kTB != tb) {
           int e = r + 1;
-          while (e < t.rows && s_tb[e] == tb) ++e;
+          while (e < t.rows && s_rtok[e] / kTB == tb) ++e;
           const int left = notify(&B.ev_tok[tb], e - r);
           if (left == 0 && dynamic_mode(p))
             queue_push(queue_of(p), 1, [&](int) { return task_enc(TK_COMB, t.blk, tb, 0); }, c0);
@@ -683,6 +752,7 @@ __device__ void run_workers(const MegaParams& p, Ctrl* c, uint8_t* simt, uint8_t
     }
     named_bar(1, kNumWorkers);
     const Task t = *slot;
+    const unsigned long long t_start = p.ws.trace ? globaltimer_ns() : 0;
     switch (t.type) {
       case TK_NORM: task_norm(p, t, wt); break;
       case TK_ROUTER: task_router(p, t, simt, wt); break;
@@ -695,6 +765,19 @@ __device__ void run_workers(const MegaParams& p, Ctrl* c, uint8_t* simt, uint8_t
       default: break;
     }
     if (t.type == TK_TERM) break;
+    if (p.ws.trace && wt == 0) {
+      const int idx = static_cast<int>(atomicAdd(p.ws.trace, 1ull));
+      if (idx < p.ws.trace_cap) {
+        unsigned long long* r = p.ws.trace + 1 + 4 * static_cast<size_t>(idx);
+        r[0] = (static_cast<unsigned long long>(t.type) << 56) |
+               (static_cast<unsigned long long>(t.blk) << 48) |
+               (static_cast<unsigned long long>(blockIdx.x) << 32) |
+               (static_cast<unsigned long long>(t.a) << 8) | static_cast<unsigned long long>(t.b);
+        r[1] = t.t_disp;
+        r[2] = t_start;
+        r[3] = globaltimer_ns();
+      }
+    }
   }
 }
 
@@ -720,8 +803,10 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
     const bool gu = t.type == TK_GU;
     const CUtensorMap* ta = gu ? &p.tm_wgu[t.blk] : &p.tm_wd[t.blk];
     const CUtensorMap* tb = gu ? &p.tm_xperm : &p.tm_act;
+    const CUtensorMap* tb64 = gu ? &p.tm_xperm64 : &p.tm_act64;
     const int KB = (gu ? p.H : p.I) / kBK;
     const int nb16 = (t.rows + 15) >> 4;
+    const int n64 = nb16 >> 2, r16 = nb16 & 3;  // token rows as 64-row boxes, then 16-row boxes
     int rowA0, rowA1;
     if (gu) {
       rowA0 = t.e * 2 * p.I + t.b * kGuRows;  // gate rows
@@ -740,8 +825,11 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
       mbar_arrive_expect_tx(&c->full[s], bytes);
       tma_load_2d(sa, ta, &c->full[s], kb * kBK, rowA0);
       tma_load_2d(sa + kStageABytes / 2, ta, &c->full[s], kb * kBK, rowA1);
-      for (int i = 0; i < nb16; ++i)
-        tma_load_2d(sb + i * 16 * kBK * 2, tb, &c->full[s], kb * kBK, t.row0 + 16 * i);
+      for (int i = 0; i < n64; ++i)
+        tma_load_2d(sb + i * 64 * kBK * 2, tb64, &c->full[s], kb * kBK, t.row0 + 64 * i);
+      for (int i = 0; i < r16; ++i)
+        tma_load_2d(sb + (n64 * 64 + i * 16) * kBK * 2, tb, &c->full[s], kb * kBK,
+                    t.row0 + n64 * 64 + 16 * i);
     }
   }
 }
@@ -786,6 +874,7 @@ struct RingWriter {
     const int r = i % kRing;
     if (!mbar_wait(&c->rempty[r], ((i / kRing) & 1) ^ 1, clk, 200)) return false;
     c->ring[r] = t;
+    c->ring[r].t_disp = globaltimer_ns();
     mbar_arrive(&c->rfull[r]);
     ++i;
     return true;
@@ -804,9 +893,9 @@ __device__ __forceinline__ Task make_task(int type, int blk, int a, int b) {
 
 __device__ __forceinline__ void resolve_chunk(const MegaParams& p, Task& t) {
   const BlockWs& B = p.ws.blk[t.blk];
-  t.e = B.chunk_expert[t.a];
-  t.row0 = B.chunk_row0[t.a];
-  t.rows = B.chunk_rows[t.a];
+  t.e = __ldcg(B.chunk_expert + t.a);
+  t.row0 = __ldcg(B.chunk_row0 + t.a);
+  t.rows = __ldcg(B.chunk_rows + t.a);
 }
 
 __device__ void sched_static(const MegaParams& p, Ctrl* c, const Clock& clk) {
@@ -921,8 +1010,8 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* simt = base + kStages * kStageBytes;
-  uint8_t* epi = simt + kSimtBytes;
-  Ctrl* c = reinterpret_cast<Ctrl*>(epi + 2 * kEpiHalfBytes);
+  uint8_t* epi = simt;  // shared with the SIMT scratch (one worker task at a time)
+  Ctrl* c = reinterpret_cast<Ctrl*>(simt + kWorkerBytes);
   const Clock clk{globaltimer_ns() + p.timeout_ns, p.ws.status, p.ws.status_host};
   const int w = warp_id();
   if (threadIdx.x == 0) {
@@ -947,6 +1036,8 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
     }
     tma_prefetch_desc(&p.tm_xperm);
     tma_prefetch_desc(&p.tm_act);
+    tma_prefetch_desc(&p.tm_xperm64);
+    tma_prefetch_desc(&p.tm_act64);
   }
   if (w == kWarpMma) {
     tmem_alloc(&c->tmem_base, kTmemCols);

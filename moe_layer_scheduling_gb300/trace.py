@@ -1,0 +1,80 @@
+"""Task-trace summary of one megakernel call (a profiling aid).
+
+Runs one MoE layer with the library's ETC_DEBUG_TRACE flag and prints, per
+task type, how many tasks ran, their summed and mean busy time on the worker
+warps, and when the stage started and ended relative to the first task;
+also the time from the first to the last task and how busy the SMs were.
+
+    python -m moe_layer_scheduling_gb300.trace --tokens 4096 --skew --sched dynamic
+"""
+from __future__ import annotations
+
+import argparse
+import json
+from collections import defaultdict
+
+
+def summarize(recs: list[dict]) -> dict:
+    if not recs:
+        return {}
+    t0 = min(r["t_dispatch"] or r["t_start"] for r in recs)
+    t_end = max(r["t_end"] for r in recs)
+    by = defaultdict(list)
+    for r in recs:
+        by[r["type"]].append(r)
+    stages = {}
+    for name, rs in by.items():
+        busy = [r["t_end"] - r["t_start"] for r in rs]
+        wait = [r["t_start"] - r["t_dispatch"] for r in rs if r["t_dispatch"]]
+        stages[name] = {
+            "tasks": len(rs),
+            "busy_us_sum": sum(busy) / 1e3,
+            "busy_us_mean": sum(busy) / len(busy) / 1e3,
+            "queue_us_mean": (sum(wait) / len(wait) / 1e3) if wait else None,
+            "first_start_us": (min(r["t_start"] for r in rs) - t0) / 1e3,
+            "last_end_us": (max(r["t_end"] for r in rs) - t0) / 1e3,
+        }
+    sms = {r["sm"] for r in recs}
+    busy_total = sum(r["t_end"] - r["t_start"] for r in recs)
+    span = t_end - t0
+    return {"span_us": span / 1e3, "sms": len(sms),
+            "worker_busy_frac": busy_total / (span * max(len(sms), 1)) if span else None,
+            "stages": stages}
+
+
+def main():
+    import torch
+
+    from . import binding as B
+    from . import inputs
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--skew", action="store_true", help="Zipf(1.2) router bias (prefill workload)")
+    ap.add_argument("--sched", default="dynamic", choices=["static", "dynamic"])
+    ap.add_argument("--repeat", type=int, default=3, help="calls before the traced one")
+    args = ap.parse_args()
+    dev = torch.device("cuda")
+    w = inputs.qwen_weights(0)
+    wl = inputs.prefill_skew_layer(args.tokens, w) if args.skew else inputs.decode_layer(args.tokens, w)
+    bias = wl.weights.router_bias.to(dev) if wl.weights.router_bias is not None else None
+    sched = B.ETC_SCHED_DYNAMIC if args.sched == "dynamic" else B.ETC_SCHED_STATIC
+    plan = B.etc_moe_plan(w.hidden, w.n_experts, w.top_k, w.inter, t_max=args.tokens, sched=sched,
+                          router_bias=bias, debug_flags=B.ETC_DEBUG_TRACE)
+    x = wl.x.to(dev)
+    gw, wgu, wd = w.gate_w.to(dev), w.w_gate_up.to(dev), w.w_down.to(dev)
+    out = torch.empty(args.tokens, w.hidden, device=dev)
+    for _ in range(args.repeat + 1):
+        B.etc_moe_forward(plan, x, gw, wgu, wd, args.tokens, out)
+    torch.cuda.synchronize()
+    assert B.etc_plan_check(plan) == B.ETC_OK, B.etc_last_error()
+    recs = B.etc_moe_debug_trace(plan, max_records=200000)
+    s = summarize(recs)
+    s["workload"] = wl.name
+    s["sched"] = args.sched
+    print(json.dumps(s, indent=1))
+    plan.close()
+
+
+if __name__ == "__main__":
+    main()
