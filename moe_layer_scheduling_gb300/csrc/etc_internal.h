@@ -85,7 +85,8 @@ __host__ __device__ inline int task_b(uint32_t d) { return static_cast<int>(d & 
 
 // Per-block workspace (the chain keeps one per block).
 struct BlockWs {
-  float* partial;      // [NC_max, T_pad, E] router partial logits per H-chunk
+  float* partial;      // [T_pad, E] router logits when H is not split (NC == 1)
+  unsigned long long* logit_fx;  // [T_pad, E] sum of H-chunk partials, fixed point 2^-40 (NC > 1)
   float* logits;       // [T_max, E] final fp32 logits (with bias)
   int* ids;            // [T_max, k]
   float* wts;          // [T_max, k]

@@ -77,6 +77,12 @@ __device__ __forceinline__ int atom_cas_relaxed(int* p, int cmp, int v) {
                : "=r"(old) : "l"(p), "r"(cmp), "r"(v) : "memory");
   return old;
 }
+__device__ __forceinline__ void red_add_relaxed(int* p, int v) {
+  asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 // *p += v on four consecutive floats, done in L2 (no return value).
 __device__ __forceinline__ void red_add_v4(float* p, float4 v) {
   asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x),

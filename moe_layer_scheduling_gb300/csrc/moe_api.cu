@@ -78,7 +78,8 @@ struct Bump {
 
 void carve_block(Bump& data, Bump& ctrl, BlockWs& b, const etc_plan_s& p) {
   const size_t E = p.E, k = p.k, T = p.T_max, nb = p.nb_max, C = p.C_max, R = p.R_max;
-  b.partial = data.take<float>(p.partial_max * E);
+  b.partial = data.take<float>(static_cast<size_t>(nb) * kTB * E);
+  b.logit_fx = ctrl.take<unsigned long long>(static_cast<size_t>(nb) * kTB * E);
   b.logits = data.take<float>(T * E);
   b.ids = data.take<int>(T * k);
   b.wts = data.take<float>(T * k);

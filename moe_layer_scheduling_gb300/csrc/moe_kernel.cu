@@ -54,6 +54,8 @@ struct Task {
   unsigned long long t_disp;  // when the scheduler handed the task over (trace only)
 };
 
+constexpr int kNoti = 8;  // finished tasks waiting for the notifier warp
+
 struct Ctrl {
   uint64_t full[kStages];
   uint64_t empty[kStages];
@@ -61,14 +63,20 @@ struct Ctrl {
   uint64_t tempty[2];
   uint64_t rfull[kRing];
   uint64_t rempty[kRing];
+  uint64_t nfull[kNoti];
+  uint64_t nempty[kNoti];
   Task ring[kRing];
   Task wtask[2];     // workers' broadcast of the current task (double-buffered)
+  Task noti[kNoti];  // workers -> notifier
+  int noti_rtok[kBT];
   uint32_t tmem_base;
   int wflag[2];      // workers' broadcast flags
+  int started;       // tasks the workers have taken from the ring
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
 constexpr int kRingConsumers = 3;  // TMA lane, MMA lane, worker thread 0
+constexpr int kWarpNotifier = 3;
 
 __device__ __forceinline__ QueueView queue_of(const MegaParams& p) {
   QueueView q;
@@ -182,15 +190,8 @@ __device__ void task_norm(const MegaParams& p, const Task& t, int wt) {
       dst_lo[c] = f32_to_bf16x8(f);
     }
   }
-  __threadfence();
-  named_bar(1, kNumWorkers);
-  if (wt == 0) {
-    st_release(&B.norm_flag[tb], p.epoch);
-    if (dynamic_mode(p)) {
-      const Clock c0{~0ull, p.ws.status, p.ws.status_host};
-      queue_push(queue_of(p), p.NC, [&](int i) { return task_enc(TK_ROUTER, blk, tb, i); }, c0);
-    }
-  }
+  named_bar(1, kNumWorkers);  // notify: norm_flag (by the notifier warp)
+  (void)B;
 }
 
 // Router partial logits of token block tb over H-chunk c, on mma.sync
@@ -268,7 +269,17 @@ __device__ void task_router(const MegaParams& p, const Task& t, uint8_t* simt, i
       named_bar(1, kNumWorkers);
     }
     const int g = lane >> 2, tq = lane & 3;
-    float* part = B.partial + static_cast<size_t>(ch) * p.T_pad * E;
+    // With H split over NC chunks the partials are summed exactly and in any
+    // order as 64-bit fixed point (units of 2^-40), so the logits do not
+    // depend on which chunk lands first.
+    auto put = [&](int tok, int e, float v) {
+      const size_t o = static_cast<size_t>(tok) * E + e;
+      if (p.NC == 1)
+        B.partial[o] = v;
+      else
+        red_add_u64(B.logit_fx + o, static_cast<unsigned long long>(
+                                        __double2ll_rn(static_cast<double>(v) * 1099511627776.0)));
+    };
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int j = ng + 4 * i;
@@ -276,25 +287,17 @@ __device__ void task_router(const MegaParams& p, const Task& t, uint8_t* simt, i
         const int e = j * 8 + 2 * tq;
         const int t0 = tb * kTB + mt * 16 + g;
         if (t0 < p.T) {
-          part[static_cast<size_t>(t0) * E + e] = acc[i][0];
-          part[static_cast<size_t>(t0) * E + e + 1] = acc[i][1];
+          put(t0, e, acc[i][0]);
+          put(t0, e + 1, acc[i][1]);
         }
         if (t0 + 8 < p.T) {
-          part[static_cast<size_t>(t0 + 8) * E + e] = acc[i][2];
-          part[static_cast<size_t>(t0 + 8) * E + e + 1] = acc[i][3];
+          put(t0 + 8, e, acc[i][2]);
+          put(t0 + 8, e + 1, acc[i][3]);
         }
       }
     }
   }
-  __threadfence();
-  named_bar(1, kNumWorkers);
-  if (wt == 0) {
-    const int arrived = atom_add_acq_rel(&B.ev_rblk[tb], 1) + 1;
-    if (arrived == p.NC && dynamic_mode(p)) {
-      const Clock c0{~0ull, p.ws.status, p.ws.status_host};
-      queue_push(queue_of(p), 1, [&](int) { return task_enc(TK_TOPK, blk, tb, 0); }, c0);
-    }
-  }
+  named_bar(1, kNumWorkers);  // notify: ev_rblk[tb] (by the notifier warp)
 }
 
 // Top-k over the summed logits of token block tb; ties go to the lower id;
@@ -308,7 +311,6 @@ __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int
   const int G = min(kTB, (24 * 1024) / (4 * E));              // tokens per pass
   for (int i = wt; i < E; i += kNumWorkers) s_cnt[i] = 0;
   const float* bias = p.bias[blk];
-  const size_t cstride = static_cast<size_t>(p.T_pad) * E;
   for (int g0 = 0; g0 < kTB; g0 += G) {
     const int tok0 = tb * kTB + g0;
     if (tok0 >= p.T) break;
@@ -321,17 +323,14 @@ __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int
         if (p.logits_in) {
           s = __ldg(p.logits_in + static_cast<size_t>(tok) * E + e);
         } else {
-          const float* pp = B.partial + static_cast<size_t>(tok) * E + e;
-          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-          int c = 0;
-          for (; c + 4 <= p.NC; c += 4) {
-            a0 += __ldcg(pp + c * cstride);
-            a1 += __ldcg(pp + (c + 1) * cstride);
-            a2 += __ldcg(pp + (c + 2) * cstride);
-            a3 += __ldcg(pp + (c + 3) * cstride);
+          const size_t o = static_cast<size_t>(tok) * E + e;
+          if (p.NC == 1) {
+            s = __ldcg(B.partial + o);
+          } else {
+            const long long v = static_cast<long long>(__ldcg(B.logit_fx + o));
+            B.logit_fx[o] = 0ull;  // consumed: re-armed for the next call
+            s = static_cast<float>(static_cast<double>(v) * 9.094947017729282379e-13);  // 2^-40
           }
-          for (; c < p.NC; ++c) a0 += __ldcg(pp + c * cstride);
-          s = (a0 + a1) + (a2 + a3);
           if (bias) s += __ldg(bias + e);
         }
         s_log[r * E + e] = s;
@@ -389,16 +388,7 @@ __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int
     named_bar(1, kNumWorkers);  // s_log reused by the next pass
   }
   for (int i = wt; i < E; i += kNumWorkers) B.blk_cnt[tb * E + i] = s_cnt[i];
-  __threadfence();
-  named_bar(1, kNumWorkers);
-  if (wt == 0) {
-    st_relaxed(&B.ev_rblk[tb], 0);  // consumed: re-armed for the next call
-    const int arrived = atom_add_acq_rel(B.ev_route, 1) + 1;
-    if (arrived == p.nb && dynamic_mode(p)) {
-      const Clock c0{~0ull, p.ws.status, p.ws.status_host};
-      queue_push(queue_of(p), 1, [&](int) { return task_enc(TK_SCAN, blk, 0, 0); }, c0);
-    }
-  }
+  named_bar(1, kNumWorkers);  // notify: ev_route (by the notifier warp)
 }
 
 // counts / exp_indptr / per-block offsets / expert chunks / event inits.
@@ -571,22 +561,7 @@ __device__ void task_perm(const MegaParams& p, const Task& t, uint8_t* simt, int
     }
   }
   fence_proxy_async_global();  // x_perm is read next by TMA (async proxy)
-  __threadfence();
-  named_bar(1, kNumWorkers);
-  const Clock c0{~0ull, p.ws.status, p.ws.status_host};
-  for (int e = wt; e < E; e += kNumWorkers) {
-    const int n = __ldcg(B.blk_cnt + tb * E + e);
-    if (n > 0) {
-      const int left = notify(&B.ev_expert[e], n);
-      if (left == 0 && dynamic_mode(p)) {
-        // Expert e is ready: fire the tiles of rows [exp_indptr[e], exp_indptr[e+1]).
-        const int c0i = __ldcg(B.chunk_indptr + e), nch = __ldcg(B.chunk_indptr + e + 1) - c0i;
-        const int NT = p.NT_gu;
-        queue_push(queue_of(p), nch * NT,
-                   [&](int i) { return task_enc(TK_GU, blk, c0i + i / NT, i % NT); }, c0);
-      }
-    }
-  }
+  named_bar(1, kNumWorkers);   // notify: ev_expert[e] per expert (by the notifier warp)
 }
 
 // Finaliser of token block tb once every down tile touching it has added its
@@ -609,15 +584,8 @@ __device__ void task_comb(const MegaParams& p, const Task& t, int wt) {
       }
     }
   }
-  __threadfence();
-  named_bar(1, kNumWorkers);
-  if (wt == 0) {
-    if (p.use_norm) st_release(&B.comb_flag[tb], p.epoch);
-    if (dynamic_mode(p) && blk + 1 < p.n_blocks) {
-      const Clock c0{~0ull, p.ws.status, p.ws.status_host};
-      queue_push(queue_of(p), 1, [&](int) { return task_enc(TK_NORM, blk + 1, tb, 0); }, c0);
-    }
-  }
+  named_bar(1, kNumWorkers);  // notify: comb_flag (by the notifier warp)
+  (void)B;
 }
 
 // TMEM epilogue of a GU or DN tile, then its notify.
@@ -703,48 +671,207 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
     }
   }
   fence_proxy_async_global();  // act is read next by TMA
-  __threadfence();
   tc_fence_before();
-  named_bar(1, kNumWorkers);
+  named_bar(1, kNumWorkers);  // notify: ev_act / ev_down (by the notifier warp)
   if (wt == 0) mbar_arrive(&c->tempty[acc]);
-  const Clock c0{~0ull, p.ws.status, p.ws.status_host};
-  if (t.type == TK_GU) {
-    if (wt == 0) {
-      const int left = notify(&B.ev_act[t.a], 1);
-      if (left == 0 && dynamic_mode(p))
-        queue_push(queue_of(p), p.NT_dn, [&](int i) { return task_enc(TK_DN, t.blk, t.a, i); }, c0);
+}
+
+// ---------------------------------------------------------------------------
+// Notifier warp: takes each finished task from the workers and performs its
+// notify (and, in dynamic mode, the early push of the tasks it makes ready),
+// so that the fence and atomic latency stays off the workers' path.
+// ---------------------------------------------------------------------------
+__device__ void hand_over(Ctrl* c, uint32_t& nit, const Task& t, const Clock& clk) {
+  const int s = nit % kNoti;
+  if (mbar_wait(&c->nempty[s], ((nit / kNoti) & 1) ^ 1, clk, 260)) {
+    c->noti[s] = t;
+    mbar_arrive(&c->nfull[s]);
+  }
+  ++nit;
+}
+
+// Warp-wide push: lane 0 reserves n slots, every lane writes some of them.
+template <class DescOf>
+__device__ void queue_push_warp(const QueueView& q, int n, DescOf desc_of, const Clock& c,
+                                int lane) {
+  int base = 0;
+  if (lane == 0) base = q.n_seed + atom_add_relaxed(q.tail, n);
+  base = __shfl_sync(0xffffffffu, base, 0);
+  __threadfence();
+  for (int i = lane; i < n; i += 32) {
+    const int idx = base + i;
+    if (idx >= q.cap) {
+      raise_error(c, DERR_QUEUE_OVERFLOW, 1, idx);
+      break;
     }
-  } else {
-    int* fin = &c->wflag[(iter & 1) ^ 1];
-    if (wt == 0) *fin = notify(&B.ev_down[t.a], 1) == 0 ? 1 : 0;
-    named_bar(1, kNumWorkers);
-    if (*fin) {
-      // Finisher of the chunk: notify each token block by its number of rows
-      // (the chunk's rows are in ascending token order, so blocks form runs).
-      for (int r = wt; r < t.rows; r += kNumWorkers) {
-        const int tb = s_rtok[r] / kTB;
-        if (r == 0 || s_rtok[r - 1] / kTB != tb) {
-          int e = r + 1;
-          while (e < t.rows && s_rtok[e] / kTB == tb) ++e;
-          const int left = notify(&B.ev_tok[tb], e - r);
-          if (left == 0 && dynamic_mode(p))
-            queue_push(queue_of(p), 1, [&](int) { return task_enc(TK_COMB, t.blk, tb, 0); }, c0);
+    st_relaxed_u64(&q.slots[idx], (static_cast<unsigned long long>(q.epoch) << 32) | desc_of(i));
+  }
+}
+
+// Phase A of a notify: the one counter or flag a finished task updates,
+// issued by one lane per record so that a batch costs one round trip.
+// Returns whether the update completed the event (when that matters).
+__device__ __forceinline__ int notify_primary(const MegaParams& p, const Task& t) {
+  const BlockWs& B = p.ws.blk[t.blk];
+  const bool dyn = dynamic_mode(p);
+  switch (t.type) {
+    case TK_NORM:
+      st_relaxed(reinterpret_cast<int*>(&B.norm_flag[t.a]), static_cast<int>(p.epoch));
+      return 0;
+    case TK_ROUTER:  // partial logits of block tb landed ("ij->i" on ev_rblk)
+      if (!dyn) {
+        red_add_relaxed(&B.ev_rblk[t.a], 1);
+        return 0;
+      }
+      return atom_add_acq_rel(&B.ev_rblk[t.a], 1) + 1 == p.NC;
+    case TK_TOPK:
+      st_relaxed(&B.ev_rblk[t.a], 0);  // consumed: re-armed for the next call
+      if (!dyn) {
+        red_add_relaxed(B.ev_route, 1);
+        return 0;
+      }
+      return atom_add_acq_rel(B.ev_route, 1) + 1 == p.nb;
+    case TK_GU:
+      if (!dyn) {
+        red_add_relaxed(&B.ev_act[t.a], -1);
+        return 0;
+      }
+      return notify(&B.ev_act[t.a], 1) == 0;
+    case TK_DN:  // both modes need to know which tile finished the chunk
+      return notify(&B.ev_down[t.a], 1) == 0;
+    case TK_COMB:
+      if (p.use_norm) st_relaxed(reinterpret_cast<int*>(&B.comb_flag[t.a]), static_cast<int>(p.epoch));
+      return 0;
+    default:
+      return 0;
+  }
+}
+
+// Phase B: what follows from the primary update, warp-wide.
+__device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int fire, int lane,
+                              const Clock& clk) {
+  const BlockWs& B = p.ws.blk[t.blk];
+  const bool dyn = dynamic_mode(p);
+  const QueueView q = queue_of(p);
+  const unsigned full = 0xffffffffu;
+  switch (t.type) {
+    case TK_NORM:
+      if (dyn) queue_push_warp(q, p.NC, [&](int i) { return task_enc(TK_ROUTER, t.blk, t.a, i); }, clk, lane);
+      break;
+    case TK_ROUTER:
+      if (fire) queue_push_warp(q, 1, [&](int) { return task_enc(TK_TOPK, t.blk, t.a, 0); }, clk, lane);
+      break;
+    case TK_TOPK:
+      if (fire) queue_push_warp(q, 1, [&](int) { return task_enc(TK_SCAN, t.blk, 0, 0); }, clk, lane);
+      break;
+    case TK_PERM:  // rows of expert e landed: ev_expert[e] -= rows of this block
+      for (int e0 = 0; e0 < p.E; e0 += 32) {
+        const int e = e0 + lane;
+        int f = 0;
+        if (e < p.E) {
+          const int n = __ldcg(B.blk_cnt + t.a * p.E + e);
+          if (n > 0) {
+            if (dyn) f = notify(&B.ev_expert[e], n) == 0;
+            else red_add_relaxed(&B.ev_expert[e], -n);
+          }
+        }
+        unsigned m = __ballot_sync(full, f);
+        while (m) {  // expert ready: fire the tiles of [exp_indptr[e], exp_indptr[e+1])
+          const int ee = e0 + __ffs(m) - 1;
+          m &= m - 1;
+          const int c0i = __ldcg(B.chunk_indptr + ee), nch = __ldcg(B.chunk_indptr + ee + 1) - c0i;
+          const int NT = p.NT_gu;
+          queue_push_warp(q, nch * NT, [&](int i) { return task_enc(TK_GU, t.blk, c0i + i / NT, i % NT); },
+                          clk, lane);
         }
       }
+      break;
+    case TK_GU:
+      if (fire) queue_push_warp(q, p.NT_dn, [&](int i) { return task_enc(TK_DN, t.blk, t.a, i); }, clk, lane);
+      break;
+    case TK_DN:
+      if (fire) {
+        // Finisher of the chunk: notify each token block by its number of rows
+        // (the chunk's rows are in ascending token order, so blocks form runs).
+        for (int r = lane; r < t.rows; r += 32) c->noti_rtok[r] = __ldcg(B.row_token + t.row0 + r) / kTB;
+        __syncwarp();
+        for (int r = lane; r < t.rows; r += 32) {
+          const int tb = c->noti_rtok[r];
+          if (r == 0 || c->noti_rtok[r - 1] != tb) {
+            int e = r + 1;
+            while (e < t.rows && c->noti_rtok[e] == tb) ++e;
+            if (!dyn) {
+              red_add_relaxed(&B.ev_tok[tb], -(e - r));
+            } else if (notify(&B.ev_tok[tb], e - r) == 0) {
+              queue_push(q, 1, [&](int) { return task_enc(TK_COMB, t.blk, tb, 0); }, clk);
+            }
+          }
+        }
+        __syncwarp();
+      }
+      break;
+    case TK_COMB:
+      if (dyn && t.blk + 1 < p.n_blocks)
+        queue_push_warp(q, 1, [&](int) { return task_enc(TK_NORM, t.blk + 1, t.a, 0); }, clk, lane);
+      break;
+    default:
+      break;
+  }
+}
+
+// Takes the finished tasks in batches of up to 8: one fence for the batch,
+// the primary updates in parallel (one lane per task), then the follow-ups.
+__device__ void run_notifier(const MegaParams& p, Ctrl* c, const Clock& clk) {
+  const int lane = lane_id();
+  const unsigned full = 0xffffffffu;
+  uint32_t nit = 0;
+  bool done = false;
+  while (!done) {
+    int n = 0;
+    if (lane == 0) {
+      if (mbar_wait(&c->nfull[nit % kNoti], (nit / kNoti) & 1, clk, 250)) {
+        n = 1;
+        while (n < kNoti && mbar_try_wait(&c->nfull[(nit + n) % kNoti], ((nit + n) / kNoti) & 1)) ++n;
+      } else {
+        n = -1;
+      }
     }
+    n = __shfl_sync(full, n, 0);
+    if (n < 0) break;
+    __syncwarp();
+    // Records up to (not including) a TERM are handled; TERM ends the loop.
+    int m = n;
+    for (int i = 0; i < n; ++i)
+      if (c->noti[(nit + i) % kNoti].type == TK_TERM) {
+        m = i;
+        done = true;
+        break;
+      }
+    __threadfence();  // the workers' writes (ordered by the mbarrier) precede the notifies
+    int fire = 0;
+    if (lane < m) fire = notify_primary(p, c->noti[(nit + lane) % kNoti]);
+    for (int i = 0; i < m; ++i) {
+      const Task t = c->noti[(nit + i) % kNoti];
+      notify_follow(p, c, t, __shfl_sync(full, fire, i), lane, clk);
+    }
+    __syncwarp();
+    if (lane == 0)
+      for (int i = 0; i < n; ++i) mbar_arrive(&c->nempty[(nit + i) % kNoti]);
+    nit += n;
   }
 }
 
 __device__ void run_workers(const MegaParams& p, Ctrl* c, uint8_t* simt, uint8_t* epi,
                             const Clock& clk) {
   const int wt = threadIdx.x - kWorkerWarp0 * 32;
-  uint32_t gemm_i = 0;
+  uint32_t gemm_i = 0, nit = 0;
   for (uint32_t ri = 0;; ++ri) {
     Task* slot = &c->wtask[ri & 1];
     if (wt == 0) {
       const int r = ri % kRing;
       if (mbar_wait(&c->rfull[r], (ri / kRing) & 1, clk, 210)) {
         *slot = c->ring[r];
+        *reinterpret_cast<volatile int*>(&c->started) = static_cast<int>(ri + 1);
       } else {
         slot->type = TK_TERM;
       }
@@ -764,6 +891,8 @@ __device__ void run_workers(const MegaParams& p, Ctrl* c, uint8_t* simt, uint8_t
       case TK_COMB: task_comb(p, t, wt); break;
       default: break;
     }
+    // Every task ends with a barrier of the 256 workers: its writes are done.
+    if (wt == 0 && t.type != TK_SCAN) hand_over(c, nit, t, clk);
     if (t.type == TK_TERM) break;
     if (p.ws.trace && wt == 0) {
       const int idx = static_cast<int>(atomicAdd(p.ws.trace, 1ull));
@@ -965,7 +1094,14 @@ __device__ void sched_static(const MegaParams& p, Ctrl* c, const Clock& clk) {
 __device__ void sched_dynamic(const MegaParams& p, Ctrl* c, const Clock& clk) {
   RingWriter rw{c, 0};
   const QueueView q = queue_of(p);
+  constexpr int kLookahead = 2;  // tasks popped but not yet started by the workers
   for (;;) {
+    // Pop only when this CTA is about to need work: a CTA that grabbed many
+    // ready tasks would leave other SMs idle.
+    const volatile int* started = &c->started;
+    if (!spin_until([&] { return static_cast<int>(rw.i) - *started < kLookahead; }, clk,
+                    DERR_TIMEOUT_QUEUE, 1, 0))
+      break;
     const int idx = atom_add_relaxed(q.head, 1);
     uint32_t desc = 0;
     bool have = false;
@@ -1015,6 +1151,7 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
   const Clock clk{globaltimer_ns() + p.timeout_ns, p.ws.status, p.ws.status_host};
   const int w = warp_id();
   if (threadIdx.x == 0) {
+    c->started = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&c->full[s], 1);
       mbar_init(&c->empty[s], 1);
@@ -1026,6 +1163,10 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&c->rfull[r], 1);
       mbar_init(&c->rempty[r], kRingConsumers);
+    }
+    for (int s = 0; s < kNoti; ++s) {
+      mbar_init(&c->nfull[s], 1);
+      mbar_init(&c->nempty[s], 1);
     }
     mbar_fence_init();
   }
@@ -1058,6 +1199,8 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
     if (lane_id() == 0) run_producer(p, c, base, clk);
   } else if (w == kWarpMma) {
     if (lane_id() == 0) run_mma(p, c, base, clk);
+  } else if (w == kWarpNotifier) {
+    run_notifier(p, c, clk);
   } else if (w >= kWorkerWarp0) {
     run_workers(p, c, simt, epi, clk);
   }

@@ -28,7 +28,8 @@
 namespace etc {
 namespace {
 
-constexpr int kSkThreads = 288;  // warp 0 producer + 8 consumer warps
+constexpr int kSkThreads = 320;  // warp 0 producer, 8 consumer warps, warp 9 notifier
+constexpr int kSkNotifierWarp = 9;
 constexpr int kSkConsumers = 256;
 constexpr int kSkMaxStages = 6;
 constexpr int kSkMaxRows = 8;
@@ -52,10 +53,15 @@ struct SkParams {
   long long fault_row;  // row whose event waits for one notify more (-1: none)
 };
 
+constexpr int kSkNotiRing = 16;  // reduced stages waiting for their notify
+
 struct SkCtrl {
   uint64_t full[kSkMaxStages];
   uint64_t empty[kSkMaxStages];
+  uint64_t noti_full[kSkNotiRing];
+  uint64_t noti_empty[kSkNotiRing];
   long long task[kSkMaxStages];
+  long long noti_task[kSkNotiRing];  // partial task whose B entries are written (-1: stop)
   long long go;  // task handed to all consumers (-1: stop)
   float red[8][kSkMaxRows];
 };
@@ -84,6 +90,10 @@ __global__ void __launch_bounds__(kSkThreads, 1) splitk_kernel(const __grid_cons
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&ctrl->full[s], 1);
       mbar_init(&ctrl->empty[s], 1);
+    }
+    for (int s = 0; s < kSkNotiRing; ++s) {
+      mbar_init(&ctrl->noti_full[s], 1);
+      mbar_init(&ctrl->noti_empty[s], 1);
     }
     mbar_fence_init();
     if (blockIdx.x == 0)  // re-arm the other parity for the next call, whatever its mode
@@ -125,11 +135,67 @@ __global__ void __launch_bounds__(kSkThreads, 1) splitk_kernel(const __grid_cons
       }
       ++it;
     }
+  } else if (threadIdx.x >= 32 * kSkNotifierWarp) {
+    // ---- notifier: partial_sum(i, j) notifies event i ("ij->i") ----
+    // The fence and the atomics are paid here, off the consumers' path: one
+    // fence covers every stage handed over so far, then one lane per row.
+    const int lane = threadIdx.x & 31;
+    uint32_t nit = 0;
+    bool done = false;
+    while (!done) {
+      int n = 0;
+      if (lane == 0) {
+        if (mbar_wait(&ctrl->noti_full[nit % kSkNotiRing], (nit / kSkNotiRing) & 1, clk, 102)) {
+          n = 1;
+          while (n < 8 && mbar_try_wait(&ctrl->noti_full[(nit + n) % kSkNotiRing],
+                                        ((nit + n) / kSkNotiRing) & 1))
+            ++n;
+        } else {
+          n = -1;
+        }
+      }
+      n = __shfl_sync(0xffffffffu, n, 0);
+      if (n < 0) break;
+      __syncwarp();
+      __threadfence();  // the consumers' B writes (ordered by the mbarrier) before the notifies
+      for (int i = 0; i < n; ++i) {
+        const long long t = ctrl->noti_task[(nit + i) % kSkNotiRing];
+        if (t < 0) {
+          done = true;
+          break;
+        }
+        const long long rb = t / p.n_split;
+        const int rows = static_cast<int>(min(static_cast<long long>(p.R), p.n_rows - rb * p.R));
+        if (lane < rows) {
+          const long long row = rb * p.R + lane;
+          if (p.mode == ETC_SCHED_DYNAMIC) {
+            // The notify that completes row i runs final_sum(i) at once (early push).
+            const int arrived = atom_add_acq_rel(&p.ev[row], 1) + 1;
+            if (arrived == row_target(p, row)) final_sum(p, row);
+          } else {
+            red_add_relaxed(&p.ev[row], 1);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0)
+        for (int i = 0; i < n; ++i) mbar_arrive(&ctrl->noti_empty[(nit + i) % kSkNotiRing]);
+      nit += n;
+    }
   } else if (threadIdx.x >= 32) {
-    // ---- consumers: reduce a stage, write B, notify ----
+    // ---- consumers: reduce a stage, write B, hand the notify over ----
     const int ct = threadIdx.x - 32;
     const int cw = ct >> 5, lane = ct & 31;
     const int n4 = p.tile / 4;
+    uint32_t nit = 0;
+    auto hand_over = [&](long long t) {  // consumer thread 0 only
+      const int ns = nit % kSkNotiRing;
+      if (mbar_wait(&ctrl->noti_empty[ns], ((nit / kSkNotiRing) & 1) ^ 1, clk, 103)) {
+        ctrl->noti_task[ns] = t;
+        mbar_arrive(&ctrl->noti_full[ns]);
+      }
+      ++nit;
+    };
     for (uint32_t it = 0;; ++it) {
       const int s = it % p.stages;
       const uint32_t par = (it / p.stages) & 1;
@@ -138,7 +204,10 @@ __global__ void __launch_bounds__(kSkThreads, 1) splitk_kernel(const __grid_cons
       if (ct == 0) ctrl->go = mbar_wait(&ctrl->full[s], par, clk, 101) ? ctrl->task[s] : -1;
       named_bar(1, kSkConsumers);
       const long long t = ctrl->go;
-      if (t < 0) break;
+      if (t < 0) {
+        if (ct == 0) hand_over(-1);
+        break;
+      }
       while (!mbar_try_wait(&ctrl->full[s], par)) {
       }  // phase already complete: makes the TMA bytes visible to this thread
       const long long rb = t / p.n_split;
@@ -173,11 +242,9 @@ __global__ void __launch_bounds__(kSkThreads, 1) splitk_kernel(const __grid_cons
         for (int w = 0; w < 8; ++w) v += ctrl->red[w][ct];
         const long long row = rb * p.R + ct;
         p.B[row * p.n_split + j] = v;
-        // partial_sum(i, j) notifies event i ("ij->i").
-        const int arrived = atom_add_acq_rel(&p.ev[row], 1) + 1;
-        if (p.mode == ETC_SCHED_DYNAMIC && arrived == row_target(p, row)) final_sum(p, row);
       }
-      named_bar(1, kSkConsumers);  // red[] reused next iteration
+      named_bar(1, kSkConsumers);  // B written; red[] reused next iteration
+      if (ct == 0) hand_over(t);
     }
     if (p.mode == ETC_SCHED_STATIC) {
       // final_sum(i) for this CTA's row blocks, each waiting on event i ("i->i").
