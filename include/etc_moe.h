@@ -228,9 +228,9 @@ int etc_splitk_check(void);
 
 /*
  * etc_splitk_rowsum for callers that must not allocate device memory: code
- * running while a CUDA graph is being captured, code inside an allocator or
- * memory-pool callback that may not re-enter the allocator, and runtimes that
- * reserve all device memory up front.  Same arguments, result and tolerance
+ * inside an allocator or memory-pool callback that may not re-enter the
+ * allocator, and runtimes that reserve all device memory up front and forbid
+ * allocation afterwards.  Same arguments, result and tolerance
  * as etc_splitk_rowsum; the paper has no counterpart of this entry point.
  *
  * Its scratch (partial sums, per-row counters, queue counters, status) is a

@@ -416,10 +416,9 @@ int etc_splitk_check(void) {
 // Split-K row sum that allocates nothing.
 //
 // Some callers cannot call cudaMalloc at the moment they need this operation:
-// code running while a CUDA graph is being captured, code inside an allocator
-// or a memory-pool callback that must not re-enter the allocator, and
-// runtimes that reserve all device memory up front and forbid allocation
-// later.  For them the scratch this kernel needs (the per-row partial sums B,
+// code inside an allocator or a memory-pool callback that must not re-enter
+// the allocator, and runtimes that reserve all device memory up front and
+// forbid allocation later.  For them the scratch this kernel needs (the per-row partial sums B,
 // the per-row event counters and the queue counters) lives in one fixed-size
 // array in the library's device image instead of a buffer from cudaMalloc.
 // The array exists on every GPU that loads the library and stays there until

@@ -1,8 +1,8 @@
 """The split-K entry point that allocates nothing.
 
 It serves callers that cannot call cudaMalloc when they need the operation
-(graph capture, allocator callbacks, runtimes that reserve all memory up
-front).  Its result must match the allocating entry point within the split-K
+(allocator or memory-pool callbacks that must not re-enter the allocator,
+runtimes that reserve all device memory up front).  Its result must match the allocating entry point within the split-K
 tolerance, on two calls in a row (the second reuses the fixed scratch the
 first left behind), and sizes beyond its fixed scratch must be refused.
 This file is collected last on purpose.
