@@ -38,6 +38,24 @@ ROUTER_BYTES = H * E * 2                                     # 524,288
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of ONE launch of the
+# headline kernel (dynamic megakernel, prefill T=4096), from one ncu capture.
+# Valid only for the kernel sources it was taken on: reported as null once any
+# of them changes.
+MEGAKERNEL_SOURCES = ("moe_kernel.cu", "moe_api.cu", "etc_internal.h", "etc_event.cuh", "etc_ptx.cuh")
+NCU_TRAFFIC = {"sources_sha256_16": "ce8865c8bc71d251", "bytes_per_launch": 1229872000 + 275685888}
+
+
+def megakernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for name in MEGAKERNEL_SOURCES:
+        with open(os.path.join(ROOT, "moe_layer_scheduling_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -249,6 +267,12 @@ def run_ours(args, rank, world):
 
     flops = T * FLOPS_PER_TOKEN
     achieved_tflops = flops / sec / 1e12
+    if megakernel_source_hash() == NCU_TRAFFIC["sources_sha256_16"]:
+        traffic = NCU_TRAFFIC["bytes_per_launch"]
+        traffic_src = ("bytes per launch, ncu dram__bytes_read.sum + dram__bytes_write.sum of one "
+                       "launch of this kernel on this workload")
+    else:
+        traffic, traffic_src = None, "kernel sources changed since the ncu capture"
     peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     results["prefill_T4096"] = {"us": sec * 1e6, "tok_s": T / sec, "tflops": achieved_tflops}
 
@@ -301,7 +325,8 @@ def run_ours(args, rank, world):
         },
         "roofline": {
             "bound": "tensor", "achieved": achieved_tflops, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved_tflops / peak, "traffic": None,
+            "frac": achieved_tflops / peak, "traffic": traffic,
+            "traffic_source": traffic_src,
             "kernel": "etc_moe_megakernel (dynamic)",
             "peak_source": f"bf16_tflops (burst) of {peak_src} MEASURED_PEAKS.json"
             if peak_src == "measured" else "fallback 1.9 PFLOP/s",
