@@ -66,7 +66,7 @@ typedef struct etc_plan_s* etc_plan_t;
 
 typedef struct {
   int hidden;        /* H: model width; multiple of 128 */
-  int n_experts;     /* E: 8..256, multiple of 8 */
+  int n_experts;     /* E: 8..128, multiple of 8 (one router tile holds all experts) */
   int top_k;         /* k: 1..min(E,16) */
   int inter;         /* I: expert intermediate width; multiple of 64 */
   int t_max;         /* largest token count a call may pass (>= 1) */
@@ -103,8 +103,10 @@ int etc_moe_plan(etc_plan_t* plan, const etc_moe_opts* opts);
  *   w_gate_up  bf16 [E, 2I, H]   rows 0..I-1 gate, rows I..2I-1 up (K-major)
  *   w_down     bf16 [E, H, I]    (K-major)
  *   out        fp32 [T, H] (bf16 [T, H] when opts.out_dtype = ETC_OUT_BF16)
- * Routing: top-k of the fp32 logits, ties to the lower expert id; weights =
- * softmax over the k selected logits.  Accumulation is fp32; the SwiGLU
+ * Routing: the logits are bf16 x bf16 products summed in fp32 on the tensor
+ * cores (when T is small, H is split into chunks whose partial sums are added
+ * exactly as 64-bit fixed point); top-k of the fp32 logits, ties to the lower
+ * expert id; weights = softmax over the k selected logits.  Accumulation is fp32; the SwiGLU
  * activation is rounded to bf16 (the operand of the second GEMM); each down
  * tile adds its weighted fp32 outputs into the token rows of `out` with
  * fp32 reductions in L2 (the order of the k additions per element is not
@@ -117,7 +119,8 @@ int etc_moe_forward(etc_plan_t plan, void* stream, const void* x, const void* ga
 
 /*
  * The same layer computed by the same task code, one kernel launch per stage
- * (router, top-k, scan, permute, gate/up, down, combine: 7 launches).  The
+ * (router, top-k, scan, permute, gate/up, down, combine: 7 launches; 6 when
+ * the top-k runs inside the router stage, i.e. when H is not split).  The
  * ablation baseline for the one-launch megakernel.  Same arguments and result.
  */
 int etc_moe_forward_unfused(etc_plan_t plan, void* stream, const void* x, const void* gate_w,

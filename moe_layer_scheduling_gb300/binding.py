@@ -188,7 +188,11 @@ def etc_moe_debug_buffer(plan: Plan, which: int, dst, stream=None):
 
 def etc_chain_forward(plan: Plan, x, norm_w, gate_w, router_bias, w_gate_up, w_down, T, out,
                       stream=None):
-    n = len(norm_w)
+    n = plan.opts.n_blocks
+    for name, ts in (("norm_w", norm_w), ("gate_w", gate_w), ("w_gate_up", w_gate_up),
+                     ("w_down", w_down), ("router_bias", router_bias)):
+        if ts is not None and len(ts) != n:
+            raise ValueError(f"{name}: the plan has {n} blocks, got {len(ts)} tensors")
     arr = ctypes.c_void_p * n
 
     def ptrs(ts):

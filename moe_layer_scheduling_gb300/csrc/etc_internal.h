@@ -28,7 +28,7 @@ constexpr int kDnRows = 128;        // output columns of H per down tile
 constexpr int kAccCols = 128;       // TMEM columns per accumulator buffer
 constexpr int kTmemCols = 256;      // two accumulator buffers
 constexpr int kMaxBlocks = 4;       // chain depth per launch
-constexpr int kMaxE = 256;
+constexpr int kMaxE = 128;        // experts: one M=128 router MMA covers them all
 constexpr int kMaxK = 16;
 constexpr int kStageABytes = 128 * kBK * 2;   // 16 KB: 128 weight rows
 constexpr int kStageBBytes = kBT * kBK * 2;   // 16 KB: up to 128 token rows
@@ -41,7 +41,6 @@ constexpr int kWorkerBytes = kSimtBytes > 2 * kEpiHalfBytes ? kSimtBytes : 2 * k
 constexpr int kCtrlBytes = 2048;
 constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kWorkerBytes + kCtrlBytes;
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
-constexpr int kRouterKStep = 32;    // K elements per router smem stage
 
 enum TaskType : int {
   TK_NONE = 0,
@@ -85,7 +84,6 @@ __host__ __device__ inline int task_b(uint32_t d) { return static_cast<int>(d & 
 
 // Per-block workspace (the chain keeps one per block).
 struct BlockWs {
-  float* partial;      // [T_pad, E] router logits when H is not split (NC == 1)
   unsigned long long* logit_fx;  // [T_pad, E] sum of H-chunk partials, fixed point 2^-40 (NC > 1)
   float* logits;       // [T_max, E] final fp32 logits (with bias)
   int* ids;            // [T_max, k]
@@ -94,7 +92,7 @@ struct BlockWs {
   int* row_token;      // [R_max] token of each expert-sorted row
   float* row_w;        // [R_max] routing weight of each expert-sorted row
   int* blk_cnt;        // [nb_max, E] per-token-block expert histogram
-  int* blk_off;        // [nb_max, E] first row of (token block, expert)
+  int* cnt_acc;        // [E] counts summed by the routing tasks; the scan reads and re-arms it
   int* counts;         // [E]
   int* exp_indptr;     // [E+1]
   int* chunk_indptr;   // [E+1]
@@ -142,6 +140,9 @@ struct MegaParams {
   CUtensorMap tm_act;              // [R_max, I] box 16x64
   CUtensorMap tm_xperm64;          // [R_max, H] box 64x64
   CUtensorMap tm_act64;            // [R_max, I] box 64x64
+  CUtensorMap tm_wg[kMaxBlocks];   // router weight [H, E], box 64 experts x 64 rows (MN-major A)
+  CUtensorMap tm_xr;               // router input rows [T, H] (x, or xn in the chain), box 32x64
+  CUtensorMap tm_xrlo;             // xn_lo [T_max, H] (chain), box 32x64
   Workspace ws;
   const __nv_bfloat16* x;
   void* out;     // fp32 [T, H], or bf16 when out_bf16
@@ -155,6 +156,7 @@ struct MegaParams {
   int use_norm;  // chain: RMSNorm before and residual after each block
   float eps;
   int T, nb, NC, HC, n_router, T_pad;
+  int KBr;       // 64-wide K blocks per router task (HC / 64)
   int NT_gu, NT_dn;
   unsigned epoch;
   int mode;  // 0 static, 1 dynamic

@@ -1,7 +1,7 @@
 // etc_ptx.cuh -- thin inline-PTX wrappers for sm_103a used by the Event Tensor
 // megakernels: gpu-scope acquire/release atomics, mbarriers, TMA (tiled and
-// bulk), tcgen05 (TMEM alloc, MMA, commit, load) and the legacy mma.sync used
-// by the small router contraction.
+// bulk) and tcgen05 (TMEM alloc, MMA with K- and MN-major operands, commit,
+// load).
 #pragma once
 
 #include <cuda.h>
@@ -229,53 +229,28 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major bf16 operand with 128-byte swizzle,
+// as TMA writes a box of 64 MN elements (128 B) x K rows: each K row is 128 B,
+// 8-row K groups are 1024 B apart (stride byte offset), and consecutive
+// 64-element MN groups are `mn_group_bytes` apart (leading byte offset).
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t smem_addr, uint32_t mn_group_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);          // start address
+  d |= static_cast<uint64_t>((mn_group_bytes >> 4) & 0x3FFFu) << 16;  // leading byte offset
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                       // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                               // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                               // 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor: kind::f16, A = B = bf16, D = fp32, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
-
-// ---------------------------------------------------------------------------
-// mma.sync m16n8k16 (router only) and ldmatrix
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                            uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                                  uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldmatrix_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r0), "=r"(r1)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// 16-byte async copy global -> shared; src_bytes < 16 zero-fills the rest.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// Same, with A read MN-major (transposed).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_amn(int M, int N) {
+  return idesc_bf16_f32(M, N) | (1u << 15);
 }
 
 }  // namespace etc

@@ -36,6 +36,12 @@ struct etc_plan_s {
   const void* cached_wgu[kMaxBlocks] = {};
   const void* cached_wd[kMaxBlocks] = {};
   CUtensorMap tm_wgu[kMaxBlocks]{}, tm_wd[kMaxBlocks]{};
+  const void* cached_wg[kMaxBlocks] = {};
+  CUtensorMap tm_wg[kMaxBlocks]{};
+  const void* cached_x = nullptr;  // router input map of the caller's x, per (pointer, T)
+  int cached_xT = 0;
+  CUtensorMap tm_x{};
+  CUtensorMap tm_xn{}, tm_xnlo{};  // router input maps of the chain's normalised rows
   unsigned epoch = 0;
   long long launches = 0;
   int last_T = 0;
@@ -43,13 +49,14 @@ struct etc_plan_s {
 
 namespace {
 
-// Router H-split for a call: enough (token block, H-chunk) tasks to cover the
-// grid, each chunk a multiple of 32 rows of H.
+// Router H-split for a call: with few token blocks, split H into NC chunks
+// (multiples of 64 rows) so that the router tiles still spread over the grid;
+// with enough blocks (nb > grid / 2) H stays whole and the top-k runs inside
+// the router tile.
 int choose_nc(int T, int H, int grid) {
   const int nb = (T + kTB - 1) / kTB;
   int nc = 1;
-  while (nb * nc < grid && nc < 32 && (H / (nc * 2)) % kRouterKStep == 0 && H / (nc * 2) >= 64)
-    nc *= 2;
+  while (nb * nc * 2 <= grid && (H / (nc * 2)) % kBK == 0) nc *= 2;
   return nc;
 }
 
@@ -78,8 +85,7 @@ struct Bump {
 
 void carve_block(Bump& data, Bump& ctrl, BlockWs& b, const etc_plan_s& p) {
   const size_t E = p.E, k = p.k, T = p.T_max, nb = p.nb_max, C = p.C_max, R = p.R_max;
-  b.partial = data.take<float>(static_cast<size_t>(nb) * kTB * E);
-  b.logit_fx = ctrl.take<unsigned long long>(static_cast<size_t>(nb) * kTB * E);
+  b.logit_fx = ctrl.take<unsigned long long>(static_cast<size_t>(p.partial_max) * E);
   b.logits = data.take<float>(T * E);
   b.ids = data.take<int>(T * k);
   b.wts = data.take<float>(T * k);
@@ -87,7 +93,7 @@ void carve_block(Bump& data, Bump& ctrl, BlockWs& b, const etc_plan_s& p) {
   b.row_token = data.take<int>(R);
   b.row_w = data.take<float>(R);
   b.blk_cnt = data.take<int>(nb * E);
-  b.blk_off = data.take<int>(nb * E);
+  b.cnt_acc = ctrl.take<int>(E);
   b.counts = data.take<int>(E);
   b.exp_indptr = data.take<int>(E + 1);
   b.chunk_indptr = data.take<int>(E + 1);
@@ -166,6 +172,16 @@ int weight_maps(etc_plan_t p, int b, const void* wgu, const void* wd) {
   return ETC_OK;
 }
 
+int router_weight_map(etc_plan_t p, int b, const void* gate_w) {
+  if (p->cached_wg[b] != gate_w) {
+    // [H, E] row-major, read as the MN-major A operand: boxes of 64 experts x 64 rows.
+    CUresult r = encode_tensor_map_2d_bf16(&p->tm_wg[b], gate_w, p->E, p->H, 64, kBK);
+    if (r != CUDA_SUCCESS) return set_error(ETC_ERR_CUDA, "tensor map (gate_w) failed: %d", r);
+    p->cached_wg[b] = gate_w;
+  }
+  return ETC_OK;
+}
+
 struct CallArgs {
   const void* x = nullptr;
   void* out = nullptr;
@@ -211,10 +227,16 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
 
   MegaParams prm;
   std::memset(&prm, 0, sizeof prm);
+  const bool router_tiles = a.logits_in == nullptr;
   for (int b = 0; b < a.n_blocks; ++b) {
     if (stage_hi >= TK_GU) {
       int r = weight_maps(p, b, a.wgu[b], a.wd[b]);
       if (r != ETC_OK) return r;
+    }
+    if (router_tiles) {
+      int r = router_weight_map(p, b, a.gate_w[b]);
+      if (r != ETC_OK) return r;
+      prm.tm_wg[b] = p->tm_wg[b];
     }
     prm.tm_wgu[b] = p->tm_wgu[b];
     prm.tm_wd[b] = p->tm_wd[b];
@@ -226,6 +248,21 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   prm.tm_act = p->tm_act;
   prm.tm_xperm64 = p->tm_xperm64;
   prm.tm_act64 = p->tm_act64;
+  if (router_tiles) {
+    if (a.use_norm) {
+      prm.tm_xr = p->tm_xn;
+      prm.tm_xrlo = p->tm_xnlo;
+    } else {
+      if (p->cached_x != a.x || p->cached_xT != a.T) {
+        // Rows past T read as zero: the map's extent is the call's T.
+        CUresult r = encode_tensor_map_2d_bf16(&p->tm_x, a.x, p->H, a.T, kBK, kTB);
+        if (r != CUDA_SUCCESS) return set_error(ETC_ERR_CUDA, "tensor map (x) failed: %d", r);
+        p->cached_x = a.x;
+        p->cached_xT = a.T;
+      }
+      prm.tm_xr = p->tm_x;
+    }
+  }
   prm.ws = p->ws;
   prm.x = static_cast<const __nv_bfloat16*>(a.x);
   prm.out = a.out;
@@ -241,8 +278,9 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   prm.eps = p->opts.rms_eps > 0.f ? p->opts.rms_eps : 1e-6f;
   prm.T = a.T;
   prm.nb = (a.T + kTB - 1) / kTB;
-  prm.NC = choose_nc(a.T, p->H, p->grid);
+  prm.NC = router_tiles ? choose_nc(a.T, p->H, p->grid) : 1;
   prm.HC = p->H / prm.NC;
+  prm.KBr = prm.HC / kBK;
   prm.n_router = prm.nb * prm.NC;
   prm.T_pad = prm.nb * kTB;
   prm.NT_gu = p->I / kGuRows;
@@ -271,6 +309,7 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
     g_launches.fetch_add(1);
   } else {
     for (int stg = TK_ROUTER; stg <= TK_COMB; ++stg) {
+      if (stg == TK_TOPK && prm.NC == 1) continue;  // top-k ran inside the router stage
       prm.stage_lo = prm.stage_hi = stg;
       ETC_CUDA_TRY(launch_megakernel(prm, p->grid, s));
       ++p->launches;
@@ -314,15 +353,17 @@ int etc_moe_plan(etc_plan_t* out, const etc_moe_opts* opts) {
   p->nb_max = (p->T_max + kTB - 1) / kTB;
   p->R_max = p->T_max * p->k;
   p->C_max = (p->R_max + kBT - 1) / kBT + p->E;
-  p->partial_max = 0;
-  for (int nb = 1; nb <= p->nb_max; ++nb) {  // the router split depends on T only through nb
-    const int T = std::min(nb * kTB, p->T_max);
-    p->partial_max = std::max<long long>(p->partial_max,
-                                         static_cast<long long>(choose_nc(T, p->H, p->grid)) * nb * kTB);
+  // Rows of fixed-point router sums: the token rows of the largest call whose
+  // H is split (the split depends on T only through nb).
+  p->partial_max = kTB;
+  long long n_router_max = p->nb_max;
+  for (int nb = 1; nb <= p->nb_max; ++nb) {
+    const int nc = choose_nc(std::min(nb * kTB, p->T_max), p->H, p->grid);
+    if (nc > 1) p->partial_max = std::max<long long>(p->partial_max, static_cast<long long>(nb) * kTB);
+    n_router_max = std::max<long long>(n_router_max, static_cast<long long>(nb) * nc);
   }
   {
     const int nb = p->nb_max;
-    const long long n_router_max = std::max<long long>(p->partial_max / kTB, nb);
     const long long per_block = nb /*norm*/ + n_router_max + nb + 1 + nb +
                                 static_cast<long long>(p->C_max) * (p->I / kGuRows + p->H / kDnRows) + nb;
     p->ws.qcap = static_cast<int>(per_block * p->n_blocks + 64);
@@ -356,11 +397,16 @@ int etc_moe_plan(etc_plan_t* out, const etc_moe_opts* opts) {
     if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 4)) != ETC_OK) return fail(r);
     p->ws.acc = static_cast<float*>(m);
   }
+  // Normalised rows of the chain (any plan may be given to etc_chain_forward,
+  // a one-block chain included).
+  if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 2)) != ETC_OK) return fail(r);
+  p->ws.xn = static_cast<__nv_bfloat16*>(m);
+  if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 2)) != ETC_OK) return fail(r);
+  p->ws.xn_lo = static_cast<__nv_bfloat16*>(m);
+  if (encode_tensor_map_2d_bf16(&p->tm_xn, p->ws.xn, p->H, p->T_max, kBK, kTB) != CUDA_SUCCESS ||
+      encode_tensor_map_2d_bf16(&p->tm_xnlo, p->ws.xn_lo, p->H, p->T_max, kBK, kTB) != CUDA_SUCCESS)
+    return fail(set_error(ETC_ERR_CUDA, "tensor map encoding of the normalised rows failed"));
   if (p->n_blocks > 1) {
-    if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 2)) != ETC_OK) return fail(r);
-    p->ws.xn = static_cast<__nv_bfloat16*>(m);
-    if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 2)) != ETC_OK) return fail(r);
-    p->ws.xn_lo = static_cast<__nv_bfloat16*>(m);
     if ((r = alloc_dev(p, &m, static_cast<size_t>(p->n_blocks - 1) * p->T_max * p->H * 4)) != ETC_OK)
       return fail(r);
     p->ws.resid = static_cast<float*>(m);

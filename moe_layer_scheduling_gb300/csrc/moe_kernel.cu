@@ -5,12 +5,15 @@
 // Tasks (one per tile) and the events between them:
 //
 //   NORM(b,tb)      chain only: RMSNorm of token block tb -> xn   flag norm_flag[tb]
-//   ROUTER(b,tb,c)  partial logits of token block tb over H-chunk c     -> ev_rblk[tb] (+1)
-//   TOPK(b,tb)      sums the NC partials, top-k, softmax over the top-k,
-//                   per-block expert histogram                          -> ev_route (+1)
-//   SCAN(b)         counts, exp_indptr, per-block row offsets, expert
-//                   chunks; DATA-DEPENDENT EVENT UPDATE: ev_expert[e] :=
-//                   counts[e]; publishes the plan                      flag plan_flag
+//   ROUTER(b,tb,c)  tcgen05 tile: logits of token block tb over H-chunk c.
+//                   H unsplit (NC == 1): bias, top-k, softmax over the
+//                   top-k and the block's expert histogram right here   -> ev_route (+1)
+//                   H split: fixed-point partial sums                  -> ev_rblk[tb] (+1)
+//   TOPK(b,tb)      H split only: sums the NC partials, top-k, softmax,
+//                   expert histogram                                    -> ev_route (+1)
+//   SCAN(b)         counts, exp_indptr, expert chunks; DATA-DEPENDENT
+//                   EVENT UPDATE: ev_expert[e] := counts[e]; publishes
+//                   the plan                                           flag plan_flag
 //   PERM(b,tb)      writes x_perm rows [exp_indptr[e] + rank]           -> ev_expert[e] (-n)
 //   GU(b,ch,n)      gate/up tile: 64 gate + 64 up weight rows x chunk
 //                   tokens, SwiGLU -> act                               -> ev_act[ch] (-1)
@@ -35,7 +38,9 @@
 //            writes them into a shared-memory ring
 //   warp 1   TMA producer (lane 0): weight and token tiles -> smem stages
 //   warp 2   tcgen05 issuer (lane 0); the warp owns 256 TMEM columns
-//   warps 4-11  workers: TMEM epilogues of the GEMM tiles and every SIMT task
+//   warp 3   notifier: event updates and dynamic early pushes
+//   warps 4-11  workers: TMEM epilogues of the router and GEMM tiles and
+//            every SIMT task
 //
 // GEMM tiles are "swap-AB": the MMA's M = 128 weight rows, its N = the
 // chunk's token rows rounded up to 16 (16..128).  Decode-sized chunks (a few
@@ -190,236 +195,195 @@ __device__ void task_norm(const MegaParams& p, const Task& t, int wt) {
       dst_lo[c] = f32_to_bf16x8(f);
     }
   }
-  named_bar(1, kNumWorkers);  // notify: norm_flag (by the notifier warp)
+  fence_proxy_async_global();  // xn / xn_lo are read next by TMA (router tiles)
+  named_bar(1, kNumWorkers);   // notify: norm_flag (by the notifier warp)
   (void)B;
 }
 
-// Router partial logits of token block tb over H-chunk c, on mma.sync
-// (a [32 x HC] x [HC x E] contraction; logits are fp32).  In the chain the
-// input is the normalised row split as hi + lo bf16 parts (two MMAs).
-__device__ void task_router(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
-  const int blk = t.blk, tb = t.a, ch = t.b;
-  const BlockWs& B = p.ws.blk[blk];
-  if (p.logits_in == nullptr) {
-    const bool split = p.use_norm != 0;
-    const __nv_bfloat16* X = split ? p.ws.xn : p.x;
-    const __nv_bfloat16* Wg = p.gate_w[blk];
-    const int E = p.E, H = p.H, ldw = E + 8, ldx = kRouterKStep + 8;
-    // NS-deep cp.async ring, as deep as the worker scratch allows (1..3).
-    const int stage_bytes = (2 * kTB * ldx + kRouterKStep * ldw) * 2;
-    const int NS = min(3, kSimtBytes / stage_bytes);
-    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(simt);       // [NS][2 hi/lo][32][40]
-    __nv_bfloat16* wsm = xs + NS * 2 * kTB * ldx;                     // [NS][32][E+8]
-    const int h0 = ch * p.HC, nks = p.HC / kRouterKStep;
-    const int ww = wt >> 5, lane = wt & 31;
-    auto load = [&](int ks, int buf) {
-      if (wt < kTB * 4 * (split ? 2 : 1)) {
-        const int part = wt >> 7, r = (wt >> 2) & 31, q = wt & 3;
-        const int tok = tb * kTB + r;
-        const __nv_bfloat16* src = (part ? p.ws.xn_lo : X) +
-            static_cast<size_t>(tok < p.T ? tok : p.T - 1) * H + h0 + ks * kRouterKStep + q * 8;
-        cp_async16(xs + ((buf * 2 + part) * kTB + r) * ldx + q * 8, src, tok < p.T ? 16 : 0);
-      }
-      const int per_row = E / 8;
-      for (int i = wt; i < kRouterKStep * per_row; i += kNumWorkers) {
-        const int r = i / per_row, q = i - r * per_row;
-        const __nv_bfloat16* src = Wg + static_cast<size_t>(h0 + ks * kRouterKStep + r) * E + q * 8;
-        cp_async16(wsm + (buf * kRouterKStep + r) * ldw + q * 8, src, 16);
-      }
-      cp_async_commit();
-    };
-    float acc[8][4];
+// ---------------------------------------------------------------------------
+// Routing.  A router task is a tcgen05 tile: A = the router weight [H, E]
+// read MN-major (TMEM lane = expert), B = the token block's 32 input rows
+// (column = token), K = the task's H range.  With H unsplit (NC == 1) the
+// epilogue adds the bias and runs the top-k at once; with H split over NC
+// tasks each adds its partial into exact fixed-point sums and a top-k task
+// of the block follows.
+// ---------------------------------------------------------------------------
+
+// Top-k of the tokens tok0.. of a block whose fp32 logits (bias included) are
+// in s_log [kTB][E]: one warp per token, ties to the lower expert id, weights
+// the softmax over the k selected logits.  Counts the experts in s_cnt.
+__device__ void topk_rows(const MegaParams& p, const BlockWs& B, const float* s_log, int tok0,
+                          int* s_cnt, int ww, int lane) {
+  const int E = p.E, k = p.k;
+  for (int r = ww; r < kTB; r += 8) {
+    const int tok = tok0 + r;
+    if (tok >= p.T) break;
+    float v[kMaxE / 32];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    const int mt = ww & 1, ng = ww >> 1, n8 = E / 8;
-    for (int s = 0; s < NS - 1; ++s) {
-      if (s < nks) load(s, s);
-      else cp_async_commit();  // keep one group per stage
-    }
-    for (int ks = 0; ks < nks; ++ks) {
-      const int nxt = ks + NS - 1;
-      if (nxt < nks) load(nxt, nxt % NS);
-      else cp_async_commit();
-      if (NS == 3) cp_async_wait<2>();  // stage ks has landed
-      else if (NS == 2) cp_async_wait<1>();
-      else cp_async_wait<0>();
-      named_bar(1, kNumWorkers);
-      const int buf = ks % NS;
+    for (int i = 0; i < kMaxE / 32; ++i)
+      v[i] = 32 * i + lane < E ? s_log[r * E + 32 * i + lane] : -INFINITY;
+    unsigned taken = 0;
+    float my_v = -INFINITY;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        uint32_t a0, a1, a2, a3, l0 = 0, l1 = 0, l2 = 0, l3 = 0;
-        ldmatrix_x4(smem_u32(xs + (buf * 2 * kTB + mt * 16 + (lane & 15)) * ldx + kk * 16 + (lane >> 4) * 8),
-                    a0, a1, a2, a3);
-        if (split)
-          ldmatrix_x4(smem_u32(xs + ((buf * 2 + 1) * kTB + mt * 16 + (lane & 15)) * ldx + kk * 16 +
-                               (lane >> 4) * 8),
-                      l0, l1, l2, l3);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int j = ng + 4 * i;
-          if (j < n8) {
-            uint32_t b0, b1;
-            ldmatrix_x2_trans(smem_u32(wsm + (buf * kRouterKStep + kk * 16 + (lane & 15)) * ldw + j * 8),
-                              b0, b1);
-            mma_bf16_16816(acc[i], a0, a1, a2, a3, b0, b1);
-            if (split) mma_bf16_16816(acc[i], l0, l1, l2, l3, b0, b1);
-          }
+      for (int i = 0; i < kMaxE / 32; ++i) {
+        const int e = 32 * i + lane;
+        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+          bv = v[i];
+          bi = e;
         }
       }
-      named_bar(1, kNumWorkers);
-    }
-    const int g = lane >> 2, tq = lane & 3;
-    // With H split over NC chunks the partials are summed exactly and in any
-    // order as 64-bit fixed point (units of 2^-40), so the logits do not
-    // depend on which chunk lands first.
-    auto put = [&](int tok, int e, float v) {
-      const size_t o = static_cast<size_t>(tok) * E + e;
-      if (p.NC == 1)
-        B.partial[o] = v;
-      else
-        red_add_u64(B.logit_fx + o, static_cast<unsigned long long>(
-                                        __double2ll_rn(static_cast<double>(v) * 1099511627776.0)));
-    };
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int j = ng + 4 * i;
-      if (j < n8) {
-        const int e = j * 8 + 2 * tq;
-        const int t0 = tb * kTB + mt * 16 + g;
-        if (t0 < p.T) {
-          put(t0, e, acc[i][0]);
-          put(t0, e + 1, acc[i][1]);
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
         }
-        if (t0 + 8 < p.T) {
-          put(t0 + 8, e, acc[i][2]);
-          put(t0 + 8, e + 1, acc[i][3]);
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        my_v = bv;
+        my_id = bi;
+      }
+    }
+    const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
+    const float ex = lane < k ? expf(my_v - v0) : 0.f;
+    float z = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    if (lane < k) {
+      B.ids[tok * k + lane] = my_id;
+      B.wts[tok * k + lane] = ex / z;
+      atomicAdd(&s_cnt[my_id], 1);
+    }
+  }
+}
+
+// The block's expert histogram: kept per block (the permute derives its row
+// offsets from it) and added into the call's counts (what the scan reads).
+__device__ __forceinline__ void publish_block_counts(const MegaParams& p, const BlockWs& B, int tb,
+                                                     const int* s_cnt, int wt) {
+  for (int e = wt; e < p.E; e += kNumWorkers) {
+    const int n = s_cnt[e];
+    B.blk_cnt[tb * p.E + e] = n;
+    if (n) atomicAdd(B.cnt_acc + e, n);
+  }
+}
+
+// Epilogue of a router tile of token block tb (TMEM lane = expert, column =
+// token; each worker warp reads its 32 lanes x 16 columns).
+__device__ void task_router_epilogue(const MegaParams& p, Ctrl* c, uint8_t* simt, const Task& t,
+                                     uint32_t& gemm_i, const Clock& clk, int wt, uint32_t iter) {
+  const int acc = gemm_i & 1;
+  const uint32_t aph = (gemm_i >> 1) & 1;
+  ++gemm_i;
+  int* flag = &c->wflag[iter & 1];
+  if (wt == 0) *flag = mbar_wait(&c->tfull[acc], aph, clk, 231) ? 1 : 0;
+  named_bar(1, kNumWorkers);
+  const bool ok = *flag != 0;
+  tc_fence_after();
+  const BlockWs& B = p.ws.blk[t.blk];
+  const int w = warp_id(), q = w & 3, h = (w - kWorkerWarp0) >> 2, lane = lane_id();
+  const int E = p.E, tb = t.a, e = 32 * q + lane, ww = wt >> 5;
+  int* s_cnt = reinterpret_cast<int*>(simt);             // [E]
+  float* s_log = reinterpret_cast<float*>(simt + 1024);  // [kTB][E]
+  for (int i = wt; i < E; i += kNumWorkers) s_cnt[i] = 0;
+  if (ok) {
+    float v[16];
+    tmem_ld16(c->tmem_base + acc * kAccCols + (static_cast<uint32_t>(32 * q) << 16) + h * 16, v);
+    if (e < E) {
+      if (p.NC == 1) {
+        const float b = p.bias[t.blk] ? __ldg(p.bias[t.blk] + e) : 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s_log[(h * 16 + i) * E + e] = v[i] + b;
+      } else {
+        // Partials over H-chunks are summed exactly, in any order, as 64-bit
+        // fixed point (units of 2^-40): the logits do not depend on which
+        // chunk lands first.
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int tok = tb * kTB + h * 16 + i;
+          if (tok < p.T)
+            red_add_u64(B.logit_fx + static_cast<size_t>(tok) * E + e,
+                        static_cast<unsigned long long>(
+                            __double2ll_rn(static_cast<double>(v[i]) * 1099511627776.0)));
         }
       }
     }
   }
-  named_bar(1, kNumWorkers);  // notify: ev_rblk[tb] (by the notifier warp)
+  tc_fence_before();
+  named_bar(1, kNumWorkers);
+  if (wt == 0) mbar_arrive(&c->tempty[acc]);  // accumulator free for the next tile
+  if (ok && p.NC == 1) {
+    const int tok0 = tb * kTB;
+    for (int idx = wt; idx < kTB * E; idx += kNumWorkers) {
+      const int r = idx / E;
+      if (tok0 + r < p.T) B.logits[static_cast<size_t>(tok0) * E + idx] = s_log[idx];
+    }
+    topk_rows(p, B, s_log, tok0, s_cnt, ww, lane);
+    named_bar(1, kNumWorkers);
+    publish_block_counts(p, B, tb, s_cnt, wt);
+  }
+  named_bar(1, kNumWorkers);  // notify: ev_route, or ev_rblk[tb] with H split (notifier warp)
 }
 
-// Top-k over the summed logits of token block tb; ties go to the lower id;
-// weights are the softmax over the k selected logits.
+// Top-k of token block tb as a SIMT task: from the NC summed partials (H
+// split), or from logits the caller gave (routing-only calls).
 __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
   const int blk = t.blk, tb = t.a;
   const BlockWs& B = p.ws.blk[blk];
-  const int E = p.E, k = p.k, ww = wt >> 5, lane = wt & 31;
-  int* s_cnt = reinterpret_cast<int*>(simt);                  // [E]
-  float* s_log = reinterpret_cast<float*>(simt + 1024);       // [G][E]
-  const int G = min(kTB, (24 * 1024) / (4 * E));              // tokens per pass
+  const int E = p.E, ww = wt >> 5, lane = wt & 31;
+  int* s_cnt = reinterpret_cast<int*>(simt);             // [E]
+  float* s_log = reinterpret_cast<float*>(simt + 1024);  // [kTB][E]
   for (int i = wt; i < E; i += kNumWorkers) s_cnt[i] = 0;
   const float* bias = p.bias[blk];
-  for (int g0 = 0; g0 < kTB; g0 += G) {
-    const int tok0 = tb * kTB + g0;
-    if (tok0 >= p.T) break;
-    // Phase 1, all threads: logits of G tokens x E experts (coalesced; the
-    // NC partials come from other CTAs, hence L2-only loads).
-    for (int idx = wt; idx < G * E; idx += kNumWorkers) {
-      const int r = idx / E, e = idx - r * E, tok = tok0 + r;
-      if (tok < p.T) {
-        float s;
-        if (p.logits_in) {
-          s = __ldg(p.logits_in + static_cast<size_t>(tok) * E + e);
-        } else {
-          const size_t o = static_cast<size_t>(tok) * E + e;
-          if (p.NC == 1) {
-            s = __ldcg(B.partial + o);
-          } else {
-            const long long v = static_cast<long long>(__ldcg(B.logit_fx + o));
-            B.logit_fx[o] = 0ull;  // consumed: re-armed for the next call
-            s = static_cast<float>(static_cast<double>(v) * 9.094947017729282379e-13);  // 2^-40
-          }
-          if (bias) s += __ldg(bias + e);
-        }
-        s_log[r * E + e] = s;
-        B.logits[static_cast<size_t>(tok) * E + e] = s;
+  const int tok0 = tb * kTB;
+  for (int idx = wt; idx < kTB * E; idx += kNumWorkers) {
+    const int r = idx / E, e = idx - r * E, tok = tok0 + r;
+    if (tok < p.T) {
+      const size_t o = static_cast<size_t>(tok) * E + e;
+      float s;
+      if (p.logits_in) {
+        s = __ldg(p.logits_in + o);
+      } else {
+        // written by other CTAs' router tiles: L2-only load
+        const long long v = static_cast<long long>(__ldcg(B.logit_fx + o));
+        B.logit_fx[o] = 0ull;  // consumed: re-armed for the next call
+        s = static_cast<float>(static_cast<double>(v) * 9.094947017729282379e-13);  // 2^-40
+        if (bias) s += __ldg(bias + e);
       }
+      s_log[idx] = s;
+      B.logits[o] = s;
     }
-    named_bar(1, kNumWorkers);
-    // Phase 2, one warp per token.
-    for (int r = ww; r < G; r += 8) {
-      const int tok = tok0 + r;
-      if (tok >= p.T) break;
-      float v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 32 * i + lane < E ? s_log[r * E + 32 * i + lane] : -INFINITY;
-      unsigned taken = 0;
-      float my_v = -INFINITY;
-      int my_id = 0;
-      for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int e = 32 * i + lane;
-          if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-            bv = v[i];
-            bi = e;
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (ov > bv || (ov == bv && oi < bi)) {
-            bv = ov;
-            bi = oi;
-          }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == j) {
-          my_v = bv;
-          my_id = bi;
-        }
-      }
-      const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
-      const float ex = lane < k ? expf(my_v - v0) : 0.f;
-      float z = ex;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-      if (lane < k) {
-        B.ids[tok * k + lane] = my_id;
-        B.wts[tok * k + lane] = ex / z;
-        atomicAdd(&s_cnt[my_id], 1);
-      }
-    }
-    named_bar(1, kNumWorkers);  // s_log reused by the next pass
   }
-  for (int i = wt; i < E; i += kNumWorkers) B.blk_cnt[tb * E + i] = s_cnt[i];
+  named_bar(1, kNumWorkers);
+  topk_rows(p, B, s_log, tok0, s_cnt, ww, lane);
+  named_bar(1, kNumWorkers);
+  publish_block_counts(p, B, tb, s_cnt, wt);
   named_bar(1, kNumWorkers);  // notify: ev_route (by the notifier warp)
 }
 
-// counts / exp_indptr / per-block offsets / expert chunks / event inits.
-// The token blocks are split over the 8 worker warps; lane l of every warp
-// owns experts l, l+32, ...
+// counts / exp_indptr / expert chunks / event inits, from the counts the
+// routing tasks summed (thread e < E owns expert e).
 __device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
   const int blk = t.blk;
   const BlockWs& B = p.ws.blk[blk];
-  const int E = p.E, nb = p.nb, ww = wt >> 5, lane = wt & 31;
-  int* tmp = reinterpret_cast<int*>(simt);               // scan scratch [32]
-  int* s_part = tmp + 32;                                 // [8][E] per-warp partial counts
-  int* s_row0 = s_part + 8 * kMaxE;                       // [E]
-  const int per = (nb + 7) / 8, tb_lo = min(nb, ww * per), tb_hi = min(nb, tb_lo + per);
-  int part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int tb = tb_lo; tb < tb_hi; ++tb) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (32 * i + lane < E) part[i] += __ldcg(B.blk_cnt + tb * E + 32 * i + lane);
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    if (32 * i + lane < E) s_part[ww * kMaxE + 32 * i + lane] = part[i];
-  named_bar(1, kNumWorkers);
+  const int E = p.E, nb = p.nb;
+  int* tmp = reinterpret_cast<int*>(simt);  // scan scratch [32]
   int cnt = 0;
-  if (wt < E)
-    for (int w = 0; w < 8; ++w) cnt += s_part[w * kMaxE + wt];
+  if (wt < E) {
+    cnt = __ldcg(B.cnt_acc + wt);
+    B.cnt_acc[wt] = 0;  // consumed: re-armed for the next call
+  }
   const int nch = (cnt + kBT - 1) / kBT;
   const int row0 = workers_excl_scan(cnt, tmp, wt);
   const int ch0 = workers_excl_scan(nch, tmp + 16, wt);
   if (wt < E) {
-    s_row0[wt] = row0;
     B.counts[wt] = cnt;
     B.exp_indptr[wt] = row0;
     B.chunk_indptr[wt] = ch0;
@@ -442,20 +406,6 @@ __device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int
     const int extra = ((p.debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT) && wt == p.debug_arg) ? 1 : 0;
     B.ev_expert[wt] = cnt + extra;
   }
-  named_bar(1, kNumWorkers);
-  // First row of (token block, expert): exp_indptr[e] + rows of e in earlier blocks.
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = 32 * i + lane;
-    if (e < E) {
-      int run = s_row0[e];
-      for (int w = 0; w < ww; ++w) run += s_part[w * kMaxE + e];
-      for (int tb = tb_lo; tb < tb_hi; ++tb) {
-        B.blk_off[tb * E + e] = run;
-        run += __ldcg(B.blk_cnt + tb * E + e);
-      }
-    }
-  }
   for (int tb = wt; tb < nb; tb += kNumWorkers)
     B.ev_tok[tb] = p.k * (min(p.T, tb * kTB + kTB) - tb * kTB);
   __threadfence();
@@ -465,7 +415,7 @@ __device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int
     const bool dyn = dynamic_mode(p);
     if (dyn) {
       const int n_chunks = B.meta[0];
-      const int blk_tasks = (p.use_norm ? nb : 0) + p.n_router + nb + 1 + nb +
+      const int blk_tasks = (p.use_norm ? nb : 0) + p.n_router + (p.NC > 1 ? nb : 0) + 1 + nb +
                             n_chunks * (p.NT_gu + p.NT_dn) + nb;
       const int acc = (blk == 0 ? 0 : *p.ws.qacc) + blk_tasks;
       *p.ws.qacc = acc;
@@ -504,9 +454,28 @@ __device__ void task_perm(const MegaParams& p, const Task& t, uint8_t* simt, int
   int* s_run = reinterpret_cast<int*>(simt);
   int* s_slot = s_run + kMaxE;
   int* s_ids = s_slot + kTB * kMaxK;
+  int* s_part = s_ids + kTB * kMaxK;  // [kNumWorkers]
   const int t0 = tb * kTB, ntok = min(kTB, p.T - t0), nslots = ntok * k;
-  for (int i = wt; i < E; i += kNumWorkers) s_run[i] = __ldcg(B.blk_off + tb * E + i);
+  // First row of each expert in this block: exp_indptr[e] plus the rows of e
+  // in the blocks before tb, summed from the block histograms by `per`
+  // threads per expert.
+  const int per = kNumWorkers / E;
+  {
+    const int e = wt % E, part = wt / E;
+    int sum = 0;
+    if (part < per) {
+#pragma unroll 4
+      for (int b = part; b < tb; b += per) sum += __ldcg(B.blk_cnt + b * E + e);
+    }
+    s_part[wt] = sum;
+  }
   for (int i = wt; i < nslots; i += kNumWorkers) s_ids[i] = __ldcg(B.ids + t0 * k + i);
+  named_bar(1, kNumWorkers);
+  for (int e = wt; e < E; e += kNumWorkers) {
+    int run = __ldcg(B.exp_indptr + e);
+    for (int j = 0; j < per; ++j) run += s_part[j * E + e];
+    s_run[e] = run;
+  }
   named_bar(1, kNumWorkers);
   if (ww == 0) {
     // Ranks in ascending token order; one token's k experts are distinct.
@@ -718,7 +687,15 @@ __device__ __forceinline__ int notify_primary(const MegaParams& p, const Task& t
     case TK_NORM:
       st_relaxed(reinterpret_cast<int*>(&B.norm_flag[t.a]), static_cast<int>(p.epoch));
       return 0;
-    case TK_ROUTER:  // partial logits of block tb landed ("ij->i" on ev_rblk)
+    case TK_ROUTER:
+      if (p.NC == 1) {  // block tb routed (top-k ran in the router task)
+        if (!dyn) {
+          red_add_relaxed(B.ev_route, 1);
+          return 0;
+        }
+        return atom_add_acq_rel(B.ev_route, 1) + 1 == p.nb;
+      }
+      // partial logits of block tb landed ("ij->i" on ev_rblk)
       if (!dyn) {
         red_add_relaxed(&B.ev_rblk[t.a], 1);
         return 0;
@@ -759,7 +736,10 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
       if (dyn) queue_push_warp(q, p.NC, [&](int i) { return task_enc(TK_ROUTER, t.blk, t.a, i); }, clk, lane);
       break;
     case TK_ROUTER:
-      if (fire) queue_push_warp(q, 1, [&](int) { return task_enc(TK_TOPK, t.blk, t.a, 0); }, clk, lane);
+      if (fire)
+        queue_push_warp(q, 1, [&](int) {
+          return p.NC == 1 ? task_enc(TK_SCAN, t.blk, 0, 0) : task_enc(TK_TOPK, t.blk, t.a, 0);
+        }, clk, lane);
       break;
     case TK_TOPK:
       if (fire) queue_push_warp(q, 1, [&](int) { return task_enc(TK_SCAN, t.blk, 0, 0); }, clk, lane);
@@ -882,7 +862,10 @@ __device__ void run_workers(const MegaParams& p, Ctrl* c, uint8_t* simt, uint8_t
     const unsigned long long t_start = p.ws.trace ? globaltimer_ns() : 0;
     switch (t.type) {
       case TK_NORM: task_norm(p, t, wt); break;
-      case TK_ROUTER: task_router(p, t, simt, wt); break;
+      case TK_ROUTER:
+        if (p.logits_in) task_topk(p, t, simt, wt);
+        else task_router_epilogue(p, c, simt, t, gemm_i, clk, wt, ri);
+        break;
       case TK_TOPK: task_topk(p, t, simt, wt); break;
       case TK_SCAN: task_scan(p, t, simt, wt); break;
       case TK_PERM: task_perm(p, t, simt, wt); break;
@@ -928,6 +911,26 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
   for (;;) {
     Task t;
     if (!ring_take(c, ri, t, clk, 220) || t.type == TK_TERM) break;
+    if (t.type == TK_ROUTER && !p.logits_in) {
+      // Router tile: per 64-row K block of H, the router weight's rows for
+      // experts 0-63 and 64-127 (two MN-major boxes; experts >= E read as
+      // zero) and the block's 32 input rows (the lo part second in the chain).
+      const int KB = p.KBr * (p.use_norm ? 2 : 1);
+      const uint32_t bytes = kStageABytes + kTB * kBK * 2;
+      fence_proxy_async_global();
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % kStages;
+        if (!mbar_wait(&c->empty[s], ((it / kStages) & 1) ^ 1, clk, 222)) return;
+        uint8_t* sa = base + s * kStageBytes;
+        const int part = kb >= p.KBr ? 1 : 0;
+        const int h = t.b * p.HC + (kb - part * p.KBr) * kBK;
+        mbar_arrive_expect_tx(&c->full[s], bytes);
+        tma_load_2d(sa, &p.tm_wg[t.blk], &c->full[s], 0, h);
+        tma_load_2d(sa + kStageABytes / 2, &p.tm_wg[t.blk], &c->full[s], 64, h);
+        tma_load_2d(sa + kStageABytes, part ? &p.tm_xrlo : &p.tm_xr, &c->full[s], h, t.a * kTB);
+      }
+      continue;
+    }
     if (t.type != TK_GU && t.type != TK_DN) continue;
     const bool gu = t.type == TK_GU;
     const CUtensorMap* ta = gu ? &p.tm_wgu[t.blk] : &p.tm_wd[t.blk];
@@ -969,23 +972,34 @@ __device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock
   for (;;) {
     Task t;
     if (!ring_take(c, ri, t, clk, 240) || t.type == TK_TERM) break;
-    if (t.type != TK_GU && t.type != TK_DN) continue;
+    const bool rt = t.type == TK_ROUTER && !p.logits_in;
+    if (!rt && t.type != TK_GU && t.type != TK_DN) continue;
     const int acc = tc & 1;
     if (!mbar_wait(&c->tempty[acc], ((tc >> 1) & 1) ^ 1, clk, 241)) return;
     tc_fence_after();
     const uint32_t d = tmem + acc * kAccCols;
-    const int npad = (t.rows + 15) & ~15;
-    const uint32_t idesc = idesc_bf16_f32(128, npad);
-    const int KB = (t.type == TK_GU ? p.H : p.I) / kBK;
+    const int npad = rt ? kTB : (t.rows + 15) & ~15;
+    // Router tiles read A (the router weight) MN-major; expert tiles K-major.
+    const uint32_t idesc = rt ? idesc_bf16_f32_amn(128, npad) : idesc_bf16_f32(128, npad);
+    const int KB = rt ? p.KBr * (p.use_norm ? 2 : 1) : (t.type == TK_GU ? p.H : p.I) / kBK;
     for (int kb = 0; kb < KB; ++kb, ++it) {
       const int s = it % kStages;
       if (!mbar_wait(&c->full[s], (it / kStages) & 1, clk, 242)) return;
       tc_fence_after();
-      const uint64_t ad = desc_kmajor_sw128(smem_u32(base + s * kStageBytes));
-      const uint64_t bd = desc_kmajor_sw128(smem_u32(base + s * kStageBytes + kStageABytes));
+      const uint32_t sa = smem_u32(base + s * kStageBytes);
+      const uint64_t bd = desc_kmajor_sw128(sa + kStageABytes);
+      if (rt) {
+        // 16 K rows per MMA: 2 KB further into each 64-expert box.
+        const uint64_t ad = desc_mnmajor_sw128(sa, kStageABytes / 2);
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)
-        umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          umma_bf16(d, ad + kk * (2048 >> 4), bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+      } else {
+        const uint64_t ad = desc_kmajor_sw128(sa);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+      }
       umma_commit(&c->empty[s]);  // stage free once these MMAs have read it
     }
     umma_commit(&c->tfull[acc]);  // accumulator ready
@@ -1047,7 +1061,7 @@ __device__ void sched_static(const MegaParams& p, Ctrl* c, const Clock& clk) {
         ok = ok && rw.emit(make_task(TK_ROUTER, blk, tb, i % p.NC), clk);
       }
     }
-    if (in(TK_TOPK)) {
+    if (in(TK_TOPK) && p.NC > 1) {
       for (int tb = cta; tb < p.nb && ok; tb += G) {
         ok = wait_geq(&B.ev_rblk[tb], p.NC, clk, TK_TOPK, tb);
         ok = ok && rw.emit(make_task(TK_TOPK, blk, tb, 0), clk);
@@ -1169,6 +1183,11 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
       mbar_init(&c->nempty[s], 1);
     }
     mbar_fence_init();
+  }
+  if (w == kWarpTma && lane_id() == 0 && p.stage_lo <= TK_ROUTER && !p.logits_in) {
+    for (int b = 0; b < p.n_blocks; ++b) tma_prefetch_desc(&p.tm_wg[b]);
+    tma_prefetch_desc(&p.tm_xr);
+    if (p.use_norm) tma_prefetch_desc(&p.tm_xrlo);
   }
   if (w == kWarpTma && lane_id() == 0 && p.stage_hi >= TK_GU) {
     for (int b = 0; b < p.n_blocks; ++b) {

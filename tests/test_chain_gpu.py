@@ -68,6 +68,20 @@ def _check_chain(plan, blocks, x, out, oracle_lib):
 
 
 @pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC])
+def test_chain_of_one_block(oracle_lib, blocks, blocks_dev, sched):
+    """n_blocks = 1: RMSNorm -> MoE -> residual, one launch."""
+    plan = B.etc_moe_plan(2048, 128, 8, 768, t_max=96, sched=sched, n_blocks=1)
+    x = inputs.tokens(70, 2048, 7100)
+    bd = {k: v[:1] for k, v in blocks_dev.items()}
+    out = _run_chain(plan, bd, x)
+    _check_chain(plan, blocks[:1], x, out, oracle_lib)
+    with pytest.raises(ValueError):
+        B.etc_chain_forward(plan, x.cuda(), blocks_dev["norm"], blocks_dev["gate"], None,
+                            blocks_dev["gu"], blocks_dev["dn"], 70, torch.empty(70, 2048, device="cuda"))
+    plan.close()
+
+
+@pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC])
 @pytest.mark.parametrize("T", [1, 37, 512])
 def test_chain_parity(oracle_lib, blocks, blocks_dev, sched, T):
     plan = B.etc_moe_plan(2048, 128, 8, 768, t_max=512, sched=sched, n_blocks=4)
