@@ -65,7 +65,7 @@ typedef enum { ETC_SCHED_STATIC = 0, ETC_SCHED_DYNAMIC = 1 } etc_sched_t;
 typedef struct etc_plan_s* etc_plan_t;
 
 typedef struct {
-  int hidden;        /* H: model width; multiple of 128 */
+  int hidden;        /* H: model width; multiple of 128, at most 12288 */
   int n_experts;     /* E: 8..128, multiple of 8 (one router tile holds all experts) */
   int top_k;         /* k: 1..min(E,16) */
   int inter;         /* I: expert intermediate width; multiple of 64 */

@@ -125,8 +125,9 @@ void carve_globals(Bump& ctrl, Workspace& w) {
 
 int validate_opts(const etc_moe_opts* o) {
   if (!o) return set_error(ETC_ERR_INVALID, "opts is NULL");
-  if (o->hidden <= 0 || o->hidden % 128 != 0)
-    return set_error(ETC_ERR_INVALID, "hidden=%d must be a positive multiple of 128", o->hidden);
+  if (o->hidden <= 0 || o->hidden % 128 != 0 || o->hidden > 12288)
+    return set_error(ETC_ERR_INVALID, "hidden=%d must be a multiple of 128 in [128, 12288]",
+                     o->hidden);
   if (o->n_experts < 8 || o->n_experts > kMaxE || o->n_experts % 8 != 0)
     return set_error(ETC_ERR_INVALID, "n_experts=%d must be a multiple of 8 in [8, %d]",
                      o->n_experts, kMaxE);

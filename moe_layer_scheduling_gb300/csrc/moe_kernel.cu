@@ -60,6 +60,9 @@ struct Task {
 };
 
 constexpr int kNoti = 8;  // finished tasks waiting for the notifier warp
+constexpr int kPermSlots = 6;                         // token rows in flight in a permute task
+constexpr int kPermRowOff = 8 * 1024;                 // row slots' offset in the worker scratch
+constexpr int kPermBytes = kSimtBytes - kPermRowOff;  // row slots' bytes
 
 struct Ctrl {
   uint64_t full[kStages];
@@ -70,6 +73,7 @@ struct Ctrl {
   uint64_t rempty[kRing];
   uint64_t nfull[kNoti];
   uint64_t nempty[kNoti];
+  uint64_t pbar[kPermSlots];  // permute row loads
   Task ring[kRing];
   Task wtask[2];     // workers' broadcast of the current task (double-buffered)
   Task noti[kNoti];  // workers -> notifier
@@ -101,6 +105,7 @@ __device__ __forceinline__ bool dynamic_mode(const MegaParams& p) { return p.mod
 // the caller's bf16 x for block 0, the fp32 residual stream after that.
 __device__ __forceinline__ void load_block_input8(const MegaParams& p, int blk, int tok, int c,
                                                   float (&f)[8]);
+__device__ void init_acc_rows(const MegaParams& p, int blk, int tb, int wt);
 
 // ---------------------------------------------------------------------------
 // small helpers
@@ -282,6 +287,8 @@ __device__ void task_router_epilogue(const MegaParams& p, Ctrl* c, uint8_t* simt
   const int acc = gemm_i & 1;
   const uint32_t aph = (gemm_i >> 1) & 1;
   ++gemm_i;
+  // While the tile is still on the tensor cores: the block's combine rows.
+  if (t.b == 0) init_acc_rows(p, t.blk, t.a, wt);
   int* flag = &c->wflag[iter & 1];
   if (wt == 0) *flag = mbar_wait(&c->tfull[acc], aph, clk, 231) ? 1 : 0;
   named_bar(1, kNumWorkers);
@@ -343,6 +350,7 @@ __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int
   for (int i = wt; i < E; i += kNumWorkers) s_cnt[i] = 0;
   const float* bias = p.bias[blk];
   const int tok0 = tb * kTB;
+  if (p.logits_in) init_acc_rows(p, blk, tb, wt);  // no router tile ran for this block
   for (int idx = wt; idx < kTB * E; idx += kNumWorkers) {
     const int r = idx / E, e = idx - r * E, tok = tok0 + r;
     if (tok < p.T) {
@@ -443,11 +451,32 @@ __device__ __forceinline__ float* acc_rows(const MegaParams& p, int blk) {
   return p.out_bf16 ? p.ws.acc : static_cast<float*>(p.out);
 }
 
-// Writes the rows of token block tb into x_perm at exp_indptr[e] + rank,
-// records each row's token and routing weight, and sets the block's combine
-// rows to their starting value (0, or the residual in the chain) before any
-// down tile adds into them.
-__device__ void task_perm(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
+// Combine rows of token block tb start at 0 (or at the block's input in the
+// chain) before any down tile adds into them.  Run by the block's routing
+// task, which every down tile of the block follows.  (A routing-only call
+// has no output rows.)
+__device__ void init_acc_rows(const MegaParams& p, int blk, int tb, int wt) {
+  float* accr = acc_rows(p, blk);
+  if (accr == nullptr) return;
+  const int ww = wt >> 5, lane = wt & 31, n8 = p.H / 8, t0 = tb * kTB, ntok = min(kTB, p.T - t0);
+  for (int r = ww; r < ntok; r += 8) {
+    const int tok = t0 + r;
+    float4* d = reinterpret_cast<float4*>(accr + static_cast<size_t>(tok) * p.H);
+    for (int c = lane; c < n8; c += 32) {
+      float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (p.use_norm) load_block_input8(p, blk, tok, c, x);
+      d[2 * c] = make_float4(x[0], x[1], x[2], x[3]);
+      d[2 * c + 1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+  }
+}
+
+// Writes the rows of token block tb into x_perm at exp_indptr[e] + rank and
+// records each row's token and routing weight.  The rows move through shared
+// memory with the bulk-copy engine: worker thread 0 reads each token row once
+// (kPermSlots rows in flight) and stores it to its k expert-sorted rows.
+__device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* simt, int wt,
+                          uint32_t& li, const Clock& clk) {
   const int blk = t.blk, tb = t.a;
   const BlockWs& B = p.ws.blk[blk];
   const int E = p.E, k = p.k, ww = wt >> 5, lane = wt & 31;
@@ -455,7 +484,18 @@ __device__ void task_perm(const MegaParams& p, const Task& t, uint8_t* simt, int
   int* s_slot = s_run + kMaxE;
   int* s_ids = s_slot + kTB * kMaxK;
   int* s_part = s_ids + kTB * kMaxK;  // [kNumWorkers]
+  uint8_t* rows = simt + kPermRowOff;
   const int t0 = tb * kTB, ntok = min(kTB, p.T - t0), nslots = ntok * k;
+  const __nv_bfloat16* src = p.use_norm ? p.ws.xn : p.x;
+  const uint32_t RB = static_cast<uint32_t>(p.H) * 2;
+  const int nslot = min(kPermSlots, kPermBytes / static_cast<int>(RB));
+  if (wt == 0) {
+    for (int r = 0; r < min(ntok, nslot); ++r) {
+      const int sl = (li + r) % nslot;
+      mbar_arrive_expect_tx(&c->pbar[sl], RB);
+      bulk_load(rows + sl * RB, src + static_cast<size_t>(t0 + r) * p.H, RB, &c->pbar[sl]);
+    }
+  }
   // First row of each expert in this block: exp_indptr[e] plus the rows of e
   // in the blocks before tb, summed from the block histograms by `per`
   // threads per expert.
@@ -496,40 +536,26 @@ __device__ void task_perm(const MegaParams& p, const Task& t, uint8_t* simt, int
     B.row_token[row] = t0 + i / k;
     B.row_w[row] = __ldcg(B.wts + t0 * k + i);
   }
-  const __nv_bfloat16* src = p.use_norm ? p.ws.xn : p.x;
-  const int n8 = p.H / 8;
-  // One warp per row; all eight 16-byte loads of a lane are in flight before its stores.
-  for (int s = ww; s < nslots; s += 8) {
-    const uint4* sr = reinterpret_cast<const uint4*>(src + static_cast<size_t>(t0 + s / k) * p.H);
-    uint4* dr = reinterpret_cast<uint4*>(p.ws.x_perm + static_cast<size_t>(s_slot[s]) * p.H);
-    for (int v0 = 0; v0 < n8; v0 += 256) {
-      uint4 a[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int v = v0 + lane + 32 * u;
-        if (v < n8) a[u] = __ldcg(sr + v);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int v = v0 + lane + 32 * u;
-        if (v < n8) dr[v] = a[u];
+  if (wt == 0) {
+    for (int r = 0; r < ntok; ++r) {
+      const uint32_t L = li + r;
+      const int sl = L % nslot;
+      if (!mbar_wait(&c->pbar[sl], (L / nslot) & 1, clk, 270)) break;
+      const uint8_t* srow = rows + sl * RB;
+      for (int j = 0; j < k; ++j)
+        bulk_store(p.ws.x_perm + static_cast<size_t>(s_slot[r * k + j]) * p.H, srow, RB);
+      bulk_commit();
+      const int nx = r + nslot;
+      if (nx < ntok) {
+        bulk_wait_read_all();  // the slot's row has been read out before it is refilled
+        mbar_arrive_expect_tx(&c->pbar[sl], RB);
+        bulk_load(rows + sl * RB, src + static_cast<size_t>(t0 + nx) * p.H, RB, &c->pbar[sl]);
       }
     }
+    bulk_wait_all();  // x_perm rows written before the notify
+    li += ntok;
   }
-  // Combine rows of this token block start at 0 (or at the block's input).
-  // (A routing-only call has no output rows.)
-  float* accr = acc_rows(p, blk);
-  for (int r = ww; accr != nullptr && r < ntok; r += 8) {
-    const int tok = t0 + r;
-    float4* d = reinterpret_cast<float4*>(accr + static_cast<size_t>(tok) * p.H);
-    for (int c = lane; c < n8; c += 32) {
-      float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (p.use_norm) load_block_input8(p, blk, tok, c, x);
-      d[2 * c] = make_float4(x[0], x[1], x[2], x[3]);
-      d[2 * c + 1] = make_float4(x[4], x[5], x[6], x[7]);
-    }
-  }
-  fence_proxy_async_global();  // x_perm is read next by TMA (async proxy)
+  fence_proxy_async_global();  // x_perm / row tables are read next by other CTAs' TMA
   named_bar(1, kNumWorkers);   // notify: ev_expert[e] per expert (by the notifier warp)
 }
 
@@ -844,7 +870,7 @@ __device__ void run_notifier(const MegaParams& p, Ctrl* c, const Clock& clk) {
 __device__ void run_workers(const MegaParams& p, Ctrl* c, uint8_t* simt, uint8_t* epi,
                             const Clock& clk) {
   const int wt = threadIdx.x - kWorkerWarp0 * 32;
-  uint32_t gemm_i = 0, nit = 0;
+  uint32_t gemm_i = 0, nit = 0, perm_li = 0;
   for (uint32_t ri = 0;; ++ri) {
     Task* slot = &c->wtask[ri & 1];
     if (wt == 0) {
@@ -868,7 +894,7 @@ __device__ void run_workers(const MegaParams& p, Ctrl* c, uint8_t* simt, uint8_t
         break;
       case TK_TOPK: task_topk(p, t, simt, wt); break;
       case TK_SCAN: task_scan(p, t, simt, wt); break;
-      case TK_PERM: task_perm(p, t, simt, wt); break;
+      case TK_PERM: task_perm(p, c, t, simt, wt, perm_li, clk); break;
       case TK_GU:
       case TK_DN: task_gemm_epilogue(p, c, epi, simt, t, gemm_i, clk, wt, ri); break;
       case TK_COMB: task_comb(p, t, wt); break;
@@ -1182,6 +1208,7 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
       mbar_init(&c->nfull[s], 1);
       mbar_init(&c->nempty[s], 1);
     }
+    for (int s = 0; s < kPermSlots; ++s) mbar_init(&c->pbar[s], 1);
     mbar_fence_init();
   }
   if (w == kWarpTma && lane_id() == 0 && p.stage_lo <= TK_ROUTER && !p.logits_in) {

@@ -56,7 +56,7 @@ def _opts(**kw):
 
 
 @pytest.mark.parametrize("bad", [
-    dict(hidden=100), dict(hidden=0), dict(n_experts=7), dict(n_experts=136), dict(n_experts=512),
+    dict(hidden=100), dict(hidden=0), dict(hidden=12416), dict(n_experts=7), dict(n_experts=136), dict(n_experts=512),
     dict(top_k=0),
     dict(top_k=17), dict(inter=100), dict(t_max=0), dict(sched=5), dict(n_blocks=0),
     dict(n_blocks=9), dict(router_bias=8),
