@@ -18,19 +18,26 @@ constexpr int kWarpTma = 1;         // lane 0: TMA producer
 constexpr int kWarpMma = 2;         // lane 0: tcgen05 issuer; warp owns TMEM
 constexpr int kWorkerWarp0 = 4;     // warps 4..11: epilogue + SIMT tasks
 constexpr int kNumWorkers = 256;
-constexpr int kStages = 6;          // smem operand stages
+constexpr int kStages = 4;          // smem operand stages
 constexpr int kRing = 8;            // smem task ring depth
 constexpr int kTB = 32;             // tokens per router/top-k/permute/combine task
 constexpr int kBT = 128;            // max rows (tokens) per expert chunk = max MMA N
 constexpr int kBK = 64;             // K elements per stage (one 128-byte swizzle row)
-constexpr int kGuRows = 64;         // gate rows (and up rows) per gate/up tile
-constexpr int kDnRows = 128;        // output columns of H per down tile
-constexpr int kAccCols = 128;       // TMEM columns per accumulator buffer
-constexpr int kTmemCols = 256;      // two accumulator buffers
+// Expert tiles come in two widths.  Narrow (decode-sized calls): one M=128
+// MMA per K step.  Wide (calls with many rows per expert): two M=128 MMAs
+// that share the token operand, i.e. 256 weight rows per tile and 25% fewer
+// operand bytes per FLOP.
+constexpr int kGuRows = 64;         // narrow: gate rows (and up rows) per gate/up tile
+constexpr int kDnRows = 128;        // narrow: output columns of H per down tile
+constexpr int kGuRowsW = 128;       // wide: gate rows (and up rows) per gate/up tile
+constexpr int kDnRowsW = 256;       // wide: output columns of H per down tile
+constexpr int kAccCols = 256;       // TMEM columns per accumulator buffer (two 128-column halves)
+constexpr int kTmemCols = 512;      // two accumulator buffers
 constexpr int kMaxBlocks = 4;       // chain depth per launch
 constexpr int kMaxE = 128;        // experts: one M=128 router MMA covers them all
 constexpr int kMaxK = 16;
-constexpr int kStageABytes = 128 * kBK * 2;   // 16 KB: 128 weight rows
+constexpr int kOpABytes = 128 * kBK * 2;      // 16 KB: one M=128 operand
+constexpr int kStageABytes = 2 * kOpABytes;   // 32 KB: up to 256 weight rows
 constexpr int kStageBBytes = kBT * kBK * 2;   // 16 KB: up to 128 token rows
 constexpr int kStageBytes = kStageABytes + kStageBBytes;
 // The worker warps run one task at a time, so the SIMT tasks' scratch and the
@@ -158,6 +165,7 @@ struct MegaParams {
   int T, nb, NC, HC, n_router, T_pad;
   int KBr;       // 64-wide K blocks per router task (HC / 64)
   int NT_gu, NT_dn;
+  int wide;      // expert tiles of 256 weight rows (two MMAs per K step)
   unsigned epoch;
   int mode;  // 0 static, 1 dynamic
   int stage_lo, stage_hi;

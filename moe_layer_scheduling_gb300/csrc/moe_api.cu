@@ -284,8 +284,11 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   prm.KBr = prm.HC / kBK;
   prm.n_router = prm.nb * prm.NC;
   prm.T_pad = prm.nb * kTB;
-  prm.NT_gu = p->I / kGuRows;
-  prm.NT_dn = p->H / kDnRows;
+  // Wide expert tiles once experts average 64 rows or more (and the shapes divide).
+  prm.wide = (static_cast<long long>(a.T) * p->k >= 64LL * p->E && p->I % kGuRowsW == 0 &&
+              p->H % kDnRowsW == 0) ? 1 : 0;
+  prm.NT_gu = p->I / (prm.wide ? kGuRowsW : kGuRows);
+  prm.NT_dn = p->H / (prm.wide ? kDnRowsW : kDnRows);
   if (++p->epoch == 0) p->epoch = 1;
   prm.epoch = p->epoch;
   prm.mode = mode;

@@ -613,7 +613,30 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
     named_bar(1, kNumWorkers);
   }
   if (ok) {
-    if (t.type == TK_GU) {
+    if (t.type == TK_GU && p.wide) {
+      // Wide: gate rows in the buffer's first half, up rows in its second;
+      // lane = intermediate column, so SwiGLU pairs them in registers.
+      for (int cb = h; cb < ncb; cb += 2) {
+        float g[16], u[16];
+        tmem_ld16(tbase + cb * 16, g);
+        tmem_ld16(tbase + kAccCols / 2 + cb * 16, u);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          S[i * 128 + i128] = __float2bfloat16_rn(g[i] / (1.0f + __expf(-g[i])) * u[i]);
+        named_bar(2 + h, 128);
+        // 16 token rows x 128 columns = 256 chunks of 16 bytes
+#pragma unroll
+        for (int rep = 0; rep < 2; ++rep) {
+          const int idx = i128 + 128 * rep, r = idx >> 4, chunk = idx & 15, tok = cb * 16 + r;
+          if (tok < t.rows) {
+            const uint4 val = *reinterpret_cast<const uint4*>(S + r * 128 + chunk * 8);
+            *reinterpret_cast<uint4*>(p.ws.act + static_cast<size_t>(t.row0 + tok) * p.I +
+                                      t.b * kGuRowsW + chunk * 8) = val;
+          }
+        }
+        named_bar(2 + h, 128);
+      }
+    } else if (t.type == TK_GU) {
       for (int cb = h; cb < ncb; cb += 2) {
         float v[16];
         tmem_ld16(tbase + cb * 16, v);
@@ -641,12 +664,16 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
         named_bar(2 + h, 128);
       }
     } else {
-      // Weighted combine fused here: out[token] += w * y, 4 columns per red op.
+      // Weighted combine fused here: out[token] += w * y, 4 columns per red op
+      // (wide tiles: two 128-column halves, one per accumulator half).
       float* S32 = reinterpret_cast<float*>(epi + h * kEpiHalfBytes);  // [16][128] fp32
-      float* accr = acc_rows(p, t.blk) + t.b * kDnRows;
-      for (int cb = h; cb < ncb; cb += 2) {
+      const int nhalf = p.wide ? 2 : 1;
+      for (int hc = 0; hc < nhalf * ncb; ++hc) {
+        const int half = hc / ncb, cb = hc - half * ncb;
+        if ((cb & 1) != h) continue;  // the two worker halves take alternate column blocks
+        float* accr = acc_rows(p, t.blk) + t.b * (p.wide ? kDnRowsW : kDnRows) + half * 128;
         float v[16];
-        tmem_ld16(tbase + cb * 16, v);
+        tmem_ld16(tbase + half * (kAccCols / 2) + cb * 16, v);
 #pragma unroll
         for (int i = 0; i < 16; ++i) S32[i * 128 + 32 * q + lane] = v[i];
         named_bar(2 + h, 128);
@@ -942,7 +969,7 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
       // experts 0-63 and 64-127 (two MN-major boxes; experts >= E read as
       // zero) and the block's 32 input rows (the lo part second in the chain).
       const int KB = p.KBr * (p.use_norm ? 2 : 1);
-      const uint32_t bytes = kStageABytes + kTB * kBK * 2;
+      const uint32_t bytes = kOpABytes + kTB * kBK * 2;  // two 64-expert boxes + 32 token rows
       fence_proxy_async_global();
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const int s = it % kStages;
@@ -952,7 +979,7 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
         const int h = t.b * p.HC + (kb - part * p.KBr) * kBK;
         mbar_arrive_expect_tx(&c->full[s], bytes);
         tma_load_2d(sa, &p.tm_wg[t.blk], &c->full[s], 0, h);
-        tma_load_2d(sa + kStageABytes / 2, &p.tm_wg[t.blk], &c->full[s], 64, h);
+        tma_load_2d(sa + kOpABytes / 2, &p.tm_wg[t.blk], &c->full[s], 64, h);
         tma_load_2d(sa + kStageABytes, part ? &p.tm_xrlo : &p.tm_xr, &c->full[s], h, t.a * kTB);
       }
       continue;
@@ -965,15 +992,23 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
     const int KB = (gu ? p.H : p.I) / kBK;
     const int nb16 = (t.rows + 15) >> 4;
     const int n64 = nb16 >> 2, r16 = nb16 & 3;  // token rows as 64-row boxes, then 16-row boxes
-    int rowA0, rowA1;
+    // Weight rows as 64-row boxes, 8 KB apart.  Narrow gate/up: 64 gate + 64
+    // up rows (one M=128 operand); wide: 128 gate rows, then 128 up rows (two
+    // operands); down tiles: consecutive output rows of w_down.
+    const bool wide = p.wide != 0;
+    const int nA = wide ? 4 : 2;
+    int rowA[4];
     if (gu) {
-      rowA0 = t.e * 2 * p.I + t.b * kGuRows;  // gate rows
-      rowA1 = rowA0 + p.I;                     // matching up rows
+      const int g0 = t.e * 2 * p.I + t.b * (wide ? kGuRowsW : kGuRows);
+      rowA[0] = g0;
+      rowA[1] = wide ? g0 + 64 : g0 + p.I;
+      rowA[2] = g0 + p.I;
+      rowA[3] = g0 + p.I + 64;
     } else {
-      rowA0 = t.e * p.H + t.b * kDnRows;
-      rowA1 = rowA0 + 64;
+      const int r0 = t.e * p.H + t.b * (wide ? kDnRowsW : kDnRows);
+      for (int i = 0; i < 4; ++i) rowA[i] = r0 + 64 * i;
     }
-    const uint32_t bytes = kStageABytes + nb16 * 16 * kBK * 2;
+    const uint32_t bytes = nA * (kOpABytes / 2) + nb16 * 16 * kBK * 2;
     fence_proxy_async_global();
     for (int kb = 0; kb < KB; ++kb, ++it) {
       const int s = it % kStages;
@@ -981,8 +1016,7 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
       uint8_t* sa = base + s * kStageBytes;
       uint8_t* sb = sa + kStageABytes;
       mbar_arrive_expect_tx(&c->full[s], bytes);
-      tma_load_2d(sa, ta, &c->full[s], kb * kBK, rowA0);
-      tma_load_2d(sa + kStageABytes / 2, ta, &c->full[s], kb * kBK, rowA1);
+      for (int i = 0; i < nA; ++i) tma_load_2d(sa + i * (kOpABytes / 2), ta, &c->full[s], kb * kBK, rowA[i]);
       for (int i = 0; i < n64; ++i)
         tma_load_2d(sb + i * 64 * kBK * 2, tb64, &c->full[s], kb * kBK, t.row0 + 64 * i);
       for (int i = 0; i < r16; ++i)
@@ -1016,7 +1050,7 @@ __device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock
       const uint64_t bd = desc_kmajor_sw128(sa + kStageABytes);
       if (rt) {
         // 16 K rows per MMA: 2 KB further into each 64-expert box.
-        const uint64_t ad = desc_mnmajor_sw128(sa, kStageABytes / 2);
+        const uint64_t ad = desc_mnmajor_sw128(sa, kOpABytes / 2);
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
           umma_bf16(d, ad + kk * (2048 >> 4), bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
@@ -1025,6 +1059,12 @@ __device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
           umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+        if (p.wide) {  // second 128 weight rows into the buffer's second half
+          const uint64_t ad1 = desc_kmajor_sw128(sa + kOpABytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16(d + kAccCols / 2, ad1 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+        }
       }
       umma_commit(&c->empty[s]);  // stage free once these MMAs have read it
     }

@@ -62,6 +62,24 @@ def test_ragged_token_counts(oracle_lib, sched, unfused, T, seed):
 
 
 @pytest.mark.parametrize("sched,unfused", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("T,seed", [(300, 4), (1100, 5)])
+def test_wide_tiles(oracle_lib, sched, unfused, T, seed):
+    # Enough rows per expert (T*k >= 64*E) for the 256-weight-row tiles:
+    # H=512, E=16, k=4, I=256, a skewing bias, ragged token and chunk tails.
+    w = inputs.moe_weights(512, 16, 4, 256, seed=seed)
+    w.router_bias = inputs.zipf_bias(16, 1.2, seed)
+    x = inputs.tokens(T, 512, seed + 50)
+    _full_check(oracle_lib, w, x, sched, unfused)
+
+
+@pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC])
+def test_qwen_wide_tiles_full_parity(oracle_lib, qwen, qwen_dev, sched):
+    # Qwen shape at T=1100: wide tiles, every token checked against the oracle.
+    x = inputs.tokens(1100, inputs.QWEN_H, 1100)
+    _full_check(oracle_lib, qwen, x, sched, False, dw=qwen_dev)
+
+
+@pytest.mark.parametrize("sched,unfused", MODES, ids=MODE_IDS)
 def test_prefill_skew_full_size(oracle_lib, qwen, qwen_dev, sched, unfused):
     # T=4096 with Zipf(1.2)-biased routing: empty experts and experts with
     # hundreds of rows.  Routing and dispatch are checked for all tokens; the
