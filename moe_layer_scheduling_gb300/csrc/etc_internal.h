@@ -18,7 +18,7 @@ constexpr int kWarpTma = 1;         // lane 0: TMA producer
 constexpr int kWarpMma = 2;         // lane 0: tcgen05 issuer; warp owns TMEM
 constexpr int kWorkerWarp0 = 4;     // warps 4..11: epilogue + SIMT tasks
 constexpr int kNumWorkers = 256;
-constexpr int kStages = 4;          // smem operand stages
+constexpr int kStagesMax = 6;       // smem operand stages (6 x 32 KB narrow, 4 x 48 KB wide)
 constexpr int kRing = 8;            // smem task ring depth
 constexpr int kTB = 32;             // tokens per router/top-k/permute/combine task
 constexpr int kBT = 128;            // max rows (tokens) per expert chunk = max MMA N
@@ -39,14 +39,16 @@ constexpr int kMaxK = 16;
 constexpr int kOpABytes = 128 * kBK * 2;      // 16 KB: one M=128 operand
 constexpr int kStageABytes = 2 * kOpABytes;   // 32 KB: up to 256 weight rows
 constexpr int kStageBBytes = kBT * kBK * 2;   // 16 KB: up to 128 token rows
-constexpr int kStageBytes = kStageABytes + kStageBBytes;
+constexpr int kStageRegion = 192 * 1024;      // the operand stages' shared memory
+static_assert(kStageRegion >= 4 * (kStageABytes + kStageBBytes), "wide stages do not fit");
+static_assert(kStageRegion >= kStagesMax * (kOpABytes + kStageBBytes), "narrow stages do not fit");
 // The worker warps run one task at a time, so the SIMT tasks' scratch and the
 // GEMM epilogues' staging share one region.
 constexpr int kSimtBytes = 32 * 1024;
 constexpr int kEpiHalfBytes = 8 * 1024;       // U (4 KB fp32) + S (4 KB bf16) per half
 constexpr int kWorkerBytes = kSimtBytes > 2 * kEpiHalfBytes ? kSimtBytes : 2 * kEpiHalfBytes;
 constexpr int kCtrlBytes = 2048;
-constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kWorkerBytes + kCtrlBytes;
+constexpr int kSmemBytes = 1024 /*align slack*/ + kStageRegion + kWorkerBytes + kCtrlBytes;
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
 
 enum TaskType : int {

@@ -65,8 +65,8 @@ constexpr int kPermRowOff = 8 * 1024;                 // row slots' offset in th
 constexpr int kPermBytes = kSimtBytes - kPermRowOff;  // row slots' bytes
 
 struct Ctrl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kStagesMax];
+  uint64_t empty[kStagesMax];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t rfull[kRing];
@@ -100,6 +100,19 @@ __device__ __forceinline__ QueueView queue_of(const MegaParams& p) {
 }
 
 __device__ __forceinline__ bool dynamic_mode(const MegaParams& p) { return p.mode == ETC_SCHED_DYNAMIC; }
+
+// Operand stages of a call: narrow tiles 6 x 32 KB (16 KB of weights, then up
+// to 16 KB of token rows), wide tiles 4 x 48 KB (32 KB of weights, then the
+// token rows).
+struct StageGeom {
+  int n;          // stages
+  uint32_t bytes; // stride
+  uint32_t boff;  // token operand offset in a stage
+};
+__device__ __forceinline__ StageGeom stage_geom(const MegaParams& p) {
+  return p.wide ? StageGeom{4, kStageABytes + kStageBBytes, kStageABytes}
+                : StageGeom{kStagesMax, kOpABytes + kStageBBytes, kOpABytes};
+}
 
 // Eight consecutive values of block blk's input row `tok` (columns 8c..8c+7):
 // the caller's bf16 x for block 0, the fp32 residual stream after that.
@@ -960,7 +973,9 @@ __device__ __forceinline__ bool ring_take(Ctrl* c, uint32_t& ri, Task& t, const 
 }
 
 __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock& clk) {
-  uint32_t ri = 0, it = 0;
+  uint32_t ri = 0, ph = 0;  // stage slot and its phase, advanced without division
+  int st = 0;
+  const StageGeom g = stage_geom(p);
   for (;;) {
     Task t;
     if (!ring_take(c, ri, t, clk, 220) || t.type == TK_TERM) break;
@@ -971,16 +986,16 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
       const int KB = p.KBr * (p.use_norm ? 2 : 1);
       const uint32_t bytes = kOpABytes + kTB * kBK * 2;  // two 64-expert boxes + 32 token rows
       fence_proxy_async_global();
-      for (int kb = 0; kb < KB; ++kb, ++it) {
-        const int s = it % kStages;
-        if (!mbar_wait(&c->empty[s], ((it / kStages) & 1) ^ 1, clk, 222)) return;
-        uint8_t* sa = base + s * kStageBytes;
+      for (int kb = 0; kb < KB; ++kb, st = st + 1 == g.n ? (ph ^= 1, 0) : st + 1) {
+        const int s = st;
+        if (!mbar_wait(&c->empty[s], ph ^ 1, clk, 222)) return;
+        uint8_t* sa = base + s * g.bytes;
         const int part = kb >= p.KBr ? 1 : 0;
         const int h = t.b * p.HC + (kb - part * p.KBr) * kBK;
         mbar_arrive_expect_tx(&c->full[s], bytes);
         tma_load_2d(sa, &p.tm_wg[t.blk], &c->full[s], 0, h);
         tma_load_2d(sa + kOpABytes / 2, &p.tm_wg[t.blk], &c->full[s], 64, h);
-        tma_load_2d(sa + kStageABytes, part ? &p.tm_xrlo : &p.tm_xr, &c->full[s], h, t.a * kTB);
+        tma_load_2d(sa + g.boff, part ? &p.tm_xrlo : &p.tm_xr, &c->full[s], h, t.a * kTB);
       }
       continue;
     }
@@ -1010,11 +1025,11 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
     }
     const uint32_t bytes = nA * (kOpABytes / 2) + nb16 * 16 * kBK * 2;
     fence_proxy_async_global();
-    for (int kb = 0; kb < KB; ++kb, ++it) {
-      const int s = it % kStages;
-      if (!mbar_wait(&c->empty[s], ((it / kStages) & 1) ^ 1, clk, 221)) return;
-      uint8_t* sa = base + s * kStageBytes;
-      uint8_t* sb = sa + kStageABytes;
+    for (int kb = 0; kb < KB; ++kb, st = st + 1 == g.n ? (ph ^= 1, 0) : st + 1) {
+      const int s = st;
+      if (!mbar_wait(&c->empty[s], ph ^ 1, clk, 221)) return;
+      uint8_t* sa = base + s * g.bytes;
+      uint8_t* sb = sa + g.boff;
       mbar_arrive_expect_tx(&c->full[s], bytes);
       for (int i = 0; i < nA; ++i) tma_load_2d(sa + i * (kOpABytes / 2), ta, &c->full[s], kb * kBK, rowA[i]);
       for (int i = 0; i < n64; ++i)
@@ -1027,7 +1042,9 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
 }
 
 __device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock& clk) {
-  uint32_t ri = 0, it = 0, tc = 0;
+  uint32_t ri = 0, tc = 0, ph = 0;  // stage slot and its phase, advanced without division
+  int st = 0;
+  const StageGeom g = stage_geom(p);
   const uint32_t tmem = c->tmem_base;
   for (;;) {
     Task t;
@@ -1042,12 +1059,12 @@ __device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock
     // Router tiles read A (the router weight) MN-major; expert tiles K-major.
     const uint32_t idesc = rt ? idesc_bf16_f32_amn(128, npad) : idesc_bf16_f32(128, npad);
     const int KB = rt ? p.KBr * (p.use_norm ? 2 : 1) : (t.type == TK_GU ? p.H : p.I) / kBK;
-    for (int kb = 0; kb < KB; ++kb, ++it) {
-      const int s = it % kStages;
-      if (!mbar_wait(&c->full[s], (it / kStages) & 1, clk, 242)) return;
+    for (int kb = 0; kb < KB; ++kb, st = st + 1 == g.n ? (ph ^= 1, 0) : st + 1) {
+      const int s = st;
+      if (!mbar_wait(&c->full[s], ph, clk, 242)) return;
       tc_fence_after();
-      const uint32_t sa = smem_u32(base + s * kStageBytes);
-      const uint64_t bd = desc_kmajor_sw128(sa + kStageABytes);
+      const uint32_t sa = smem_u32(base + s * g.bytes);
+      const uint64_t bd = desc_kmajor_sw128(sa + g.boff);
       if (rt) {
         // 16 K rows per MMA: 2 KB further into each 64-expert box.
         const uint64_t ad = desc_mnmajor_sw128(sa, kOpABytes / 2);
@@ -1225,14 +1242,14 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* simt = base + kStages * kStageBytes;
+  uint8_t* simt = base + kStageRegion;
   uint8_t* epi = simt;  // shared with the SIMT scratch (one worker task at a time)
   Ctrl* c = reinterpret_cast<Ctrl*>(simt + kWorkerBytes);
   const Clock clk{globaltimer_ns() + p.timeout_ns, p.ws.status, p.ws.status_host};
   const int w = warp_id();
   if (threadIdx.x == 0) {
     c->started = 0;
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kStagesMax; ++s) {
       mbar_init(&c->full[s], 1);
       mbar_init(&c->empty[s], 1);
     }
