@@ -119,9 +119,11 @@ int etc_moe_forward(etc_plan_t plan, void* stream, const void* x, const void* ga
 
 /*
  * The same layer computed by the same task code, one kernel launch per stage
- * (router, top-k, scan, permute, gate/up, down, combine: 7 launches; 6 when
- * the top-k runs inside the router stage, i.e. when H is not split).  The
- * ablation baseline for the one-launch megakernel.  Same arguments and result.
+ * that has work (router, top-k, scan, permute, gate/up, down, combine: 5 to 7
+ * launches: no top-k launch when the top-k runs inside the router stage, i.e.
+ * when H is not split; no combine launch for an fp32 output, which is complete
+ * after the down stage).  The ablation baseline for the one-launch
+ * megakernel.  Same arguments and result.
  */
 int etc_moe_forward_unfused(etc_plan_t plan, void* stream, const void* x, const void* gate_w,
                             const void* w_gate_up, const void* w_down, int T, void* out);

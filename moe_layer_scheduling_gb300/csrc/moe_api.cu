@@ -314,6 +314,7 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   } else {
     for (int stg = TK_ROUTER; stg <= TK_COMB; ++stg) {
       if (stg == TK_TOPK && prm.NC == 1) continue;  // top-k ran inside the router stage
+      if (stg == TK_COMB && !prm.out_bf16 && a.n_blocks == 1) continue;  // nothing to finalise
       prm.stage_lo = prm.stage_hi = stg;
       ETC_CUDA_TRY(launch_megakernel(prm, p->grid, s));
       ++p->launches;

@@ -101,6 +101,13 @@ __device__ __forceinline__ QueueView queue_of(const MegaParams& p) {
 
 __device__ __forceinline__ bool dynamic_mode(const MegaParams& p) { return p.mode == ETC_SCHED_DYNAMIC; }
 
+// Whether block blk's combine finaliser has work: releasing the next block's
+// RMSNorm in the chain, or rounding the last block's rows to a bf16 output.
+// Otherwise the down tiles' fp32 additions are the result and no COMB runs.
+__device__ __forceinline__ bool needs_comb(const MegaParams& p, int blk) {
+  return blk < p.n_blocks - 1 || p.out_bf16 != 0;
+}
+
 // Operand stages of a call: narrow tiles 6 x 32 KB (16 KB of weights, then up
 // to 16 KB of token rows), wide tiles 4 x 48 KB (32 KB of weights, then the
 // token rows).
@@ -427,8 +434,9 @@ __device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int
     const int extra = ((p.debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT) && wt == p.debug_arg) ? 1 : 0;
     B.ev_expert[wt] = cnt + extra;
   }
-  for (int tb = wt; tb < nb; tb += kNumWorkers)
-    B.ev_tok[tb] = p.k * (min(p.T, tb * kTB + kTB) - tb * kTB);
+  if (needs_comb(p, blk))
+    for (int tb = wt; tb < nb; tb += kNumWorkers)
+      B.ev_tok[tb] = p.k * (min(p.T, tb * kTB + kTB) - tb * kTB);
   __threadfence();
   named_bar(1, kNumWorkers);
   if (wt == 0) {
@@ -437,7 +445,7 @@ __device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int
     if (dyn) {
       const int n_chunks = B.meta[0];
       const int blk_tasks = (p.use_norm ? nb : 0) + p.n_router + (p.NC > 1 ? nb : 0) + 1 + nb +
-                            n_chunks * (p.NT_gu + p.NT_dn) + nb;
+                            n_chunks * (p.NT_gu + p.NT_dn) + (needs_comb(p, blk) ? nb : 0);
       const int acc = (blk == 0 ? 0 : *p.ws.qacc) + blk_tasks;
       *p.ws.qacc = acc;
       if (blk == p.n_blocks - 1) *p.ws.qtotal = acc;
@@ -810,33 +818,64 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
     case TK_TOPK:
       if (fire) queue_push_warp(q, 1, [&](int) { return task_enc(TK_SCAN, t.blk, 0, 0); }, clk, lane);
       break;
-    case TK_PERM:  // rows of expert e landed: ev_expert[e] -= rows of this block
-      for (int e0 = 0; e0 < p.E; e0 += 32) {
-        const int e = e0 + lane;
-        int f = 0;
-        if (e < p.E) {
-          const int n = __ldcg(B.blk_cnt + t.a * p.E + e);
-          if (n > 0) {
-            if (dyn) f = notify(&B.ev_expert[e], n) == 0;
-            else red_add_relaxed(&B.ev_expert[e], -n);
+    case TK_PERM: {  // rows of expert e landed: ev_expert[e] -= rows of this block
+      // Lane l owns experts l, l+32, ...: their notifies go out together, then
+      // the tiles of [exp_indptr[e], exp_indptr[e+1]) of every expert this
+      // block completed are pushed under one queue reservation.
+      constexpr int kEL = kMaxE / 32;
+      int n[kEL], tiles[kEL], c0[kEL];
+#pragma unroll
+      for (int i = 0; i < kEL; ++i) {
+        const int e = 32 * i + lane;
+        n[i] = e < p.E ? __ldcg(B.blk_cnt + t.a * p.E + e) : 0;
+      }
+      int mine = 0;
+#pragma unroll
+      for (int i = 0; i < kEL; ++i) {
+        tiles[i] = 0;
+        if (n[i] > 0) {
+          const int e = 32 * i + lane;
+          if (!dyn) {
+            red_add_relaxed(&B.ev_expert[e], -n[i]);
+          } else if (notify(&B.ev_expert[e], n[i]) == 0) {
+            c0[i] = __ldcg(B.chunk_indptr + e);
+            tiles[i] = (__ldcg(B.chunk_indptr + e + 1) - c0[i]) * p.NT_gu;
+            mine += tiles[i];
           }
         }
-        unsigned m = __ballot_sync(full, f);
-        while (m) {  // expert ready: fire the tiles of [exp_indptr[e], exp_indptr[e+1])
-          const int ee = e0 + __ffs(m) - 1;
-          m &= m - 1;
-          const int c0i = __ldcg(B.chunk_indptr + ee), nch = __ldcg(B.chunk_indptr + ee + 1) - c0i;
-          const int NT = p.NT_gu;
-          queue_push_warp(q, nch * NT, [&](int i) { return task_enc(TK_GU, t.blk, c0i + i / NT, i % NT); },
-                          clk, lane);
+      }
+      if (!dyn) break;
+      int off = mine;  // inclusive prefix over the lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(full, off, o);
+        if (lane >= o) off += y;
+      }
+      const int total = __shfl_sync(full, off, 31);
+      if (total == 0) break;
+      int base = 0;
+      if (lane == 0) base = q.n_seed + atom_add_relaxed(q.tail, total);
+      base = __shfl_sync(full, base, 0) + off - mine;
+      __threadfence();  // what the notifies acquired is published with the slots
+      const int NT = p.NT_gu;
+#pragma unroll
+      for (int i = 0; i < kEL; ++i) {
+        for (int j = 0; j < tiles[i]; ++j, ++base) {
+          if (base >= q.cap) {
+            raise_error(clk, DERR_QUEUE_OVERFLOW, 2, base);
+            break;
+          }
+          st_relaxed_u64(&q.slots[base], (static_cast<unsigned long long>(q.epoch) << 32) |
+                                              task_enc(TK_GU, t.blk, c0[i] + j / NT, j % NT));
         }
       }
       break;
+    }
     case TK_GU:
       if (fire) queue_push_warp(q, p.NT_dn, [&](int i) { return task_enc(TK_DN, t.blk, t.a, i); }, clk, lane);
       break;
     case TK_DN:
-      if (fire) {
+      if (fire && needs_comb(p, t.blk)) {
         // Finisher of the chunk: notify each token block by its number of rows
         // (the chunk's rows are in ascending token order, so blocks form runs).
         for (int r = lane; r < t.rows; r += 32) c->noti_rtok[r] = __ldcg(B.row_token + t.row0 + r) / kTB;
@@ -1178,7 +1217,7 @@ __device__ void sched_static(const MegaParams& p, Ctrl* c, const Clock& clk) {
         ok = ok && rw.emit(t, clk);
       }
     }
-    if (in(TK_COMB)) {
+    if (in(TK_COMB) && needs_comb(p, blk)) {
       for (int tb = cta; tb < p.nb && ok; tb += G) {
         ok = wait_zero(&B.ev_tok[tb], clk, TK_COMB, tb);
         ok = ok && rw.emit(make_task(TK_COMB, blk, tb, 0), clk);

@@ -53,6 +53,7 @@ def main():
     ap.add_argument("--skew", action="store_true", help="Zipf(1.2) router bias (prefill workload)")
     ap.add_argument("--sched", default="dynamic", choices=["static", "dynamic"])
     ap.add_argument("--repeat", type=int, default=3, help="calls before the traced one")
+    ap.add_argument("--raw", default=None, help="also write the task records (JSON) to this file")
     args = ap.parse_args()
     dev = torch.device("cuda")
     w = inputs.qwen_weights(0)
@@ -69,6 +70,9 @@ def main():
     torch.cuda.synchronize()
     assert B.etc_plan_check(plan) == B.ETC_OK, B.etc_last_error()
     recs = B.etc_moe_debug_trace(plan, max_records=200000)
+    if args.raw:
+        with open(args.raw, "w") as f:
+            json.dump(recs, f)
     s = summarize(recs)
     s["workload"] = wl.name
     s["sched"] = args.sched

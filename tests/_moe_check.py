@@ -36,10 +36,11 @@ def run_layer(w, x_cpu, sched, unfused=False, t_max=None, debug_flags=0, plan=No
     fn(plan, x, dw["gate_w"], dw["w_gate_up"], dw["w_down"], T, out)
     torch.cuda.synchronize()
     assert B.etc_plan_check(plan) == B.ETC_OK, B.etc_last_error()
-    # unfused: one launch per stage; the top-k stage is empty (and not launched)
-    # when the top-k runs inside the router tiles
+    # unfused: one launch per stage that has work; the top-k stage is empty
+    # when the top-k runs inside the router tiles, the combine finaliser when
+    # the fp32 output is complete after the down tiles
     n = B.etc_launch_count() - before
-    assert (n in (6, 7)) if unfused else n == 1
+    assert (5 <= n <= 7) if unfused else n == 1
     return out.float().cpu().numpy(), read_routing(plan, T, w), plan
 
 
