@@ -21,6 +21,7 @@ constexpr int kNumWorkers = 256;
 constexpr int kStagesMax = 6;       // smem operand stages (6 x 32 KB narrow, 4 x 48 KB wide)
 constexpr int kRing = 8;            // smem task ring depth
 constexpr int kTB = 32;             // tokens per router/top-k/permute/combine task
+constexpr int kMaxPermParts = 4;    // permute tasks per token block when blocks are few
 constexpr int kBT = 128;            // max rows (tokens) per expert chunk = max MMA N
 constexpr int kBK = 64;             // K elements per stage (one 128-byte swizzle row)
 // Expert tiles come in two widths.  Narrow (decode-sized calls): one M=128
@@ -102,6 +103,7 @@ struct BlockWs {
   float* row_w;        // [R_max] routing weight of each expert-sorted row
   int* blk_cnt;        // [nb_max, E] per-token-block expert histogram
   int* cnt_acc;        // [E] counts summed by the routing tasks; the scan reads and re-arms it
+  int* part_cnt;       // [nb_max * kMaxPermParts, E] expert histogram of each permute part
   int* counts;         // [E]
   int* exp_indptr;     // [E+1]
   int* chunk_indptr;   // [E+1]
@@ -166,6 +168,7 @@ struct MegaParams {
   float eps;
   int T, nb, NC, HC, n_router, T_pad;
   int KBr;       // 64-wide K blocks per router task (HC / 64)
+  int PP;        // permute parts per token block (1, or kMaxPermParts for few blocks)
   int NT_gu, NT_dn;
   int wide;      // expert tiles of 256 weight rows (two MMAs per K step)
   unsigned epoch;

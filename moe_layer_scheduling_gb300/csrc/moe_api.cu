@@ -93,6 +93,7 @@ void carve_block(Bump& data, Bump& ctrl, BlockWs& b, const etc_plan_s& p) {
   b.row_token = data.take<int>(R);
   b.row_w = data.take<float>(R);
   b.blk_cnt = data.take<int>(nb * E);
+  b.part_cnt = data.take<int>(nb * kMaxPermParts * E);
   b.cnt_acc = ctrl.take<int>(E);
   b.counts = data.take<int>(E);
   b.exp_indptr = data.take<int>(E + 1);
@@ -282,6 +283,8 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   prm.NC = router_tiles ? choose_nc(a.T, p->H, p->grid) : 1;
   prm.HC = p->H / prm.NC;
   prm.KBr = prm.HC / kBK;
+  // Few token blocks: split each block's permute over kMaxPermParts tasks.
+  prm.PP = prm.nb <= 32 ? kMaxPermParts : 1;
   prm.n_router = prm.nb * prm.NC;
   prm.T_pad = prm.nb * kTB;
   // Wide expert tiles once experts average 64 rows or more (and the shapes divide).
@@ -369,7 +372,7 @@ int etc_moe_plan(etc_plan_t* out, const etc_moe_opts* opts) {
   }
   {
     const int nb = p->nb_max;
-    const long long per_block = nb /*norm*/ + n_router_max + nb + 1 + nb +
+    const long long per_block = nb /*norm*/ + n_router_max + nb + 1 + nb * kMaxPermParts +
                                 static_cast<long long>(p->C_max) * (p->I / kGuRows + p->H / kDnRows) + nb;
     p->ws.qcap = static_cast<int>(per_block * p->n_blocks + 64);
   }

@@ -444,7 +444,7 @@ __device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int
     const bool dyn = dynamic_mode(p);
     if (dyn) {
       const int n_chunks = B.meta[0];
-      const int blk_tasks = (p.use_norm ? nb : 0) + p.n_router + (p.NC > 1 ? nb : 0) + 1 + nb +
+      const int blk_tasks = (p.use_norm ? nb : 0) + p.n_router + (p.NC > 1 ? nb : 0) + 1 + nb * p.PP +
                             n_chunks * (p.NT_gu + p.NT_dn) + (needs_comb(p, blk) ? nb : 0);
       const int acc = (blk == 0 ? 0 : *p.ws.qacc) + blk_tasks;
       *p.ws.qacc = acc;
@@ -458,8 +458,25 @@ __device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int
     st_release(B.plan_flag, p.epoch);
     if (dyn) {
       if (blk == p.n_blocks - 1) st_release(p.ws.qtotal_flag, p.epoch);
-      const Clock c0{~0ull, p.ws.status, p.ws.status_host};
-      queue_push(queue_of(p), nb, [&](int i) { return task_enc(TK_PERM, blk, i, 0); }, c0);
+      const QueueView q = queue_of(p);
+      tmp[0] = q.n_seed + atom_add_relaxed(q.tail, nb * p.PP);  // the block's permute tasks
+    }
+  }
+  if (dynamic_mode(p)) {
+    // Every worker writes some of the reserved slots.
+    named_bar(1, kNumWorkers);
+    const int base = tmp[0];
+    const QueueView q = queue_of(p);
+    __threadfence();  // the plan above is published with the slots
+    for (int i = wt; i < nb * p.PP; i += kNumWorkers) {
+      if (base + i >= q.cap) {
+        const Clock c0{~0ull, p.ws.status, p.ws.status_host};
+        raise_error(c0, DERR_QUEUE_OVERFLOW, 3, base + i);
+        break;
+      }
+      st_relaxed_u64(&q.slots[base + i],
+                     (static_cast<unsigned long long>(q.epoch) << 32) |
+                         task_enc(TK_PERM, blk, i / p.PP, i % p.PP));
     }
   }
 }
@@ -492,29 +509,35 @@ __device__ void init_acc_rows(const MegaParams& p, int blk, int tb, int wt) {
   }
 }
 
-// Writes the rows of token block tb into x_perm at exp_indptr[e] + rank and
-// records each row's token and routing weight.  The rows move through shared
-// memory with the bulk-copy engine: worker thread 0 reads each token row once
-// (kPermSlots rows in flight) and stores it to its k expert-sorted rows.
+// Writes the rows of part t.b of token block tb (kTB / PP tokens; PP > 1
+// spreads the copies of few blocks over more CTAs) into x_perm at
+// exp_indptr[e] + rank, records each row's token and routing weight, and the
+// part's expert histogram (what its notify takes off ev_expert).  The rows
+// move through shared memory with the bulk-copy engine: worker thread 0 reads
+// each token row once (kPermSlots rows in flight) and stores it to its k
+// expert-sorted rows.
 __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* simt, int wt,
                           uint32_t& li, const Clock& clk) {
-  const int blk = t.blk, tb = t.a;
+  const int blk = t.blk, tb = t.a, part = t.b;
   const BlockWs& B = p.ws.blk[blk];
   const int E = p.E, k = p.k, ww = wt >> 5, lane = wt & 31;
   int* s_run = reinterpret_cast<int*>(simt);
   int* s_slot = s_run + kMaxE;
   int* s_ids = s_slot + kTB * kMaxK;
   int* s_part = s_ids + kTB * kMaxK;  // [kNumWorkers]
+  int* s_pcnt = s_part + kNumWorkers; // [E]
   uint8_t* rows = simt + kPermRowOff;
-  const int t0 = tb * kTB, ntok = min(kTB, p.T - t0), nslots = ntok * k;
+  const int t0 = tb * kTB, ntok = min(kTB, p.T - t0);
+  const int TP = kTB / p.PP, r_lo = min(ntok, part * TP), r_hi = min(ntok, r_lo + TP);
+  const int nmine = r_hi - r_lo;
   const __nv_bfloat16* src = p.use_norm ? p.ws.xn : p.x;
   const uint32_t RB = static_cast<uint32_t>(p.H) * 2;
   const int nslot = min(kPermSlots, kPermBytes / static_cast<int>(RB));
   if (wt == 0) {
-    for (int r = 0; r < min(ntok, nslot); ++r) {
+    for (int r = 0; r < min(nmine, nslot); ++r) {
       const int sl = (li + r) % nslot;
       mbar_arrive_expect_tx(&c->pbar[sl], RB);
-      bulk_load(rows + sl * RB, src + static_cast<size_t>(t0 + r) * p.H, RB, &c->pbar[sl]);
+      bulk_load(rows + sl * RB, src + static_cast<size_t>(t0 + r_lo + r) * p.H, RB, &c->pbar[sl]);
     }
   }
   // First row of each expert in this block: exp_indptr[e] plus the rows of e
@@ -522,15 +545,16 @@ __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* 
   // threads per expert.
   const int per = kNumWorkers / E;
   {
-    const int e = wt % E, part = wt / E;
+    const int e = wt % E, q = wt / E;
     int sum = 0;
-    if (part < per) {
+    if (q < per) {
 #pragma unroll 4
-      for (int b = part; b < tb; b += per) sum += __ldcg(B.blk_cnt + b * E + e);
+      for (int b = q; b < tb; b += per) sum += __ldcg(B.blk_cnt + b * E + e);
     }
     s_part[wt] = sum;
   }
-  for (int i = wt; i < nslots; i += kNumWorkers) s_ids[i] = __ldcg(B.ids + t0 * k + i);
+  for (int i = wt; i < r_hi * k; i += kNumWorkers) s_ids[i] = __ldcg(B.ids + t0 * k + i);
+  for (int i = wt; i < E; i += kNumWorkers) s_pcnt[i] = 0;
   named_bar(1, kNumWorkers);
   for (int e = wt; e < E; e += kNumWorkers) {
     int run = __ldcg(B.exp_indptr + e);
@@ -539,42 +563,47 @@ __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* 
   }
   named_bar(1, kNumWorkers);
   if (ww == 0) {
-    // Ranks in ascending token order; one token's k experts are distinct.
-    for (int r = 0; r < ntok; ++r) {
+    // Ranks in ascending token order over the block's tokens up to this
+    // part's end; one token's k experts are distinct.
+    for (int r = 0; r < r_hi; ++r) {
       if (lane < k) {
         const int e = s_ids[r * k + lane];
         const int row = s_run[e];
         s_run[e] = row + 1;
-        s_slot[r * k + lane] = row;
+        if (r >= r_lo) {
+          s_slot[r * k + lane] = row;
+          s_pcnt[e] += 1;
+        }
       }
       __syncwarp();
     }
   }
   named_bar(1, kNumWorkers);
-  for (int i = wt; i < nslots; i += kNumWorkers) {
+  for (int i = r_lo * k + wt; i < r_hi * k; i += kNumWorkers) {
     const int row = s_slot[i];
     B.pos[t0 * k + i] = row;
     B.row_token[row] = t0 + i / k;
     B.row_w[row] = __ldcg(B.wts + t0 * k + i);
   }
+  for (int e = wt; e < E; e += kNumWorkers) B.part_cnt[(tb * p.PP + part) * E + e] = s_pcnt[e];
   if (wt == 0) {
-    for (int r = 0; r < ntok; ++r) {
+    for (int r = 0; r < nmine; ++r) {
       const uint32_t L = li + r;
       const int sl = L % nslot;
       if (!mbar_wait(&c->pbar[sl], (L / nslot) & 1, clk, 270)) break;
       const uint8_t* srow = rows + sl * RB;
       for (int j = 0; j < k; ++j)
-        bulk_store(p.ws.x_perm + static_cast<size_t>(s_slot[r * k + j]) * p.H, srow, RB);
+        bulk_store(p.ws.x_perm + static_cast<size_t>(s_slot[(r_lo + r) * k + j]) * p.H, srow, RB);
       bulk_commit();
       const int nx = r + nslot;
-      if (nx < ntok) {
+      if (nx < nmine) {
         bulk_wait_read_all();  // the slot's row has been read out before it is refilled
         mbar_arrive_expect_tx(&c->pbar[sl], RB);
-        bulk_load(rows + sl * RB, src + static_cast<size_t>(t0 + nx) * p.H, RB, &c->pbar[sl]);
+        bulk_load(rows + sl * RB, src + static_cast<size_t>(t0 + r_lo + nx) * p.H, RB, &c->pbar[sl]);
       }
     }
     bulk_wait_all();  // x_perm rows written before the notify
-    li += ntok;
+    li += nmine;
   }
   fence_proxy_async_global();  // x_perm / row tables are read next by other CTAs' TMA
   named_bar(1, kNumWorkers);   // notify: ev_expert[e] per expert (by the notifier warp)
@@ -818,7 +847,7 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
     case TK_TOPK:
       if (fire) queue_push_warp(q, 1, [&](int) { return task_enc(TK_SCAN, t.blk, 0, 0); }, clk, lane);
       break;
-    case TK_PERM: {  // rows of expert e landed: ev_expert[e] -= rows of this block
+    case TK_PERM: {  // rows of expert e landed: ev_expert[e] -= rows of this block part
       // Lane l owns experts l, l+32, ...: their notifies go out together, then
       // the tiles of [exp_indptr[e], exp_indptr[e+1]) of every expert this
       // block completed are pushed under one queue reservation.
@@ -827,7 +856,7 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
 #pragma unroll
       for (int i = 0; i < kEL; ++i) {
         const int e = 32 * i + lane;
-        n[i] = e < p.E ? __ldcg(B.blk_cnt + t.a * p.E + e) : 0;
+        n[i] = e < p.E ? __ldcg(B.part_cnt + (t.a * p.PP + t.b) * p.E + e) : 0;
       }
       int mine = 0;
 #pragma unroll
@@ -1198,7 +1227,8 @@ __device__ void sched_static(const MegaParams& p, Ctrl* c, const Clock& clk) {
     if (!ok) break;
     const int n_chunks = ld_acquire(&B.meta[0]);
     if (in(TK_PERM))
-      for (int tb = cta; tb < p.nb && ok; tb += G) ok = rw.emit(make_task(TK_PERM, blk, tb, 0), clk);
+      for (int i = cta; i < p.nb * p.PP && ok; i += G)
+        ok = rw.emit(make_task(TK_PERM, blk, i / p.PP, i % p.PP), clk);
     if (in(TK_GU)) {
       const int n = n_chunks * p.NT_gu;
       for (int g = cta; g < n && ok; g += G) {
