@@ -848,14 +848,16 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
       if (fire) queue_push_warp(q, 1, [&](int) { return task_enc(TK_SCAN, t.blk, 0, 0); }, clk, lane);
       break;
     case TK_PERM: {  // rows of expert e landed: ev_expert[e] -= rows of this block part
-      // Lane l owns experts l, l+32, ...: their notifies go out together, then
-      // the tiles of [exp_indptr[e], exp_indptr[e+1]) of every expert this
-      // block completed are pushed under one queue reservation.
+      // Lane l owns experts kEL*l .. kEL*l + kEL-1: their notifies go out
+      // together, then the tiles of [exp_indptr[e], exp_indptr[e+1]) of every
+      // expert this part completed are pushed under one queue reservation, in
+      // expert order (the order the static walk takes them, so that tiles of
+      // one expert run side by side and share its weights in L2).
       constexpr int kEL = kMaxE / 32;
       int n[kEL], tiles[kEL], c0[kEL];
 #pragma unroll
       for (int i = 0; i < kEL; ++i) {
-        const int e = 32 * i + lane;
+        const int e = kEL * lane + i;
         n[i] = e < p.E ? __ldcg(B.part_cnt + (t.a * p.PP + t.b) * p.E + e) : 0;
       }
       int mine = 0;
@@ -863,7 +865,7 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
       for (int i = 0; i < kEL; ++i) {
         tiles[i] = 0;
         if (n[i] > 0) {
-          const int e = 32 * i + lane;
+          const int e = kEL * lane + i;
           if (!dyn) {
             red_add_relaxed(&B.ev_expert[e], -n[i]);
           } else if (notify(&B.ev_expert[e], n[i]) == 0) {
