@@ -77,7 +77,6 @@ struct Ctrl {
   Task ring[kRing];
   Task wtask[2];     // workers' broadcast of the current task (double-buffered)
   Task noti[kNoti];  // workers -> notifier
-  int noti_rtok[kBT];
   uint32_t tmem_base;
   int wflag[2];      // workers' broadcast flags
   int started;       // tasks the workers have taken from the ring
@@ -907,22 +906,30 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
       break;
     case TK_DN:
       if (fire && needs_comb(p, t.blk)) {
-        // Finisher of the chunk: notify each token block by its number of rows
-        // (the chunk's rows are in ascending token order, so blocks form runs).
-        for (int r = lane; r < t.rows; r += 32) c->noti_rtok[r] = __ldcg(B.row_token + t.row0 + r) / kTB;
-        __syncwarp();
-        for (int r = lane; r < t.rows; r += 32) {
-          const int tb = c->noti_rtok[r];
-          if (r == 0 || c->noti_rtok[r - 1] != tb) {
-            int e = r + 1;
-            while (e < t.rows && c->noti_rtok[e] == tb) ++e;
-            if (!dyn) {
-              red_add_relaxed(&B.ev_tok[tb], -(e - r));
-            } else if (notify(&B.ev_tok[tb], e - r) == 0) {
-              queue_push(q, 1, [&](int) { return task_enc(TK_COMB, t.blk, tb, 0); }, clk);
-            }
+        // Finisher of the chunk: notify each token block by its number of rows.
+        // The chunk's rows are in ascending token order, so blocks form runs;
+        // each lane takes a contiguous range of rows and notifies its runs (a
+        // run split between lanes is notified in two parts).
+        const int per = (t.rows + 31) / 32, r0 = min(t.rows, lane * per), r1 = min(t.rows, r0 + per);
+        int run_tb = -1, run_n = 0;
+        auto flush_run = [&]() {
+          if (run_n == 0) return;
+          if (!dyn) {
+            red_add_relaxed(&B.ev_tok[run_tb], -run_n);
+          } else if (notify(&B.ev_tok[run_tb], run_n) == 0) {
+            queue_push(q, 1, [&](int) { return task_enc(TK_COMB, t.blk, run_tb, 0); }, clk);
           }
+        };
+        for (int r = r0; r < r1; ++r) {
+          const int tb = __ldcg(B.row_token + t.row0 + r) / kTB;
+          if (tb != run_tb) {
+            flush_run();
+            run_tb = tb;
+            run_n = 0;
+          }
+          ++run_n;
         }
+        flush_run();
         __syncwarp();
       }
       break;
