@@ -169,6 +169,7 @@ struct MegaParams {
   int T, nb, NC, HC, n_router, T_pad;
   int KBr;       // 64-wide K blocks per router task (HC / 64)
   int PP;        // permute parts per token block (1, or kMaxPermParts for few blocks)
+  int fuse_scan; // one token block with H split: its top-k task runs the scan
   int NT_gu, NT_dn;
   int wide;      // expert tiles of 256 weight rows (two MMAs per K step)
   unsigned epoch;

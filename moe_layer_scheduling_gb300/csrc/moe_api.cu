@@ -285,6 +285,9 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   prm.KBr = prm.HC / kBK;
   // Few token blocks: split each block's permute over kMaxPermParts tasks.
   prm.PP = prm.nb <= 32 ? kMaxPermParts : 1;
+  // One token block with H split: the top-k task runs the scan (not in the
+  // per-stage ablation, which launches every stage on its own).
+  prm.fuse_scan = (prm.nb == 1 && prm.NC > 1 && !unfused) ? 1 : 0;
   prm.n_router = prm.nb * prm.NC;
   prm.T_pad = prm.nb * kTB;
   // Wide expert tiles once experts average 64 rows or more (and the shapes divide).

@@ -125,6 +125,7 @@ __device__ __forceinline__ StageGeom stage_geom(const MegaParams& p) {
 __device__ __forceinline__ void load_block_input8(const MegaParams& p, int blk, int tok, int c,
                                                   float (&f)[8]);
 __device__ void init_acc_rows(const MegaParams& p, int blk, int tb, int wt);
+__device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt);
 
 // ---------------------------------------------------------------------------
 // small helpers
@@ -392,13 +393,20 @@ __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int
   topk_rows(p, B, s_log, tok0, s_cnt, ww, lane);
   named_bar(1, kNumWorkers);
   publish_block_counts(p, B, tb, s_cnt, wt);
+  if (p.fuse_scan) {
+    // One token block: its histogram is the call's counts, so the scan runs
+    // here, one hop sooner (no separate scan task; the notifier leaves
+    // ev_route alone).
+    __threadfence();
+    named_bar(1, kNumWorkers);
+    scan_block(p, blk, simt, wt);
+  }
   named_bar(1, kNumWorkers);  // notify: ev_route (by the notifier warp)
 }
 
 // counts / exp_indptr / expert chunks / event inits, from the counts the
 // routing tasks summed (thread e < E owns expert e).
-__device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
-  const int blk = t.blk;
+__device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt) {
   const BlockWs& B = p.ws.blk[blk];
   const int E = p.E, nb = p.nb;
   int* tmp = reinterpret_cast<int*>(simt);  // scan scratch [32]
@@ -443,7 +451,8 @@ __device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int
     const bool dyn = dynamic_mode(p);
     if (dyn) {
       const int n_chunks = B.meta[0];
-      const int blk_tasks = (p.use_norm ? nb : 0) + p.n_router + (p.NC > 1 ? nb : 0) + 1 + nb * p.PP +
+      const int blk_tasks = (p.use_norm ? nb : 0) + p.n_router + (p.NC > 1 ? nb : 0) +
+                            (p.fuse_scan ? 0 : 1) + nb * p.PP +
                             n_chunks * (p.NT_gu + p.NT_dn) + (needs_comb(p, blk) ? nb : 0);
       const int acc = (blk == 0 ? 0 : *p.ws.qacc) + blk_tasks;
       *p.ws.qacc = acc;
@@ -478,6 +487,10 @@ __device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int
                          task_enc(TK_PERM, blk, i / p.PP, i % p.PP));
     }
   }
+}
+
+__device__ void task_scan(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
+  scan_block(p, t.blk, simt, wt);
 }
 
 // fp32 rows that block blk's combine accumulates into: the residual stream of
@@ -805,6 +818,7 @@ __device__ __forceinline__ int notify_primary(const MegaParams& p, const Task& t
       return atom_add_acq_rel(&B.ev_rblk[t.a], 1) + 1 == p.NC;
     case TK_TOPK:
       st_relaxed(&B.ev_rblk[t.a], 0);  // consumed: re-armed for the next call
+      if (p.fuse_scan) return 0;       // the task ran the scan itself
       if (!dyn) {
         red_add_relaxed(B.ev_route, 1);
         return 0;
@@ -844,7 +858,8 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
         }, clk, lane);
       break;
     case TK_TOPK:
-      if (fire) queue_push_warp(q, 1, [&](int) { return task_enc(TK_SCAN, t.blk, 0, 0); }, clk, lane);
+      if (fire && !p.fuse_scan)
+        queue_push_warp(q, 1, [&](int) { return task_enc(TK_SCAN, t.blk, 0, 0); }, clk, lane);
       break;
     case TK_PERM: {  // rows of expert e landed: ev_expert[e] -= rows of this block part
       // Lane l owns experts kEL*l .. kEL*l + kEL-1: their notifies go out
@@ -1227,7 +1242,7 @@ __device__ void sched_static(const MegaParams& p, Ctrl* c, const Clock& clk) {
         ok = ok && rw.emit(make_task(TK_TOPK, blk, tb, 0), clk);
       }
     }
-    if (in(TK_SCAN) && cta == blk % G && ok) {
+    if (in(TK_SCAN) && !p.fuse_scan && cta == blk % G && ok) {
       ok = wait_geq(B.ev_route, p.nb, clk, TK_SCAN, 0);
       ok = ok && rw.emit(make_task(TK_SCAN, blk, 0, 0), clk);
     }
