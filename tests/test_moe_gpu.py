@@ -61,6 +61,28 @@ def test_ragged_token_counts(oracle_lib, sched, unfused, T, seed):
     _full_check(oracle_lib, w, x, sched, unfused)
 
 
+SHAPE_EDGES = [
+    # (H, E, k, I, T): E not a power of two and k = 1;
+    (256, 24, 1, 64, 45),
+    # k = E = 16 (every token to every expert, the largest k);
+    (256, 16, 16, 128, 40),
+    # the largest hidden size: one 24 KB token row fills the permute's row
+    # slots, the router's H is split 32 ways;
+    (12288, 8, 2, 64, 33),
+    # T = t_max with a ragged block, H a multiple of 128 but not a power of two.
+    (384, 128, 8, 64, 77),
+]
+
+
+@pytest.mark.parametrize("sched,unfused", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("shape", SHAPE_EDGES, ids=lambda s: "H%d-E%d-k%d-I%d-T%d" % s)
+def test_shape_edges(oracle_lib, sched, unfused, shape):
+    H, E, k, I, T = shape
+    w = inputs.moe_weights(H, E, k, I, seed=H + E + k)
+    x = inputs.tokens(T, H, T + 7)
+    _full_check(oracle_lib, w, x, sched, unfused, t_max=T)
+
+
 @pytest.mark.parametrize("sched,unfused", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("T,seed", [(300, 4), (1100, 5)])
 def test_wide_tiles(oracle_lib, sched, unfused, T, seed):
