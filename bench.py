@@ -231,7 +231,8 @@ def run_ours(args, rank, world):
     launches0 = B.etc_launch_count()
     results = {}
     plans = {}
-    for name, sched in (("dynamic", B.ETC_SCHED_DYNAMIC), ("static", B.ETC_SCHED_STATIC)):
+    for name, sched in (("dynamic", B.ETC_SCHED_DYNAMIC), ("static", B.ETC_SCHED_STATIC),
+                        ("mixed", B.ETC_SCHED_MIXED)):
         plans[name] = B.etc_moe_plan(H, E, K, I, t_max=T, sched=sched, router_bias=bias)
 
     # ---- headline: dynamic megakernel, inputs resident in HBM ----
@@ -356,14 +357,14 @@ def run_extras(args, dev, weights, gw, wgu, wd, bias, x, out, T, plans, peaks, w
     steps = max(5, min(args.steps, 50))
     # --- Table 2 analogue on the prefill workload: static / dynamic / unfused ---
     abl = {}
-    for name in ("static", "dynamic"):
+    for name in ("static", "dynamic", "mixed"):
         p = plans[name]
         sec = time_gpu(lambda: B.etc_moe_forward(p, x, gw, wgu, wd, T, out), steps, 3, world)
         abl[name] = {"us": sec * 1e6, "tflops": T * FLOPS_PER_TOKEN / sec / 1e12}
     p = plans["static"]
     sec = time_gpu(lambda: B.etc_moe_forward_unfused(p, x, gw, wgu, wd, T, out), steps, 3, world)
     abl["unfused_per_stage"] = {"us": sec * 1e6, "tflops": T * FLOPS_PER_TOKEN / sec / 1e12}
-    for name in ("static", "dynamic"):
+    for name in ("static", "dynamic", "mixed"):
         abl[name]["vs_unfused"] = abl["unfused_per_stage"]["us"] / abl[name]["us"]
     res["ablation_prefill_T4096"] = abl
 
@@ -376,7 +377,8 @@ def run_extras(args, dev, weights, gw, wgu, wd, bias, x, out, T, plans, peaks, w
         xd = inputs.decode_layer(Td, weights).x.to(dev)
         od = torch.empty(Td, H, dtype=torch.float32, device=dev)
         row = {}
-        for name, sched in (("dynamic", B.ETC_SCHED_DYNAMIC), ("static", B.ETC_SCHED_STATIC)):
+        for name, sched in (("dynamic", B.ETC_SCHED_DYNAMIC), ("static", B.ETC_SCHED_STATIC),
+                            ("mixed", B.ETC_SCHED_MIXED)):
             pd = B.etc_moe_plan(H, E, K, I, t_max=64, sched=sched)
             idx = [0]
 
@@ -503,8 +505,11 @@ def run_single(args):
     from moe_layer_scheduling_gb300 import inputs
     libbuild.build()
     dev = torch.device("cuda")
-    sched = B.ETC_SCHED_DYNAMIC if args.sched == "dynamic" else B.ETC_SCHED_STATIC
+    sched = {"static": B.ETC_SCHED_STATIC, "dynamic": B.ETC_SCHED_DYNAMIC,
+             "mixed": B.ETC_SCHED_MIXED}[args.sched]
     if args.workload == "splitk":
+        if sched == B.ETC_SCHED_MIXED:
+            raise SystemExit("split-K takes static or dynamic scheduling")
         A = inputs.splitk_matrix(8192, 16384, 0).to(dev)
         C = torch.empty(8192, device=dev)
         sec = time_gpu(lambda: B.etc_splitk_rowsum(A, 4, C, sched=sched), args.steps, args.warmup, 1)
@@ -535,7 +540,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "splitk"],
                     help="prefill = the benchmark line; decode/splitk = one workload (profiling)")
-    ap.add_argument("--sched", default="dynamic", choices=["static", "dynamic"])
+    ap.add_argument("--sched", default="dynamic", choices=["static", "dynamic", "mixed"])
     ap.add_argument("--clock-window", type=float, default=1.5,
                     help="seconds of load kept up for the clock record (0 for profiler runs)")
     args = ap.parse_args()

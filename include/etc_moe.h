@@ -54,7 +54,17 @@ extern "C" {
 #define ETC_ERR_UNIMPLEMENTED (-4) /* option not supported by this build */
 #define ETC_ERR_STATE (-5)         /* plan needs etc_plan_reset after a timeout */
 
-typedef enum { ETC_SCHED_STATIC = 0, ETC_SCHED_DYNAMIC = 1 } etc_sched_t;
+/*
+ * Schedulers of the megakernel's tasks:
+ *   STATIC   every CTA walks a fixed, stage-ordered list of task slots and
+ *            spin-waits on each task's input event (notify/wait);
+ *   DYNAMIC  the notify that completes an event pushes the tasks it makes
+ *            ready into a global queue, from which CTAs pop (push/pop);
+ *   MIXED    (n_blocks == 1) router, top-k, scan and permute as STATIC, the
+ *            expert tiles and the combine finaliser through the queue as
+ *            DYNAMIC.  Not accepted by the split-K entry points.
+ */
+typedef enum { ETC_SCHED_STATIC = 0, ETC_SCHED_DYNAMIC = 1, ETC_SCHED_MIXED = 2 } etc_sched_t;
 
 /* Debug bits for etc_moe_opts.debug_flags. */
 #define ETC_DEBUG_FAULT_EXTRA_WAIT 0x1u /* add 1 to expert debug_arg's wait_count: its
@@ -70,7 +80,7 @@ typedef struct {
   int top_k;         /* k: 1..min(E,16) */
   int inter;         /* I: expert intermediate width; multiple of 64 */
   int t_max;         /* largest token count a call may pass (>= 1) */
-  int sched;         /* etc_sched_t */
+  int sched;         /* etc_sched_t (MIXED only with n_blocks == 1) */
   int n_blocks;      /* 1 for etc_moe_forward; 1..4 for etc_chain_forward */
   float rms_eps;     /* RMSNorm epsilon of the chain (0 -> 1e-6) */
   const float* router_bias;          /* device fp32 [E] added to the logits, or NULL */

@@ -21,6 +21,7 @@ ETC_ERR_UNIMPLEMENTED = -4
 ETC_ERR_STATE = -5
 ETC_SCHED_STATIC = 0
 ETC_SCHED_DYNAMIC = 1
+ETC_SCHED_MIXED = 2
 ETC_DEBUG_FAULT_EXTRA_WAIT = 0x1
 ETC_DEBUG_POISON = 0x2
 ETC_OUT_F32 = 0

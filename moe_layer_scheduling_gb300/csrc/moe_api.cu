@@ -138,8 +138,10 @@ int validate_opts(const etc_moe_opts* o) {
     return set_error(ETC_ERR_INVALID, "inter=%d must be a positive multiple of 64", o->inter);
   if (o->t_max < 1 || static_cast<long long>(o->t_max) * o->top_k > (1 << 24))
     return set_error(ETC_ERR_INVALID, "t_max=%d out of range", o->t_max);
-  if (o->sched != ETC_SCHED_STATIC && o->sched != ETC_SCHED_DYNAMIC)
+  if (o->sched != ETC_SCHED_STATIC && o->sched != ETC_SCHED_DYNAMIC && o->sched != ETC_SCHED_MIXED)
     return set_error(ETC_ERR_INVALID, "sched=%d unknown", o->sched);
+  if (o->sched == ETC_SCHED_MIXED && o->n_blocks != 1)
+    return set_error(ETC_ERR_INVALID, "sched=MIXED needs n_blocks == 1 (got %d)", o->n_blocks);
   if (o->n_blocks < 1 || o->n_blocks > kMaxBlocks)
     return set_error(ETC_ERR_INVALID, "n_blocks=%d must be in [1, %d]", o->n_blocks, kMaxBlocks);
   if (o->router_bias && !aligned16(o->router_bias))

@@ -93,12 +93,16 @@ __device__ __forceinline__ QueueView queue_of(const MegaParams& p) {
   q.head = p.ws.qhead[par];
   q.tail = p.ws.qtail[par];
   q.cap = p.ws.qcap;
-  q.n_seed = p.use_norm ? p.nb : p.n_router;
+  // DYNAMIC seeds the queue with the first tasks (virtual slots 0..n_seed-1).
+  q.n_seed = p.mode == ETC_SCHED_DYNAMIC ? (p.use_norm ? p.nb : p.n_router) : 0;
   q.epoch = p.epoch;
   return q;
 }
 
 __device__ __forceinline__ bool dynamic_mode(const MegaParams& p) { return p.mode == ETC_SCHED_DYNAMIC; }
+// Whether the expert tiles and the finaliser go through the queue (DYNAMIC and
+// MIXED); the routing tasks do only in DYNAMIC.
+__device__ __forceinline__ bool tiles_queued(const MegaParams& p) { return p.mode != ETC_SCHED_STATIC; }
 
 // Whether block blk's combine finaliser has work: releasing the next block's
 // RMSNorm in the chain, or rounding the last block's rows to a bf16 output.
@@ -449,11 +453,14 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt) 
   if (wt == 0) {
     st_relaxed(B.ev_route, 0);
     const bool dyn = dynamic_mode(p);
-    if (dyn) {
+    if (tiles_queued(p)) {
+      // Tasks of the block that pass through the queue: all of them in
+      // DYNAMIC, the expert tiles and the finaliser in MIXED.
       const int n_chunks = B.meta[0];
-      const int blk_tasks = (p.use_norm ? nb : 0) + p.n_router + (p.NC > 1 ? nb : 0) +
-                            (p.fuse_scan ? 0 : 1) + nb * p.PP +
-                            n_chunks * (p.NT_gu + p.NT_dn) + (needs_comb(p, blk) ? nb : 0);
+      const int routing = dyn ? (p.use_norm ? nb : 0) + p.n_router + (p.NC > 1 ? nb : 0) +
+                                    (p.fuse_scan ? 0 : 1) + nb * p.PP
+                              : 0;
+      const int blk_tasks = routing + n_chunks * (p.NT_gu + p.NT_dn) + (needs_comb(p, blk) ? nb : 0);
       const int acc = (blk == 0 ? 0 : *p.ws.qacc) + blk_tasks;
       *p.ws.qacc = acc;
       if (blk == p.n_blocks - 1) *p.ws.qtotal = acc;
@@ -464,8 +471,8 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt) 
     *p.ws.qtail[other] = 0;
     __threadfence();
     st_release(B.plan_flag, p.epoch);
+    if (tiles_queued(p) && blk == p.n_blocks - 1) st_release(p.ws.qtotal_flag, p.epoch);
     if (dyn) {
-      if (blk == p.n_blocks - 1) st_release(p.ws.qtotal_flag, p.epoch);
       const QueueView q = queue_of(p);
       tmp[0] = q.n_seed + atom_add_relaxed(q.tail, nb * p.PP);  // the block's permute tasks
     }
@@ -825,7 +832,7 @@ __device__ __forceinline__ int notify_primary(const MegaParams& p, const Task& t
       }
       return atom_add_acq_rel(B.ev_route, 1) + 1 == p.nb;
     case TK_GU:
-      if (!dyn) {
+      if (!tiles_queued(p)) {
         red_add_relaxed(&B.ev_act[t.a], -1);
         return 0;
       }
@@ -880,7 +887,7 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
         tiles[i] = 0;
         if (n[i] > 0) {
           const int e = kEL * lane + i;
-          if (!dyn) {
+          if (!tiles_queued(p)) {
             red_add_relaxed(&B.ev_expert[e], -n[i]);
           } else if (notify(&B.ev_expert[e], n[i]) == 0) {
             c0[i] = __ldcg(B.chunk_indptr + e);
@@ -889,7 +896,7 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
           }
         }
       }
-      if (!dyn) break;
+      if (!tiles_queued(p)) break;
       int off = mine;  // inclusive prefix over the lanes
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -929,7 +936,7 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
         int run_tb = -1, run_n = 0;
         auto flush_run = [&]() {
           if (run_n == 0) return;
-          if (!dyn) {
+          if (!tiles_queued(p)) {
             red_add_relaxed(&B.ev_tok[run_tb], -run_n);
           } else if (notify(&B.ev_tok[run_tb], run_n) == 0) {
             queue_push(q, 1, [&](int) { return task_enc(TK_COMB, t.blk, run_tb, 0); }, clk);
@@ -1216,8 +1223,11 @@ __device__ __forceinline__ void resolve_chunk(const MegaParams& p, Task& t) {
   t.rows = __ldcg(B.chunk_rows + t.a);
 }
 
-__device__ void sched_static(const MegaParams& p, Ctrl* c, const Clock& clk) {
-  RingWriter rw{c, 0};
+// Static walk.  routing_only (MIXED): the walk stops after each block's
+// permute tasks; the expert tiles then come from the queue.  Returns false
+// after a failed wait.
+__device__ bool sched_static(const MegaParams& p, Ctrl* c, const Clock& clk, RingWriter& rw,
+                             bool routing_only) {
   const int G = gridDim.x, cta = blockIdx.x;
   auto in = [&](int stage) { return stage >= p.stage_lo && stage <= p.stage_hi; };
   bool ok = true;
@@ -1253,6 +1263,7 @@ __device__ void sched_static(const MegaParams& p, Ctrl* c, const Clock& clk) {
     if (in(TK_PERM))
       for (int i = cta; i < p.nb * p.PP && ok; i += G)
         ok = rw.emit(make_task(TK_PERM, blk, i / p.PP, i % p.PP), clk);
+    if (routing_only) continue;
     if (in(TK_GU)) {
       const int n = n_chunks * p.NT_gu;
       for (int g = cta; g < n && ok; g += G) {
@@ -1278,11 +1289,12 @@ __device__ void sched_static(const MegaParams& p, Ctrl* c, const Clock& clk) {
       }
     }
   }
-  rw.emit(make_task(TK_TERM, 0, 0, 0), clk);
+  return ok;
 }
 
-__device__ void sched_dynamic(const MegaParams& p, Ctrl* c, const Clock& clk) {
-  RingWriter rw{c, 0};
+// Queue pops until every task of the call that passes through the queue has
+// been popped (the last scan publishes their number).
+__device__ void sched_dynamic(const MegaParams& p, Ctrl* c, const Clock& clk, RingWriter& rw) {
   const QueueView q = queue_of(p);
   constexpr int kLookahead = 2;  // tasks popped but not yet started by the workers
   for (;;) {
@@ -1325,7 +1337,6 @@ __device__ void sched_dynamic(const MegaParams& p, Ctrl* c, const Clock& clk) {
     if (t.type == TK_GU || t.type == TK_DN) resolve_chunk(p, t);
     if (!rw.emit(t, clk)) break;
   }
-  rw.emit(make_task(TK_TERM, 0, 0, 0), clk);
 }
 
 // ---------------------------------------------------------------------------
@@ -1386,10 +1397,15 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
 
   if (w == kWarpSched) {
     if (lane_id() == 0) {
-      if (p.mode == ETC_SCHED_DYNAMIC)
-        sched_dynamic(p, c, clk);
-      else
-        sched_static(p, c, clk);
+      RingWriter rw{c, 0};
+      if (p.mode == ETC_SCHED_DYNAMIC) {
+        sched_dynamic(p, c, clk, rw);
+      } else if (p.mode == ETC_SCHED_MIXED) {
+        if (sched_static(p, c, clk, rw, true)) sched_dynamic(p, c, clk, rw);
+      } else {
+        sched_static(p, c, clk, rw, false);
+      }
+      rw.emit(make_task(TK_TERM, 0, 0, 0), clk);
     }
   } else if (w == kWarpTma) {
     if (lane_id() == 0) run_producer(p, c, base, clk);

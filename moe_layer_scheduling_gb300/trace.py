@@ -51,7 +51,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--tokens", type=int, default=4096)
     ap.add_argument("--skew", action="store_true", help="Zipf(1.2) router bias (prefill workload)")
-    ap.add_argument("--sched", default="dynamic", choices=["static", "dynamic"])
+    ap.add_argument("--sched", default="dynamic", choices=["static", "dynamic", "mixed"])
     ap.add_argument("--repeat", type=int, default=3, help="calls before the traced one")
     ap.add_argument("--raw", default=None, help="also write the task records (JSON) to this file")
     args = ap.parse_args()
@@ -59,7 +59,8 @@ def main():
     w = inputs.qwen_weights(0)
     wl = inputs.prefill_skew_layer(args.tokens, w) if args.skew else inputs.decode_layer(args.tokens, w)
     bias = wl.weights.router_bias.to(dev) if wl.weights.router_bias is not None else None
-    sched = B.ETC_SCHED_DYNAMIC if args.sched == "dynamic" else B.ETC_SCHED_STATIC
+    sched = {"static": B.ETC_SCHED_STATIC, "dynamic": B.ETC_SCHED_DYNAMIC,
+             "mixed": B.ETC_SCHED_MIXED}[args.sched]
     plan = B.etc_moe_plan(w.hidden, w.n_experts, w.top_k, w.inter, t_max=args.tokens, sched=sched,
                           router_bias=bias, debug_flags=B.ETC_DEBUG_TRACE)
     x = wl.x.to(dev)

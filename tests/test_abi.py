@@ -58,7 +58,8 @@ def _opts(**kw):
 @pytest.mark.parametrize("bad", [
     dict(hidden=100), dict(hidden=0), dict(hidden=12416), dict(n_experts=7), dict(n_experts=136), dict(n_experts=512),
     dict(top_k=0),
-    dict(top_k=17), dict(inter=100), dict(t_max=0), dict(sched=5), dict(n_blocks=0),
+    dict(top_k=17), dict(inter=100), dict(t_max=0), dict(sched=5), dict(sched=3),
+    dict(sched=2, n_blocks=2), dict(n_blocks=0),
     dict(n_blocks=9), dict(router_bias=8),
 ])
 def test_plan_rejects_bad_options_on_the_host(lib, bad):

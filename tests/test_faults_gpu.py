@@ -16,7 +16,7 @@ from moe_layer_scheduling_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC])
+@pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC, B.ETC_SCHED_MIXED])
 def test_moe_wait_times_out_and_recovers(oracle_lib, sched):
     wl = inputs.tiny_layer(0)
     w = wl.weights

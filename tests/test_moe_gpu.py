@@ -10,8 +10,9 @@ from moe_layer_scheduling_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
-MODES = [(B.ETC_SCHED_STATIC, False), (B.ETC_SCHED_DYNAMIC, False), (B.ETC_SCHED_STATIC, True)]
-MODE_IDS = ["static", "dynamic", "unfused"]
+MODES = [(B.ETC_SCHED_STATIC, False), (B.ETC_SCHED_DYNAMIC, False), (B.ETC_SCHED_MIXED, False),
+         (B.ETC_SCHED_STATIC, True)]
+MODE_IDS = ["static", "dynamic", "mixed", "unfused"]
 
 
 @pytest.fixture(scope="module")
@@ -94,7 +95,7 @@ def test_wide_tiles(oracle_lib, sched, unfused, T, seed):
     _full_check(oracle_lib, w, x, sched, unfused)
 
 
-@pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC])
+@pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC, B.ETC_SCHED_MIXED])
 def test_qwen_wide_tiles_full_parity(oracle_lib, qwen, qwen_dev, sched):
     # Qwen shape at T=1100: wide tiles, every token checked against the oracle.
     x = inputs.tokens(1100, inputs.QWEN_H, 1100)
