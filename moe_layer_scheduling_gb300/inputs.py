@@ -142,6 +142,49 @@ def chain_blocks(n_blocks: int = 4, hidden: int = QWEN_H, n_experts: int = QWEN_
     return blocks
 
 
+# ----------------------------------------------------------------------------
+# Dense MLP (the appendix's Table 4: sequence length S, hidden H, intermediate I)
+# ----------------------------------------------------------------------------
+
+MLP_SHAPES = {
+    "MLP-1": (8192, 4096, 12288),   # Qwen3-8B
+    "MLP-2": (8192, 4096, 14336),   # LLaMA-3.1-8B
+    "MLP-3": (8192, 3584, 14336),   # Gemma-2-9B
+    "MLP-4": (8192, 4608, 36864),   # Gemma-2-27B
+    "MLP-5": (8192, 5120, 25600),   # Qwen3-32B
+}
+
+
+@dataclass
+class MLPWeights:
+    hidden: int
+    inter: int
+    w_gate_up: torch.Tensor     # bf16 [2I, H]  rows 0..I-1 gate, I..2I-1 up
+    w_down: torch.Tensor        # bf16 [H, I]
+
+
+def mlp_weights(hidden: int, inter: int, seed: int, std: float = WEIGHT_STD) -> MLPWeights:
+    """Dense MLP weights ~ N(0, std^2), cast to bf16, drawn in row slabs (low host memory)."""
+    rng = np.random.default_rng(seed)
+    slab = max(1, (1 << 24) // hidden)
+    wgu = torch.empty(2 * inter, hidden, dtype=torch.bfloat16)
+    for r in range(0, 2 * inter, slab):
+        n = min(slab, 2 * inter - r)
+        wgu[r:r + n] = _bf16(rng.standard_normal((n, hidden), dtype=np.float32) * std)
+    wd = torch.empty(hidden, inter, dtype=torch.bfloat16)
+    slab = max(1, (1 << 24) // inter)
+    for r in range(0, hidden, slab):
+        n = min(slab, hidden - r)
+        wd[r:r + n] = _bf16(rng.standard_normal((n, inter), dtype=np.float32) * std)
+    return MLPWeights(hidden, inter, wgu, wd)
+
+
+def mlp_layer(name: str = "MLP-1", T: int | None = None, seed: int = 300):
+    """(weights, x) of a Table 4 MLP shape; x ~ N(0, 1) with T rows (S by default)."""
+    S, H, I = MLP_SHAPES[name]
+    return mlp_weights(H, I, seed), tokens(S if T is None else T, H, seed + 1)
+
+
 def expected_touched_experts(T: int, n_experts: int = QWEN_E, top_k: int = QWEN_K) -> float:
     """E * (1 - ((E-k)/E)^T): expected number of experts hit under uniform routing."""
     return n_experts * (1.0 - math.pow((n_experts - top_k) / n_experts, T))

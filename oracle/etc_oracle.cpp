@@ -27,6 +27,8 @@
 //   * Within an expert's row range, rows follow ascending token index.
 //   * W_gate_up[e] holds the I gate rows first, then the I up rows; the
 //     activation is silu(gate) * up with silu(z) = z / (1 + exp(-z)).
+//   * The dense MLP of the appendix's Table 4 applies that same FFN to every
+//     row with one weight set.
 //   * The chain block is x <- x + MoE(RMSNorm(x)), RMSNorm(x) = x /
 //     sqrt(mean(x^2) + eps) * g.
 //
@@ -285,6 +287,25 @@ int oracle_expert_ffn(const uint16_t* x, const uint16_t* wgu_e, const uint16_t* 
   std::vector<double> xr(H), act(I);
   for (int h = 0; h < H; ++h) xr[h] = bf16_to_double(x[h]);
   expert_ffn(xr.data(), wgu_e, wd_e, H, I, act.data(), y);
+  return 0;
+}
+
+// Dense MLP on chosen rows of x: out[i] = FFN(x[rows[i]]) with the single
+// weight set w_gate_up bf16 [2I,H] (gate rows, then up rows) and w_down bf16
+// [H,I].  The paper summary page's appendix Table 4 gives the MLP shapes (S,
+// H, I) but no activation; the FFN is read as the experts' silu(gate) * up.
+// rows == NULL takes rows 0 .. n-1 (n <= T); out is fp64 [n, H].
+int oracle_mlp(const uint16_t* x, const uint16_t* wgu, const uint16_t* wd, long T, int H, int I,
+               const int64_t* rows, long n, double* out) {
+  if (T < 0 || H <= 0 || I <= 0 || n < 0 || (!rows && n > T)) return -1;
+  for (long i = 0; rows && i < n; ++i)
+    if (rows[i] < 0 || rows[i] >= T) return -1;
+  parallel_for(n, [&](long i) {
+    const long t = rows ? static_cast<long>(rows[i]) : i;
+    std::vector<double> xr(H), act(I);
+    for (int h = 0; h < H; ++h) xr[h] = bf16_to_double(x[t * H + h]);
+    expert_ffn(xr.data(), wgu, wd, H, I, act.data(), out + i * H);
+  });
   return 0;
 }
 

@@ -23,7 +23,7 @@ _lock = threading.Lock()
 
 __all__ = [
     "build", "lib", "set_threads", "get_threads", "router_logits", "route", "route_f32",
-    "dispatch", "expert_ffn", "moe_layer", "chain", "splitk", "event_sim",
+    "dispatch", "expert_ffn", "mlp", "moe_layer", "chain", "splitk", "event_sim",
 ]
 
 
@@ -75,6 +75,7 @@ def _declare(L):
     L.oracle_route_f32.argtypes = [_P, _L, _I, _I, _P, _P]
     L.oracle_dispatch.argtypes = [_P, _L, _I, _I, _P, _P, _P, _P]
     L.oracle_expert_ffn.argtypes = [_P, _P, _P, _I, _I, _P]
+    L.oracle_mlp.argtypes = [_P, _P, _P, _L, _I, _I, _P, _L, _P]
     L.oracle_moe_layer.argtypes = [_P, _P, _P, _P, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P]
     L.oracle_chain.argtypes = [_P, _I, _P, _P, _P, _P, _P, _L, _I, _I, _I, _I, ctypes.c_double,
                                _P, _P, _P]
@@ -174,6 +175,22 @@ def expert_ffn(x_row, w_gate_up_e, w_down_e):
     y = np.empty(H, dtype=np.float64)
     _check(lib().oracle_expert_ffn(_ptr(xb), _ptr(a), _ptr(b), H, I, _ptr(y)), "expert_ffn")
     return y
+
+
+def mlp(x, w_gate_up, w_down, rows=None):
+    """fp64 dense MLP (silu(x Wg^T) * (x Wu^T)) Wd^T on rows of x [T, H] (all rows if None)."""
+    xb, a, b = _u16(x), _u16(w_gate_up), _u16(w_down)
+    T, H = xb.shape
+    I = a.shape[0] // 2
+    if rows is None:
+        n, rp = T, None
+    else:
+        rp = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n = rp.shape[0]
+    out = np.empty((n, H), dtype=np.float64)
+    _check(lib().oracle_mlp(_ptr(xb), _ptr(a), _ptr(b), T, H, I,
+                            None if rp is None else _ptr(rp), n, _ptr(out)), "mlp")
+    return out
 
 
 def moe_layer(x, gate_w, w_gate_up, w_down, top_k: int, bias=None, want_routing=False):

@@ -35,6 +35,8 @@ MUTANTS = [
      "const long r = exp_indptr[e + 1] - 1 - seen[e]++;"),
     ("combine_unweighted", "s += w[t * k + j] * y[static_cast<long>(pos[t * k + j]) * H + m];",
      "s += y[static_cast<long>(pos[t * k + j]) * H + m];"),
+    ("mlp_ignores_row_list", "const long t = rows ? static_cast<long>(rows[i]) : i;",
+     "const long t = i;"),
     ("splitk_drops_last_column", "for (long col = j * tile; col < (j + 1) * tile; ++col)",
      "for (long col = j * tile; col < (j + 1) * tile - 1; ++col)"),
     ("rmsnorm_sum_not_mean", "const double inv = 1.0 / std::sqrt(ss / H + eps);",

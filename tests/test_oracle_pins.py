@@ -191,6 +191,55 @@ def test_expert_ffn_matches_matmul(oracle_lib):
 
 
 # ---------------------------------------------------------------------------
+# Dense MLP: the same FFN on every row with one weight set
+# ---------------------------------------------------------------------------
+
+def test_mlp_hand_values(oracle_lib):
+    # H=2, I=1: gate row [1, 0], up row [0, 1], down [[1], [2]]
+    wgu = torch.tensor([[1.0, 0.0], [0.0, 1.0]], dtype=torch.bfloat16)
+    wd = torch.tensor([[1.0], [2.0]], dtype=torch.bfloat16)
+    x = torch.tensor([[2.0, 3.0], [0.0, 5.0], [-1.0, 1.0]], dtype=torch.bfloat16)
+    y = oracle_lib.mlp(x, wgu, wd)
+    a0 = 2.0 / (1 + math.exp(-2.0)) * 3.0
+    a2 = -1.0 / (1 + math.exp(1.0)) * 1.0
+    assert np.allclose(y, [[a0, 2 * a0], [0.0, 0.0], [a2, 2 * a2]], rtol=1e-15, atol=0)
+
+
+def test_mlp_matches_matmul(oracle_lib):
+    rng = np.random.default_rng(5)
+    T, H, I = 7, 64, 48
+    x = torch.from_numpy(rng.standard_normal((T, H), dtype=np.float32)).to(torch.bfloat16)
+    w = inputs.mlp_weights(H, I, seed=6)
+    y = oracle_lib.mlp(x, w.w_gate_up, w.w_down)
+    gu = _f64(x) @ _f64(w.w_gate_up).T
+    g, u = gu[:, :I], gu[:, I:]
+    ref = (g / (1 + np.exp(-g)) * u) @ _f64(w.w_down).T
+    assert y.shape == (T, H)
+    assert _rel(y, ref) < 1e-13
+
+
+def test_mlp_row_subset_is_those_rows(oracle_lib):
+    w = inputs.mlp_weights(32, 64, seed=7)
+    x = inputs.tokens(6, 32, seed=8)
+    full = oracle_lib.mlp(x, w.w_gate_up, w.w_down)
+    rows = [4, 0, 5, 4]
+    sub = oracle_lib.mlp(x, w.w_gate_up, w.w_down, rows=rows)
+    assert np.array_equal(sub, full[rows])
+    # rows are independent: permuting the input permutes the output
+    perm = [3, 1, 5, 0, 2, 4]
+    assert np.array_equal(oracle_lib.mlp(x[perm], w.w_gate_up, w.w_down), full[perm])
+
+
+def test_mlp_is_a_one_expert_layer(oracle_lib):
+    # one expert, top-1: the routing weight is exactly 1 and the layer is the MLP
+    w = inputs.mlp_weights(48, 40, seed=9)
+    x = inputs.tokens(5, 48, seed=10)
+    gate_w = torch.zeros(48, 1, dtype=torch.bfloat16)
+    moe = oracle_lib.moe_layer(x, gate_w, w.w_gate_up[None], w.w_down[None], 1)
+    assert np.array_equal(oracle_lib.mlp(x, w.w_gate_up, w.w_down), moe)
+
+
+# ---------------------------------------------------------------------------
 # Whole layer
 # ---------------------------------------------------------------------------
 
