@@ -194,6 +194,58 @@ int etc_chain_forward(etc_plan_t plan, void* stream, const void* x, const void* 
                       const void* const* w_gate_up, const void* const* w_down, int T, void* out);
 
 /*
+ * Dense MLP, out = (silu(x Wg^T) * (x Wu^T)) Wd^T, run by the same persistent
+ * megakernel, operand pipeline and event counters as the MoE layer, with one
+ * always-taken weight set and no routing stages.  The shapes are the dense MLP
+ * configurations of the paper summary page's appendix (Table 4: S, H, I); the
+ * pages name no activation, and SwiGLU (the experts' FFN) is used.  Gate/up
+ * tiles of 128-token chunks need no input event; the down tiles of chunk c
+ * wait on chunk c's counter, which its gate/up tiles notify (count-up, re-armed
+ * by the chunk's last down tile).  STATIC is the schedule the pages expect to
+ * win on regular dense layers (Table 3; podcast transcript, cue 13); DYNAMIC
+ * seeds the queue with every gate/up tile and pushes a chunk's down tiles
+ * when its counter completes.
+ */
+typedef struct {
+  int hidden;        /* H: multiple of 128, at most 16384 */
+  int inter;         /* I: multiple of 64, at most 65536 */
+  int t_max;         /* largest token count a call may pass: 1..65536 */
+  int sched;         /* ETC_SCHED_STATIC or ETC_SCHED_DYNAMIC */
+  unsigned long long wait_timeout_ns; /* device wait limit (0 -> 2 s) */
+  unsigned debug_flags;              /* ETC_DEBUG_POISON, ETC_DEBUG_TRACE */
+  int out_dtype;                     /* ETC_OUT_F32 (default) or ETC_OUT_BF16 */
+} etc_mlp_opts;
+
+/*
+ * Creates a dense MLP plan: validates the options, allocates the event
+ * counters, the task queue and the activation buffer act bf16 [t_max, I].
+ * The plan serves etc_mlp_forward(_unfused) and the plan-level calls
+ * (etc_plan_check, _reset, _stats, _destroy, etc_moe_debug_trace,
+ * etc_moe_debug_buffer with which = 1); the MoE entry points refuse it with
+ * ETC_ERR_INVALID, and etc_mlp_forward refuses MoE plans.
+ */
+int etc_mlp_plan(etc_plan_t* plan, const etc_mlp_opts* opts);
+
+/*
+ * One dense MLP in ONE kernel launch on `stream`:
+ *   x          bf16 [T, H]
+ *   w_gate_up  bf16 [2I, H]   rows 0..I-1 gate, rows I..2I-1 up (K-major)
+ *   w_down     bf16 [H, I]    (K-major)
+ *   out        fp32 [T, H] (bf16 [T, H] when opts.out_dtype = ETC_OUT_BF16)
+ * Accumulation is fp32 on the tensor cores; the SwiGLU activation is rounded
+ * to bf16 (the operand of the second GEMM); each output element is written
+ * once, by the down tile that owns it (the result is deterministic).
+ * 0 <= T <= t_max; T == 0 returns ETC_OK without launching.
+ */
+int etc_mlp_forward(etc_plan_t plan, void* stream, const void* x, const void* w_gate_up,
+                    const void* w_down, int T, void* out);
+
+/* The same MLP by the same task code in two launches (gate/up stage, then
+ * down stage): the unfused baseline of the one-launch kernel. */
+int etc_mlp_forward_unfused(etc_plan_t plan, void* stream, const void* x, const void* w_gate_up,
+                            const void* w_down, int T, void* out);
+
+/*
  * Reads the plan's device status (after the caller has synchronised the
  * stream of the last call): ETC_OK, or ETC_ERR_TIMEOUT with the site in
  * etc_last_error().  Does not synchronise anything itself.

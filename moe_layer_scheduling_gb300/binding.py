@@ -33,6 +33,7 @@ EXPORTED = [
     "etc_plan_check", "etc_plan_reset",
     "etc_plan_stats", "etc_plan_destroy", "etc_splitk_rowsum", "etc_splitk_rowsum_ex",
     "etc_splitk_check", "etc_splitk_rowsum_noalloc", "etc_launch_count", "etc_last_error",
+    "etc_mlp_plan", "etc_mlp_forward", "etc_mlp_forward_unfused",
 ]
 
 
@@ -50,6 +51,14 @@ class etc_moe_opts(ctypes.Structure):
         ("router_bias", ctypes.c_void_p), ("wait_timeout_ns", ctypes.c_ulonglong),
         ("debug_flags", ctypes.c_uint), ("debug_arg", ctypes.c_int),
         ("out_dtype", ctypes.c_int),
+    ]
+
+
+class etc_mlp_opts(ctypes.Structure):
+    _fields_ = [
+        ("hidden", ctypes.c_int), ("inter", ctypes.c_int), ("t_max", ctypes.c_int),
+        ("sched", ctypes.c_int), ("wait_timeout_ns", ctypes.c_ulonglong),
+        ("debug_flags", ctypes.c_uint), ("out_dtype", ctypes.c_int),
     ]
 
 
@@ -78,6 +87,9 @@ def load(build_if_missing: bool = True):
     L.etc_moe_debug_buffer.argtypes = [P, P, I, P, ctypes.c_ulonglong]
     L.etc_moe_debug_trace.argtypes = [P, P, P, I]
     L.etc_chain_forward.argtypes = [P, P, P, P, P, P, P, P, I, P]
+    L.etc_mlp_plan.argtypes = [ctypes.POINTER(P), ctypes.POINTER(etc_mlp_opts)]
+    L.etc_mlp_forward.argtypes = [P, P, P, P, P, I, P]
+    L.etc_mlp_forward_unfused.argtypes = [P, P, P, P, P, I, P]
     L.etc_plan_check.argtypes = [P]
     L.etc_plan_reset.argtypes = [P, P]
     L.etc_plan_stats.argtypes = [P, ctypes.POINTER(LL), I]
@@ -167,6 +179,24 @@ def etc_moe_forward_unfused(plan: Plan, x, gate_w, w_gate_up, w_down, T, out, st
     return _check(load().etc_moe_forward_unfused(plan.handle, _stream(stream), _ptr(x),
                                                  _ptr(gate_w), _ptr(w_gate_up), _ptr(w_down),
                                                  int(T), _ptr(out)))
+
+
+def etc_mlp_plan(hidden, inter, t_max, sched=ETC_SCHED_STATIC, wait_timeout_ns=0, debug_flags=0,
+                 out_dtype=ETC_OUT_F32) -> Plan:
+    o = etc_mlp_opts(hidden, inter, t_max, sched, wait_timeout_ns, debug_flags, out_dtype)
+    h = ctypes.c_void_p()
+    _check(load().etc_mlp_plan(ctypes.byref(h), ctypes.byref(o)))
+    return Plan(h.value, o)
+
+
+def etc_mlp_forward(plan: Plan, x, w_gate_up, w_down, T, out, stream=None):
+    return _check(load().etc_mlp_forward(plan.handle, _stream(stream), _ptr(x), _ptr(w_gate_up),
+                                         _ptr(w_down), int(T), _ptr(out)))
+
+
+def etc_mlp_forward_unfused(plan: Plan, x, w_gate_up, w_down, T, out, stream=None):
+    return _check(load().etc_mlp_forward_unfused(plan.handle, _stream(stream), _ptr(x),
+                                                 _ptr(w_gate_up), _ptr(w_down), int(T), _ptr(out)))
 
 
 def etc_moe_route_from_logits(plan: Plan, logits, x, T, stream=None):

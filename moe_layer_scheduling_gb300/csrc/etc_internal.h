@@ -118,6 +118,8 @@ struct BlockWs {
   int* ev_expert;      // [E] count-down from counts[e] (permuted rows still missing)
   int* ev_act;         // [C_max] count-down from gate/up tiles per chunk
   int* ev_down;        // [C_max] count-down from down tiles per chunk
+                       // (dense MLP: ev_act / ev_down count up and are re-armed
+                       // to 0 by the chunk's last down tile)
   int* ev_tok;         // [nb_max] count-down from expert rows per token block
   unsigned* norm_flag; // [nb_max] epoch once the token block is normalised (chain)
   unsigned* comb_flag; // [nb_max] epoch once the token block is combined (chain)
@@ -147,9 +149,9 @@ struct Workspace {
 struct MegaParams {
   CUtensorMap tm_wgu[kMaxBlocks];  // [E*2I, H] box 64x64, 128B swizzle
   CUtensorMap tm_wd[kMaxBlocks];   // [E*H, I]  box 64x64
-  CUtensorMap tm_xperm;            // [R_max, H] box 16x64
+  CUtensorMap tm_xperm;            // [R_max, H] box 16x64 (dense MLP: the caller's x [T, H])
   CUtensorMap tm_act;              // [R_max, I] box 16x64
-  CUtensorMap tm_xperm64;          // [R_max, H] box 64x64
+  CUtensorMap tm_xperm64;          // [R_max, H] box 64x64 (dense MLP: x)
   CUtensorMap tm_act64;            // [R_max, I] box 64x64
   CUtensorMap tm_wg[kMaxBlocks];   // router weight [H, E], box 64 experts x 64 rows (MN-major A)
   CUtensorMap tm_xr;               // router input rows [T, H] (x, or xn in the chain), box 32x64
@@ -173,7 +175,10 @@ struct MegaParams {
   int NT_gu, NT_dn;
   int wide;      // expert tiles of 256 weight rows (two MMAs per K step)
   unsigned epoch;
-  int mode;  // 0 static, 1 dynamic
+  int mode;  // 0 static, 1 dynamic, 2 mixed
+  int dense;     // dense MLP: one weight set, chunks are 128-row slices of x, no routing
+  int n_chunks;  // dense MLP: chunks of this call
+  int q_total;   // dense MLP: tasks of the call (known on the host)
   int stage_lo, stage_hi;
   unsigned long long timeout_ns;
   int debug_flags, debug_arg;

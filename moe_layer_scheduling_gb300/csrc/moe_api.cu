@@ -45,6 +45,10 @@ struct etc_plan_s {
   unsigned epoch = 0;
   long long launches = 0;
   int last_T = 0;
+  int dense = 0;                    // dense MLP plan (etc_mlp_plan)
+  const void* cached_xd = nullptr;  // dense MLP: token-operand maps of the caller's x, per (pointer, T)
+  int cached_xdT = 0;
+  CUtensorMap tm_xd16{}, tm_xd64{};
 };
 
 namespace {
@@ -205,6 +209,7 @@ struct CallArgs {
 int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int stage_lo,
              int stage_hi, int mode) {
   if (!p) return set_error(ETC_ERR_INVALID, "plan is NULL");
+  if (p->dense) return set_error(ETC_ERR_INVALID, "a dense MLP plan serves etc_mlp_forward only");
   if (a.T < 0 || a.T > p->T_max)
     return set_error(ETC_ERR_INVALID, "T=%d outside [0, t_max=%d]", a.T, p->T_max);
   if (a.T == 0) return ETC_OK;
@@ -333,17 +338,109 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   return ETC_OK;
 }
 
-}  // namespace
+int validate_mlp_opts(const etc_mlp_opts* o) {
+  if (!o) return set_error(ETC_ERR_INVALID, "opts is NULL");
+  if (o->hidden <= 0 || o->hidden % 128 != 0 || o->hidden > 16384)
+    return set_error(ETC_ERR_INVALID, "hidden=%d must be a multiple of 128 in [128, 16384]",
+                     o->hidden);
+  if (o->inter <= 0 || o->inter % 64 != 0 || o->inter > 65536)
+    return set_error(ETC_ERR_INVALID, "inter=%d must be a multiple of 64 in [64, 65536]", o->inter);
+  if (o->t_max < 1 || o->t_max > 65536)
+    return set_error(ETC_ERR_INVALID, "t_max=%d must be in [1, 65536]", o->t_max);
+  if (o->sched != ETC_SCHED_STATIC && o->sched != ETC_SCHED_DYNAMIC)
+    return set_error(ETC_ERR_INVALID, "sched=%d: the dense MLP takes STATIC or DYNAMIC", o->sched);
+  if (o->out_dtype != ETC_OUT_F32 && o->out_dtype != ETC_OUT_BF16)
+    return set_error(ETC_ERR_INVALID, "out_dtype=%d unknown", o->out_dtype);
+  return ETC_OK;
+}
 
-extern "C" {
-
-int etc_moe_plan(etc_plan_t* out, const etc_moe_opts* opts) {
-  clear_error();
-  if (!out) return set_error(ETC_ERR_INVALID, "plan pointer is NULL");
-  *out = nullptr;
-  int r = validate_opts(opts);
+// One dense MLP call: gate/up and down tiles of the same megakernel over
+// 128-row chunks of x (one launch, or one per stage for the ablation).
+int run_dense_call(etc_plan_t p, void* stream, const void* x, const void* wgu, const void* wd,
+                   int T, void* out, bool unfused) {
+  if (!p) return set_error(ETC_ERR_INVALID, "plan is NULL");
+  if (!p->dense) return set_error(ETC_ERR_INVALID, "plan is not a dense MLP plan (etc_mlp_plan)");
+  if (T < 0 || T > p->T_max)
+    return set_error(ETC_ERR_INVALID, "T=%d outside [0, t_max=%d]", T, p->T_max);
+  if (T == 0) return ETC_OK;
+  if (!x || !out || !wgu || !wd || !aligned16(x) || !aligned16(out) || !aligned16(wgu) ||
+      !aligned16(wd))
+    return set_error(ETC_ERR_INVALID, "x, weights and out must be 16-byte aligned device pointers");
+  int st = status_of(p);
+  if (st != ETC_OK) return set_error(ETC_ERR_STATE, "%s", last_error());
+  int dev = 0;
+  ETC_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != p->device)
+    return set_error(ETC_ERR_INVALID, "plan belongs to device %d, current device is %d", p->device, dev);
+  int r = weight_maps(p, 0, wgu, wd);
   if (r != ETC_OK) return r;
+  if (p->cached_xd != x || p->cached_xdT != T) {
+    // Rows past T read as zero: the maps' extent is the call's T.
+    if (encode_tensor_map_2d_bf16(&p->tm_xd16, x, p->H, T, kBK, 16) != CUDA_SUCCESS ||
+        encode_tensor_map_2d_bf16(&p->tm_xd64, x, p->H, T, kBK, 64) != CUDA_SUCCESS)
+      return set_error(ETC_ERR_CUDA, "tensor map (x) failed");
+    p->cached_xd = x;
+    p->cached_xdT = T;
+  }
+  MegaParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  prm.tm_wgu[0] = p->tm_wgu[0];
+  prm.tm_wd[0] = p->tm_wd[0];
+  prm.tm_xperm = p->tm_xd16;
+  prm.tm_xperm64 = p->tm_xd64;
+  prm.tm_act = p->tm_act;
+  prm.tm_act64 = p->tm_act64;
+  prm.ws = p->ws;
+  prm.x = static_cast<const __nv_bfloat16*>(x);
+  prm.out = out;
+  prm.out_bf16 = p->opts.out_dtype == ETC_OUT_BF16 ? 1 : 0;
+  prm.H = p->H;
+  prm.E = 1;
+  prm.k = 1;
+  prm.I = p->I;
+  prm.T_max = p->T_max;
+  prm.n_blocks = 1;
+  prm.T = T;
+  prm.nb = (T + kTB - 1) / kTB;
+  prm.NC = 1;
+  prm.HC = p->H;
+  prm.PP = 1;
+  prm.T_pad = prm.nb * kTB;
+  prm.wide = (T >= 64 && p->I % kGuRowsW == 0 && p->H % kDnRowsW == 0) ? 1 : 0;
+  prm.NT_gu = p->I / (prm.wide ? kGuRowsW : kGuRows);
+  prm.NT_dn = p->H / (prm.wide ? kDnRowsW : kDnRows);
+  prm.dense = 1;
+  prm.n_chunks = (T + kBT - 1) / kBT;
+  prm.q_total = prm.n_chunks * (prm.NT_gu + prm.NT_dn);
+  if (++p->epoch == 0) p->epoch = 1;
+  prm.epoch = p->epoch;
+  prm.mode = unfused ? ETC_SCHED_STATIC : p->opts.sched;
+  prm.timeout_ns = p->opts.wait_timeout_ns ? p->opts.wait_timeout_ns : 2000000000ull;
+  prm.debug_flags = static_cast<int>(p->opts.debug_flags);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p->ws.trace) ETC_CUDA_TRY(cudaMemsetAsync(p->ws.trace, 0, 8, s));
+  if (p->opts.debug_flags & ETC_DEBUG_POISON)
+    ETC_CUDA_TRY(cudaMemsetAsync(p->ws.act, 0xFF, static_cast<size_t>(T) * p->I * 2, s));
+  // Fused: one launch of both stages; unfused: the gate/up stage, then the down stage.
+  const int stage[2] = {TK_GU, TK_DN};
+  for (int i = 0; i < (unfused ? 2 : 1); ++i) {
+    prm.stage_lo = unfused ? stage[i] : TK_GU;
+    prm.stage_hi = unfused ? stage[i] : TK_DN;
+    ETC_CUDA_TRY(launch_megakernel(prm, p->grid, s));
+    ++p->launches;
+    g_launches.fetch_add(1);
+  }
+  p->last_T = T;
+  return ETC_OK;
+}
+
+int plan_moe_buffers(etc_plan_t p);
+
+// Plan body shared by the MoE layer and the dense MLP (options validated).
+int make_plan(etc_plan_t* out, const etc_moe_opts* opts, bool dense) {
+  int r = ETC_OK;
   etc_plan_t p = new etc_plan_s();
+  p->dense = dense ? 1 : 0;
   p->opts = *opts;
   p->H = opts->hidden;
   p->E = opts->n_experts;
@@ -402,28 +499,12 @@ int etc_moe_plan(etc_plan_t* out, const etc_moe_opts* opts) {
 
   void* m = nullptr;
   const size_t R = static_cast<size_t>(p->R_max);
-  if ((r = alloc_dev(p, &m, R * p->H * 2)) != ETC_OK) return fail(r);
-  p->ws.x_perm = static_cast<__nv_bfloat16*>(m);
   if ((r = alloc_dev(p, &m, R * p->I * 2)) != ETC_OK) return fail(r);
   p->ws.act = static_cast<__nv_bfloat16*>(m);
-  if (opts->out_dtype == ETC_OUT_BF16) {  // fp32 accumulator behind a bf16 output
-    if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 4)) != ETC_OK) return fail(r);
-    p->ws.acc = static_cast<float*>(m);
-  }
-  // Normalised rows of the chain (any plan may be given to etc_chain_forward,
-  // a one-block chain included).
-  if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 2)) != ETC_OK) return fail(r);
-  p->ws.xn = static_cast<__nv_bfloat16*>(m);
-  if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 2)) != ETC_OK) return fail(r);
-  p->ws.xn_lo = static_cast<__nv_bfloat16*>(m);
-  if (encode_tensor_map_2d_bf16(&p->tm_xn, p->ws.xn, p->H, p->T_max, kBK, kTB) != CUDA_SUCCESS ||
-      encode_tensor_map_2d_bf16(&p->tm_xnlo, p->ws.xn_lo, p->H, p->T_max, kBK, kTB) != CUDA_SUCCESS)
-    return fail(set_error(ETC_ERR_CUDA, "tensor map encoding of the normalised rows failed"));
-  if (p->n_blocks > 1) {
-    if ((r = alloc_dev(p, &m, static_cast<size_t>(p->n_blocks - 1) * p->T_max * p->H * 4)) != ETC_OK)
-      return fail(r);
-    p->ws.resid = static_cast<float*>(m);
-  }
+  if (encode_tensor_map_2d_bf16(&p->tm_act, p->ws.act, p->I, R, kBK, 16) != CUDA_SUCCESS ||
+      encode_tensor_map_2d_bf16(&p->tm_act64, p->ws.act, p->I, R, kBK, 64) != CUDA_SUCCESS)
+    return fail(set_error(ETC_ERR_CUDA, "tensor map encoding of the workspace failed"));
+  if (!dense && (r = plan_moe_buffers(p)) != ETC_OK) return fail(r);
   for (int i = 0; i < 2; ++i) {
     if ((r = alloc_dev(p, &m, static_cast<size_t>(p->ws.qcap) * 8)) != ETC_OK) return fail(r);
     p->ws.qslots[i] = static_cast<unsigned long long*>(m);
@@ -441,14 +522,86 @@ int etc_moe_plan(etc_plan_t* out, const etc_moe_opts* opts) {
     return fail(set_error(ETC_ERR_CUDA, "cudaHostAlloc failed"));
   std::memset(hs, 0, sizeof *hs);
   p->ws.status_host = hs;
-
-  if (encode_tensor_map_2d_bf16(&p->tm_xperm, p->ws.x_perm, p->H, R, kBK, 16) != CUDA_SUCCESS ||
-      encode_tensor_map_2d_bf16(&p->tm_act, p->ws.act, p->I, R, kBK, 16) != CUDA_SUCCESS ||
-      encode_tensor_map_2d_bf16(&p->tm_xperm64, p->ws.x_perm, p->H, R, kBK, 64) != CUDA_SUCCESS ||
-      encode_tensor_map_2d_bf16(&p->tm_act64, p->ws.act, p->I, R, kBK, 64) != CUDA_SUCCESS)
-    return fail(set_error(ETC_ERR_CUDA, "tensor map encoding of the workspace failed"));
   *out = p;
   return ETC_OK;
+}
+
+// Buffers only the MoE layer and the chain use: permuted rows, the fp32
+// combine accumulator, the chain's normalised rows and residual stream.
+int plan_moe_buffers(etc_plan_t p) {
+  int r = ETC_OK;
+  void* m = nullptr;
+  const size_t R = static_cast<size_t>(p->R_max);
+  if ((r = alloc_dev(p, &m, R * p->H * 2)) != ETC_OK) return r;
+  p->ws.x_perm = static_cast<__nv_bfloat16*>(m);
+  if (encode_tensor_map_2d_bf16(&p->tm_xperm, p->ws.x_perm, p->H, R, kBK, 16) != CUDA_SUCCESS ||
+      encode_tensor_map_2d_bf16(&p->tm_xperm64, p->ws.x_perm, p->H, R, kBK, 64) != CUDA_SUCCESS)
+    return set_error(ETC_ERR_CUDA, "tensor map encoding of the workspace failed");
+  if (p->opts.out_dtype == ETC_OUT_BF16) {  // fp32 accumulator behind a bf16 output
+    if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 4)) != ETC_OK) return r;
+    p->ws.acc = static_cast<float*>(m);
+  }
+  // Normalised rows of the chain (any plan may be given to etc_chain_forward,
+  // a one-block chain included).
+  if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 2)) != ETC_OK) return r;
+  p->ws.xn = static_cast<__nv_bfloat16*>(m);
+  if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 2)) != ETC_OK) return r;
+  p->ws.xn_lo = static_cast<__nv_bfloat16*>(m);
+  if (encode_tensor_map_2d_bf16(&p->tm_xn, p->ws.xn, p->H, p->T_max, kBK, kTB) != CUDA_SUCCESS ||
+      encode_tensor_map_2d_bf16(&p->tm_xnlo, p->ws.xn_lo, p->H, p->T_max, kBK, kTB) != CUDA_SUCCESS)
+    return set_error(ETC_ERR_CUDA, "tensor map encoding of the normalised rows failed");
+  if (p->n_blocks > 1) {
+    if ((r = alloc_dev(p, &m, static_cast<size_t>(p->n_blocks - 1) * p->T_max * p->H * 4)) != ETC_OK)
+      return r;
+    p->ws.resid = static_cast<float*>(m);
+  }
+  return ETC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int etc_moe_plan(etc_plan_t* out, const etc_moe_opts* opts) {
+  clear_error();
+  if (!out) return set_error(ETC_ERR_INVALID, "plan pointer is NULL");
+  *out = nullptr;
+  const int r = validate_opts(opts);
+  if (r != ETC_OK) return r;
+  return make_plan(out, opts, false);
+}
+
+int etc_mlp_plan(etc_plan_t* out, const etc_mlp_opts* opts) {
+  clear_error();
+  if (!out) return set_error(ETC_ERR_INVALID, "plan pointer is NULL");
+  *out = nullptr;
+  const int r = validate_mlp_opts(opts);
+  if (r != ETC_OK) return r;
+  // One always-taken weight set: the plan of a one-expert, top-1 layer.
+  etc_moe_opts o{};
+  o.hidden = opts->hidden;
+  o.n_experts = 1;
+  o.top_k = 1;
+  o.inter = opts->inter;
+  o.t_max = opts->t_max;
+  o.sched = opts->sched;
+  o.n_blocks = 1;
+  o.wait_timeout_ns = opts->wait_timeout_ns;
+  o.debug_flags = opts->debug_flags & (ETC_DEBUG_POISON | ETC_DEBUG_TRACE);
+  o.out_dtype = opts->out_dtype;
+  return make_plan(out, &o, true);
+}
+
+int etc_mlp_forward(etc_plan_t p, void* stream, const void* x, const void* w_gate_up,
+                    const void* w_down, int T, void* out) {
+  clear_error();
+  return run_dense_call(p, stream, x, w_gate_up, w_down, T, out, false);
+}
+
+int etc_mlp_forward_unfused(etc_plan_t p, void* stream, const void* x, const void* w_gate_up,
+                            const void* w_down, int T, void* out) {
+  clear_error();
+  return run_dense_call(p, stream, x, w_gate_up, w_down, T, out, true);
 }
 
 void etc_plan_destroy(etc_plan_t p) {
@@ -528,6 +681,7 @@ int etc_moe_debug_routing(etc_plan_t p, void* stream, int block, void* logits, v
                           void* topk_w, void* counts, void* exp_indptr, void* pos) {
   clear_error();
   if (!p) return set_error(ETC_ERR_INVALID, "plan is NULL");
+  if (p->dense) return set_error(ETC_ERR_INVALID, "a dense MLP plan has no routing");
   if (block < 0 || block >= p->n_blocks) return set_error(ETC_ERR_INVALID, "bad block %d", block);
   const BlockWs& b = p->ws.blk[block];
   const size_t T = p->last_T;
@@ -558,6 +712,7 @@ int etc_moe_debug_buffer(etc_plan_t p, void* stream, int which, void* dst,
   } else {
     return set_error(ETC_ERR_INVALID, "unknown buffer %d", which);
   }
+  if (!src) return set_error(ETC_ERR_INVALID, "this plan holds no buffer %d", which);
   if (bytes > cap) return set_error(ETC_ERR_INVALID, "buffer %d holds %llu bytes", which, cap);
   ETC_CUDA_TRY(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice,
                                static_cast<cudaStream_t>(stream)));

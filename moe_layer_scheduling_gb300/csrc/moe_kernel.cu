@@ -94,7 +94,11 @@ __device__ __forceinline__ QueueView queue_of(const MegaParams& p) {
   q.tail = p.ws.qtail[par];
   q.cap = p.ws.qcap;
   // DYNAMIC seeds the queue with the first tasks (virtual slots 0..n_seed-1).
-  q.n_seed = p.mode == ETC_SCHED_DYNAMIC ? (p.use_norm ? p.nb : p.n_router) : 0;
+  // (dense MLP: every gate/up tile).
+  q.n_seed = p.mode != ETC_SCHED_DYNAMIC ? 0
+             : p.dense                   ? p.n_chunks * p.NT_gu
+             : p.use_norm                ? p.nb
+                                         : p.n_router;
   q.epoch = p.epoch;
   return q;
 }
@@ -107,8 +111,9 @@ __device__ __forceinline__ bool tiles_queued(const MegaParams& p) { return p.mod
 // Whether block blk's combine finaliser has work: releasing the next block's
 // RMSNorm in the chain, or rounding the last block's rows to a bf16 output.
 // Otherwise the down tiles' fp32 additions are the result and no COMB runs.
+// The dense MLP's down tiles store their outputs themselves.
 __device__ __forceinline__ bool needs_comb(const MegaParams& p, int blk) {
-  return blk < p.n_blocks - 1 || p.out_bf16 != 0;
+  return !p.dense && (blk < p.n_blocks - 1 || p.out_bf16 != 0);
 }
 
 // Operand stages of a call: narrow tiles 6 x 32 KB (16 KB of weights, then up
@@ -674,7 +679,7 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
   // Down tiles: each chunk row's token and routing weight, for the combine.
   int* s_rtok = reinterpret_cast<int*>(simt + 2 * kEpiHalfBytes);                 // [128]
   float* s_rw = reinterpret_cast<float*>(simt + 2 * kEpiHalfBytes + 4 * kBT);     // [128]
-  if (t.type == TK_DN) {
+  if (t.type == TK_DN && !p.dense) {
     for (int r = wt; r < t.rows; r += kNumWorkers) {
       s_rtok[r] = __ldcg(B.row_token + t.row0 + r);
       s_rw[r] = __ldcg(B.row_w + t.row0 + r);
@@ -734,13 +739,15 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
       }
     } else {
       // Weighted combine fused here: out[token] += w * y, 4 columns per red op
-      // (wide tiles: two 128-column halves, one per accumulator half).
+      // (wide tiles: two 128-column halves, one per accumulator half).  The
+      // dense MLP's tile owns its outputs and stores them.
       float* S32 = reinterpret_cast<float*>(epi + h * kEpiHalfBytes);  // [16][128] fp32
       const int nhalf = p.wide ? 2 : 1;
       for (int hc = 0; hc < nhalf * ncb; ++hc) {
         const int half = hc / ncb, cb = hc - half * ncb;
         if ((cb & 1) != h) continue;  // the two worker halves take alternate column blocks
-        float* accr = acc_rows(p, t.blk) + t.b * (p.wide ? kDnRowsW : kDnRows) + half * 128;
+        const int col0 = t.b * (p.wide ? kDnRowsW : kDnRows) + half * 128;
+        float* accr = p.dense ? nullptr : acc_rows(p, t.blk) + col0;
         float v[16];
         tmem_ld16(tbase + half * (kAccCols / 2) + cb * 16, v);
 #pragma unroll
@@ -750,7 +757,20 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
         for (int rep = 0; rep < 4; ++rep) {
           const int idx = i128 + 128 * rep;
           const int r = cb * 16 + (idx >> 5), chunk = idx & 31;
-          if (r < t.rows) {
+          if (r < t.rows && p.dense) {
+            const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
+            const size_t o = static_cast<size_t>(t.row0 + r) * p.H + col0 + chunk * 4;
+            if (p.out_bf16) {
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(val.x, val.y);
+              const __nv_bfloat162 hi = __floats2bfloat162_rn(val.z, val.w);
+              uint2 pk;
+              pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+              pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+              *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + o) = pk;
+            } else {
+              *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = val;
+            }
+          } else if (r < t.rows) {
             const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
             const float wr = s_rw[r];
             red_add_v4(accr + static_cast<size_t>(s_rtok[r]) * p.H + chunk * 4,
@@ -832,12 +852,20 @@ __device__ __forceinline__ int notify_primary(const MegaParams& p, const Task& t
       }
       return atom_add_acq_rel(B.ev_route, 1) + 1 == p.nb;
     case TK_GU:
+      if (p.dense) {  // count-up chunk counters (no scan to arm them)
+        if (!tiles_queued(p)) {
+          red_add_relaxed(&B.ev_act[t.a], 1);
+          return 0;
+        }
+        return atom_add_acq_rel(&B.ev_act[t.a], 1) + 1 == p.NT_gu;
+      }
       if (!tiles_queued(p)) {
         red_add_relaxed(&B.ev_act[t.a], -1);
         return 0;
       }
       return notify(&B.ev_act[t.a], 1) == 0;
     case TK_DN:  // both modes need to know which tile finished the chunk
+      if (p.dense) return atom_add_acq_rel(&B.ev_down[t.a], 1) + 1 == p.NT_dn;
       return notify(&B.ev_down[t.a], 1) == 0;
     case TK_COMB:
       if (p.use_norm) st_relaxed(reinterpret_cast<int*>(&B.comb_flag[t.a]), static_cast<int>(p.epoch));
@@ -927,6 +955,15 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
       if (fire) queue_push_warp(q, p.NT_dn, [&](int i) { return task_enc(TK_DN, t.blk, t.a, i); }, clk, lane);
       break;
     case TK_DN:
+      if (p.dense) {
+        // Last down tile of the chunk: every tile of the chunk has passed its
+        // wait, so both counters go back to 0 for the next call.
+        if (fire && lane == 0) {
+          st_relaxed(&B.ev_act[t.a], 0);
+          st_relaxed(&B.ev_down[t.a], 0);
+        }
+        break;
+      }
       if (fire && needs_comb(p, t.blk)) {
         // Finisher of the chunk: notify each token block by its number of rows.
         // The chunk's rows are in ascending token order, so blocks form runs;
@@ -1049,7 +1086,7 @@ __device__ void run_workers(const MegaParams& p, Ctrl* c, uint8_t* simt, uint8_t
         r[0] = (static_cast<unsigned long long>(t.type) << 56) |
                (static_cast<unsigned long long>(t.blk) << 48) |
                (static_cast<unsigned long long>(blockIdx.x) << 32) |
-               (static_cast<unsigned long long>(t.a) << 8) | static_cast<unsigned long long>(t.b);
+               (static_cast<unsigned long long>(t.a) << 8) | static_cast<unsigned long long>(t.b & 0xFF);
         r[1] = t.t_disp;
         r[2] = t_start;
         r[3] = globaltimer_ns();
@@ -1217,10 +1254,43 @@ __device__ __forceinline__ Task make_task(int type, int blk, int a, int b) {
 }
 
 __device__ __forceinline__ void resolve_chunk(const MegaParams& p, Task& t) {
+  if (p.dense) {  // chunk a = rows [128a, min(128a + 128, T)) of x
+    t.e = 0;
+    t.row0 = t.a * kBT;
+    t.rows = min(kBT, p.T - t.row0);
+    return;
+  }
   const BlockWs& B = p.ws.blk[t.blk];
   t.e = __ldcg(B.chunk_expert + t.a);
   t.row0 = __ldcg(B.chunk_row0 + t.a);
   t.rows = __ldcg(B.chunk_rows + t.a);
+}
+
+// Dense MLP gate/up tile g of a call, taken weight-slice major: the tiles that
+// run side by side share one slice of w_gate_up (read from HBM once for all
+// chunks) and read all of x, which stays in L2.
+__device__ __forceinline__ Task dense_gu_task(const MegaParams& p, int g) {
+  Task t = make_task(TK_GU, 0, g % p.n_chunks, g / p.n_chunks);
+  resolve_chunk(p, t);
+  return t;
+}
+
+// Static walk of the dense MLP: gate/up tiles (no input event), then the down
+// tiles chunk by chunk, each after its chunk's gate/up tiles (count-up event).
+__device__ bool sched_static_dense(const MegaParams& p, Ctrl* c, const Clock& clk, RingWriter& rw) {
+  const int G = gridDim.x, cta = blockIdx.x;
+  const BlockWs& B = p.ws.blk[0];
+  bool ok = true;
+  if (p.stage_lo <= TK_GU && p.stage_hi >= TK_GU)
+    for (int g = cta; g < p.n_chunks * p.NT_gu && ok; g += G) ok = rw.emit(dense_gu_task(p, g), clk);
+  if (p.stage_lo <= TK_DN && p.stage_hi >= TK_DN)
+    for (int d = cta; d < p.n_chunks * p.NT_dn && ok; d += G) {
+      Task t = make_task(TK_DN, 0, d / p.NT_dn, d % p.NT_dn);
+      ok = wait_geq(&B.ev_act[t.a], p.NT_gu, clk, TK_DN, t.a);
+      resolve_chunk(p, t);
+      ok = ok && rw.emit(t, clk);
+    }
+  return ok;
 }
 
 // Static walk.  routing_only (MIXED): the walk stops after each block's
@@ -1307,6 +1377,11 @@ __device__ void sched_dynamic(const MegaParams& p, Ctrl* c, const Clock& clk, Ri
     const int idx = atom_add_relaxed(q.head, 1);
     uint32_t desc = 0;
     bool have = false;
+    if (idx < q.n_seed && p.dense) {
+      if (!rw.emit(dense_gu_task(p, idx), clk)) break;
+      continue;
+    }
+    if (p.dense && idx >= p.q_total) break;  // every task of the call has been popped
     if (idx < q.n_seed) {
       desc = p.use_norm ? task_enc(TK_NORM, 0, idx, 0)
                         : task_enc(TK_ROUTER, 0, idx / p.NC, idx % p.NC);
@@ -1398,7 +1473,16 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
   if (w == kWarpSched) {
     if (lane_id() == 0) {
       RingWriter rw{c, 0};
-      if (p.mode == ETC_SCHED_DYNAMIC) {
+      if (p.dense && blockIdx.x == 0) {
+        // Re-arm the other parity's queue for the next call (the routing
+        // scan does this in the MoE layer).
+        const int other = (p.epoch + 1) & 1;
+        *p.ws.qhead[other] = 0;
+        *p.ws.qtail[other] = 0;
+      }
+      if (p.dense && p.mode != ETC_SCHED_DYNAMIC) {
+        sched_static_dense(p, c, clk, rw);
+      } else if (p.mode == ETC_SCHED_DYNAMIC) {
         sched_dynamic(p, c, clk, rw);
       } else if (p.mode == ETC_SCHED_MIXED) {
         if (sched_static(p, c, clk, rw, true)) sched_dynamic(p, c, clk, rw);

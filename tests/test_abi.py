@@ -26,7 +26,8 @@ def lib():
 def test_header_declares_the_boundary():
     names = _declared()
     for required in ("etc_moe_plan", "etc_moe_forward", "etc_splitk_rowsum", "etc_chain_forward",
-                     "etc_moe_forward_unfused", "etc_plan_destroy", "etc_last_error"):
+                     "etc_moe_forward_unfused", "etc_plan_destroy", "etc_last_error",
+                     "etc_mlp_plan", "etc_mlp_forward", "etc_mlp_forward_unfused"):
         assert required in names
 
 
@@ -70,6 +71,30 @@ def test_plan_rejects_bad_options_on_the_host(lib, bad):
     assert rc == binding.ETC_ERR_INVALID
     assert h.value is None
     assert lib.etc_last_error().decode() != ""
+
+
+@pytest.mark.parametrize("bad", [
+    dict(hidden=100), dict(hidden=0), dict(hidden=16512), dict(inter=32), dict(inter=0),
+    dict(inter=65600), dict(t_max=0), dict(t_max=65537), dict(sched=2), dict(sched=7),
+    dict(out_dtype=2),
+])
+def test_mlp_plan_rejects_bad_options_on_the_host(lib, bad):
+    from moe_layer_scheduling_gb300 import binding
+    base = dict(hidden=4096, inter=12288, t_max=8192, sched=0, wait_timeout_ns=0, debug_flags=0,
+                out_dtype=0)
+    base.update(bad)
+    o = binding.etc_mlp_opts(**base)
+    h = ctypes.c_void_p()
+    assert lib.etc_mlp_plan(ctypes.byref(h), ctypes.byref(o)) == binding.ETC_ERR_INVALID
+    assert h.value is None
+    assert lib.etc_last_error().decode() != ""
+
+
+def test_mlp_null_plan_is_rejected(lib):
+    from moe_layer_scheduling_gb300 import binding
+    assert lib.etc_mlp_forward(None, None, None, None, None, 1, None) == binding.ETC_ERR_INVALID
+    assert lib.etc_mlp_forward_unfused(None, None, None, None, None, 1, None) == binding.ETC_ERR_INVALID
+    assert lib.etc_mlp_plan(None, None) == binding.ETC_ERR_INVALID
 
 
 def test_null_plan_is_rejected(lib):
