@@ -441,7 +441,40 @@ def run_extras(args, dev, weights, gw, wgu, wd, bias, x, out, T, plans, peaks, w
                     "tok_s": sum(seq) / tot, "launches_per_call": (B.etc_plan_stats(pc)["launches"] - l0) / len(seq)}
         pc.close()
     res["chain_4blocks_200calls"] = ch
+
+    # --- dense MLP (the appendix's Table 4, MLP-1 = Qwen3-8B shape), same megakernel ---
+    res["dense_mlp"] = run_mlp_rows(dev, tflops_peak, world)
     return res
+
+
+def run_mlp_rows(dev, tflops_peak, world, names=("MLP-1",)):
+    """Dense MLP at Table 4 shapes: static / dynamic one-launch and the two-launch ablation.
+    Weights (> L2) are read from HBM on every call."""
+    import torch
+
+    from moe_layer_scheduling_gb300 import binding as B
+    from moe_layer_scheduling_gb300 import inputs
+    rows = {}
+    for nm in names:
+        S, Hm, Im = inputs.MLP_SHAPES[nm]
+        w, x = inputs.mlp_layer(nm)
+        wgu, wd, xd = w.w_gate_up.to(dev), w.w_down.to(dev), x.to(dev)
+        out = torch.empty(S, Hm, device=dev)
+        flops = 6.0 * S * Hm * Im
+        row = {"S": S, "H": Hm, "I": Im, "gflop": flops / 1e9}
+        for mode, sched, unf in (("static", B.ETC_SCHED_STATIC, False),
+                                 ("dynamic", B.ETC_SCHED_DYNAMIC, False),
+                                 ("unfused_two_launches", B.ETC_SCHED_STATIC, True)):
+            pm = B.etc_mlp_plan(Hm, Im, S, sched=sched)
+            fn = B.etc_mlp_forward_unfused if unf else B.etc_mlp_forward
+            sec = time_gpu(lambda: fn(pm, xd, wgu, wd, S, out), 10, 3, world)
+            assert B.etc_plan_check(pm) == B.ETC_OK, B.etc_last_error()
+            tf = flops / sec / 1e12
+            row[mode] = {"us": sec * 1e6, "tflops": tf, "tensor_frac_of_measured": tf / tflops_peak}
+            pm.close()
+        rows[nm] = row
+        del wgu, wd, xd, out
+    return rows
 
 
 def cpu_baseline(args, wl, budget_s=15.0):
@@ -497,7 +530,7 @@ def run_reference(args, rank, world):
 
 
 def run_single(args):
-    """One workload only, no extras (used for profiling captures): decode or splitk."""
+    """One workload only, no extras (used for profiling captures): decode, splitk or mlp."""
     import torch
 
     from moe_layer_scheduling_gb300 import binding as B
@@ -507,6 +540,19 @@ def run_single(args):
     dev = torch.device("cuda")
     sched = {"static": B.ETC_SCHED_STATIC, "dynamic": B.ETC_SCHED_DYNAMIC,
              "mixed": B.ETC_SCHED_MIXED}[args.sched]
+    if args.workload == "mlp":
+        if sched == B.ETC_SCHED_MIXED:
+            raise SystemExit("the dense MLP takes static or dynamic scheduling")
+        S, Hm, Im = inputs.MLP_SHAPES[args.mlp]
+        w, x = inputs.mlp_layer(args.mlp)
+        wgu, wd, xd = w.w_gate_up.to(dev), w.w_down.to(dev), x.to(dev)
+        out = torch.empty(S, Hm, device=dev)
+        plan = B.etc_mlp_plan(Hm, Im, S, sched=sched)
+        sec = time_gpu(lambda: B.etc_mlp_forward(plan, xd, wgu, wd, S, out), args.steps,
+                       args.warmup, 1)
+        plan.close()
+        return {"workload": f"dense_mlp_{args.mlp}_S{S}_H{Hm}_I{Im}", "sched": args.sched,
+                "us": sec * 1e6, "tflops": 6.0 * S * Hm * Im / sec / 1e12}
     if args.workload == "splitk":
         if sched == B.ETC_SCHED_MIXED:
             raise SystemExit("split-K takes static or dynamic scheduling")
@@ -538,8 +584,9 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "splitk"],
-                    help="prefill = the benchmark line; decode/splitk = one workload (profiling)")
+    ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "splitk", "mlp"],
+                    help="prefill = the benchmark line; decode/splitk/mlp = one workload (profiling)")
+    ap.add_argument("--mlp", default="MLP-1", help="Table 4 shape for --workload mlp")
     ap.add_argument("--sched", default="dynamic", choices=["static", "dynamic", "mixed"])
     ap.add_argument("--clock-window", type=float, default=1.5,
                     help="seconds of load kept up for the clock record (0 for profiler runs)")
