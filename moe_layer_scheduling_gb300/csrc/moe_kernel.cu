@@ -134,7 +134,8 @@ __device__ __forceinline__ StageGeom stage_geom(const MegaParams& p) {
 __device__ __forceinline__ void load_block_input8(const MegaParams& p, int blk, int tok, int c,
                                                   float (&f)[8]);
 __device__ void init_acc_rows(const MegaParams& p, int blk, int tb, int wt);
-__device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt);
+__device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
+                           const int* s_counts = nullptr);
 
 // ---------------------------------------------------------------------------
 // small helpers
@@ -299,13 +300,14 @@ __device__ void topk_rows(const MegaParams& p, const BlockWs& B, const float* s_
 }
 
 // The block's expert histogram: kept per block (the permute derives its row
-// offsets from it) and added into the call's counts (what the scan reads).
+// offsets from it) and added into the call's counts (what the scan reads),
+// unless it is the call's only block and its task runs the scan itself.
 __device__ __forceinline__ void publish_block_counts(const MegaParams& p, const BlockWs& B, int tb,
-                                                     const int* s_cnt, int wt) {
+                                                     const int* s_cnt, int wt, bool sum = true) {
   for (int e = wt; e < p.E; e += kNumWorkers) {
     const int n = s_cnt[e];
     B.blk_cnt[tb * p.E + e] = n;
-    if (n) atomicAdd(B.cnt_acc + e, n);
+    if (n && sum) atomicAdd(B.cnt_acc + e, n);
   }
 }
 
@@ -401,29 +403,35 @@ __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int
   named_bar(1, kNumWorkers);
   topk_rows(p, B, s_log, tok0, s_cnt, ww, lane);
   named_bar(1, kNumWorkers);
-  publish_block_counts(p, B, tb, s_cnt, wt);
+  publish_block_counts(p, B, tb, s_cnt, wt, !p.fuse_scan);
   if (p.fuse_scan) {
-    // One token block: its histogram is the call's counts, so the scan runs
-    // here, one hop sooner (no separate scan task; the notifier leaves
+    // One token block: its histogram (in shared memory) is the call's counts,
+    // so the scan runs here, one hop sooner (no separate scan task, no
+    // round trip through the count accumulators; the notifier leaves
     // ev_route alone).
-    __threadfence();
     named_bar(1, kNumWorkers);
-    scan_block(p, blk, simt, wt);
+    scan_block(p, blk, simt, wt, s_cnt);
   }
   named_bar(1, kNumWorkers);  // notify: ev_route (by the notifier warp)
 }
 
 // counts / exp_indptr / expert chunks / event inits, from the counts the
 // routing tasks summed (thread e < E owns expert e).
-__device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt) {
+__device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
+                           const int* s_counts) {
   const BlockWs& B = p.ws.blk[blk];
   const int E = p.E, nb = p.nb;
-  int* tmp = reinterpret_cast<int*>(simt);  // scan scratch [32]
   int cnt = 0;
   if (wt < E) {
-    cnt = __ldcg(B.cnt_acc + wt);
-    B.cnt_acc[wt] = 0;  // consumed: re-armed for the next call
+    if (s_counts) {
+      cnt = s_counts[wt];
+    } else {
+      cnt = __ldcg(B.cnt_acc + wt);
+      B.cnt_acc[wt] = 0;  // consumed: re-armed for the next call
+    }
   }
+  named_bar(1, kNumWorkers);  // the counts are read before the scan scratch is reused
+  int* tmp = reinterpret_cast<int*>(simt);  // scan scratch [32]
   const int nch = (cnt + kBT - 1) / kBT;
   const int row0 = workers_excl_scan(cnt, tmp, wt);
   const int ch0 = workers_excl_scan(nch, tmp + 16, wt);

@@ -63,8 +63,10 @@ def _check_chain(plan, blocks, x, out, oracle_lib):
     assert flipped.sum() <= max(3, int(0.15 * T)), f"{int(flipped.sum())} of {T} tokens re-routed"
     keep = ~flipped
     rms = float(np.sqrt(np.mean(ref * ref)))
-    err = float(np.max(np.abs(out[keep] - ref[keep])))
-    assert err <= 2e-2 * rms, f"chain max err {err:.4e} > {2e-2 * rms:.4e}"
+    assert np.isfinite(out).all()
+    if keep.any():  # (a one-token call whose token is a near-tie leaves nothing to compare)
+        err = float(np.max(np.abs(out[keep] - ref[keep])))
+        assert err <= 2e-2 * rms, f"chain max err {err:.4e} > {2e-2 * rms:.4e}"
 
 
 @pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC])

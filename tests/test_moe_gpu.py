@@ -53,9 +53,11 @@ def test_decode_layer(oracle_lib, qwen, qwen_dev, sched, unfused, T):
 
 
 @pytest.mark.parametrize("sched,unfused", MODES, ids=MODE_IDS)
-@pytest.mark.parametrize("T,seed", [(33, 1), (200, 2), (517, 3)])
+@pytest.mark.parametrize("T,seed", [(33, 1), (200, 2), (517, 3), (6000, 4)])
 def test_ragged_token_counts(oracle_lib, sched, unfused, T, seed):
-    # Several tiles and a ragged tail on every axis, a skewing bias, odd T.
+    # Several tiles and a ragged tail on every axis, a skewing bias, odd T;
+    # T=6000 has more token blocks (188) than SMs, so CTAs run several
+    # routing and permute tasks in one launch.
     w = inputs.moe_weights(256, 16, 4, 192, seed=seed)
     w.router_bias = inputs.zipf_bias(16, 1.2, seed)
     x = inputs.tokens(T, 256, seed + 50)
