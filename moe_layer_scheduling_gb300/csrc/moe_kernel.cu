@@ -666,6 +666,15 @@ __device__ void task_comb(const MegaParams& p, const Task& t, int wt) {
 }
 
 // TMEM epilogue of a GU or DN tile, then its notify.
+// act rows of the dense MLP (larger than L2, re-read only by the down
+// phase) are stored evict-first, so that they do not push x and the weight
+// slices in use out of L2; the MoE layer's act (re-read soon, from L2) is
+// stored normally.
+__device__ __forceinline__ void store_act(const MegaParams& p, uint4* dst, const uint4& v) {
+  if (p.dense) __stcs(dst, v);
+  else *dst = v;
+}
+
 __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, uint8_t* simt,
                                    const Task& t, uint32_t& gemm_i, const Clock& clk, int wt,
                                    uint32_t iter) {
@@ -712,8 +721,8 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
           const int idx = i128 + 128 * rep, r = idx >> 4, chunk = idx & 15, tok = cb * 16 + r;
           if (tok < t.rows) {
             const uint4 val = *reinterpret_cast<const uint4*>(S + r * 128 + chunk * 8);
-            *reinterpret_cast<uint4*>(p.ws.act + static_cast<size_t>(t.row0 + tok) * p.I +
-                                      t.b * kGuRowsW + chunk * 8) = val;
+            store_act(p, reinterpret_cast<uint4*>(p.ws.act + static_cast<size_t>(t.row0 + tok) * p.I +
+                                                  t.b * kGuRowsW + chunk * 8), val);
           }
         }
         named_bar(2 + h, 128);
@@ -740,8 +749,8 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
         const int tok = cb * 16 + (i128 >> 3), chunk = i128 & 7;
         if (tok < t.rows) {
           const uint4 val = *reinterpret_cast<const uint4*>(S + (i128 >> 3) * 64 + chunk * 8);
-          *reinterpret_cast<uint4*>(p.ws.act + static_cast<size_t>(t.row0 + tok) * p.I +
-                                    t.b * kGuRows + chunk * 8) = val;
+          store_act(p, reinterpret_cast<uint4*>(p.ws.act + static_cast<size_t>(t.row0 + tok) * p.I +
+                                                t.b * kGuRows + chunk * 8), val);
         }
         named_bar(2 + h, 128);
       }
@@ -774,9 +783,9 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
               uint2 pk;
               pk.x = *reinterpret_cast<const uint32_t*>(&lo);
               pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-              *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + o) = pk;
+              __stcs(reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + o), pk);
             } else {
-              *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = val;
+              __stcs(reinterpret_cast<float4*>(static_cast<float*>(p.out) + o), val);
             }
           } else if (r < t.rows) {
             const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
