@@ -1283,11 +1283,16 @@ __device__ __forceinline__ void resolve_chunk(const MegaParams& p, Task& t) {
   t.rows = __ldcg(B.chunk_rows + t.a);
 }
 
-// Dense MLP gate/up tile g of a call, taken weight-slice major: the tiles that
-// run side by side share one slice of w_gate_up (read from HBM once for all
-// chunks) and read all of x, which stays in L2.
+// Dense MLP gate/up tile g of a call: groups of kGc chunks, each group taken
+// weight-slice major.  The tiles that run side by side share a slice or two
+// of w_gate_up (read from HBM once per group) and read only the group's rows
+// of x (32 MB at H = 4096), which stay in L2; walking all of x at once
+// (67 MB at H = 4096) had x re-read from HBM for every slice.
 __device__ __forceinline__ Task dense_gu_task(const MegaParams& p, int g) {
-  Task t = make_task(TK_GU, 0, g % p.n_chunks, g / p.n_chunks);
+  constexpr int kGc = 32;  // chunks per group
+  const int per_group = kGc * p.NT_gu, grp = g / per_group, w = g - grp * per_group;
+  const int c0 = grp * kGc, gs = min(kGc, p.n_chunks - c0);
+  Task t = make_task(TK_GU, 0, c0 + w % gs, w / gs);
   resolve_chunk(p, t);
   return t;
 }
