@@ -41,7 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of ONE launch of the
-# headline kernel (dynamic megakernel, prefill T=4096), from one ncu capture.
+# benchmark line's kernel (static scheduler, prefill T=4096), from one ncu capture.
 # Valid only for the kernel sources it was taken on: reported as null once any
 # of them changes.
 MEGAKERNEL_SOURCES = ("moe_kernel.cu", "moe_api.cu", "etc_internal.h", "etc_event.cuh", "etc_ptx.cuh")
