@@ -18,7 +18,8 @@ constexpr int kWarpTma = 1;         // lane 0: TMA producer
 constexpr int kWarpMma = 2;         // lane 0: tcgen05 issuer; warp owns TMEM
 constexpr int kWorkerWarp0 = 4;     // warps 4..11: epilogue + SIMT tasks
 constexpr int kNumWorkers = 256;
-constexpr int kStagesMax = 6;       // smem operand stages (6 x 32 KB narrow, 4 x 48 KB wide)
+constexpr int kStagesMax = 9;       // smem operand stages (9 x 20 KB thin, 6 x 32 KB narrow, 4 x 48 KB wide)
+constexpr int kStagesNarrow = 6;
 constexpr int kRing = 8;            // smem task ring depth
 constexpr int kTB = 32;             // tokens per router/top-k/permute/combine task
 constexpr int kMaxPermParts = 4;    // permute tasks per token block when blocks are few
@@ -42,7 +43,11 @@ constexpr int kStageABytes = 2 * kOpABytes;   // 32 KB: up to 256 weight rows
 constexpr int kStageBBytes = kBT * kBK * 2;   // 16 KB: up to 128 token rows
 constexpr int kStageRegion = 192 * 1024;      // the operand stages' shared memory
 static_assert(kStageRegion >= 4 * (kStageABytes + kStageBBytes), "wide stages do not fit");
-static_assert(kStageRegion >= kStagesMax * (kOpABytes + kStageBBytes), "narrow stages do not fit");
+static_assert(kStageRegion >= kStagesNarrow * (kOpABytes + kStageBBytes), "narrow stages do not fit");
+// Thin calls (no chunk above 32 rows): 16 KB of weights + 32 token rows.
+constexpr int kStageThinBytes = kOpABytes + kTB * kBK * 2;
+static_assert(kStageRegion >= kStagesMax * kStageThinBytes, "thin stages do not fit");
+static_assert(kStageThinBytes % 1024 == 0, "thin stages must keep the 1 KB swizzle alignment");
 // The worker warps run one task at a time, so the SIMT tasks' scratch and the
 // GEMM epilogues' staging share one region.
 constexpr int kSimtBytes = 32 * 1024;
@@ -174,6 +179,7 @@ struct MegaParams {
   int fuse_scan; // one token block with H split: its top-k task runs the scan
   int NT_gu, NT_dn;
   int wide;      // expert tiles of 256 weight rows (two MMAs per K step)
+  int thin;      // narrow tiles whose chunks hold at most kTB rows: 20 KB stages
   unsigned epoch;
   int mode;  // 0 static, 1 dynamic, 2 mixed
   int dense;     // dense MLP: one weight set, chunks are 128-row slices of x, no routing

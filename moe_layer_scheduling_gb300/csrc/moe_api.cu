@@ -302,6 +302,9 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
               p->H % kDnRowsW == 0) ? 1 : 0;
   prm.NT_gu = p->I / (prm.wide ? kGuRowsW : kGuRows);
   prm.NT_dn = p->H / (prm.wide ? kDnRowsW : kDnRows);
+  // An expert holds at most one row per token: with T <= kTB no chunk is
+  // above kTB rows, and the thin stages hold a whole token operand.
+  prm.thin = (!prm.wide && a.T <= kTB) ? 1 : 0;
   if (++p->epoch == 0) p->epoch = 1;
   prm.epoch = p->epoch;
   prm.mode = mode;
@@ -409,6 +412,7 @@ int run_dense_call(etc_plan_t p, void* stream, const void* x, const void* wgu, c
   prm.wide = (T >= 64 && p->I % kGuRowsW == 0 && p->H % kDnRowsW == 0) ? 1 : 0;
   prm.NT_gu = p->I / (prm.wide ? kGuRowsW : kGuRows);
   prm.NT_dn = p->H / (prm.wide ? kDnRowsW : kDnRows);
+  prm.thin = (!prm.wide && T <= kTB) ? 1 : 0;  // chunks of at most kTB rows
   prm.dense = 1;
   prm.n_chunks = (T + kBT - 1) / kBT;
   prm.q_total = prm.n_chunks * (prm.NT_gu + prm.NT_dn);

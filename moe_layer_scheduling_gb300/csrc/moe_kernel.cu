@@ -118,15 +118,18 @@ __device__ __forceinline__ bool needs_comb(const MegaParams& p, int blk) {
 
 // Operand stages of a call: narrow tiles 6 x 32 KB (16 KB of weights, then up
 // to 16 KB of token rows), wide tiles 4 x 48 KB (32 KB of weights, then the
-// token rows).
+// token rows).  Calls whose chunks hold at most 32 rows (T <= 32) take 9 x
+// 20 KB: 16 KB of weights and at most 4 KB of token rows (or a router block),
+// so that half as many bytes again are in flight while weights stream.
 struct StageGeom {
   int n;          // stages
   uint32_t bytes; // stride
   uint32_t boff;  // token operand offset in a stage
 };
 __device__ __forceinline__ StageGeom stage_geom(const MegaParams& p) {
-  return p.wide ? StageGeom{4, kStageABytes + kStageBBytes, kStageABytes}
-                : StageGeom{kStagesMax, kOpABytes + kStageBBytes, kOpABytes};
+  return p.wide   ? StageGeom{4, kStageABytes + kStageBBytes, kStageABytes}
+         : p.thin ? StageGeom{kStagesMax, kStageThinBytes, kOpABytes}
+                  : StageGeom{kStagesNarrow, kOpABytes + kStageBBytes, kOpABytes};
 }
 
 // Eight consecutive values of block blk's input row `tok` (columns 8c..8c+7):
