@@ -67,8 +67,9 @@ extern "C" {
 typedef enum { ETC_SCHED_STATIC = 0, ETC_SCHED_DYNAMIC = 1, ETC_SCHED_MIXED = 2 } etc_sched_t;
 
 /* Debug bits for etc_moe_opts.debug_flags. */
-#define ETC_DEBUG_FAULT_EXTRA_WAIT 0x1u /* add 1 to expert debug_arg's wait_count: its
-                                           tiles never become ready, so a wait times out */
+#define ETC_DEBUG_FAULT_EXTRA_WAIT 0x1u /* add 1 to expert debug_arg's wait_count (dense MLP:
+                                           chunk debug_arg's gate/up target): its tiles never
+                                           become ready, so a wait times out */
 #define ETC_DEBUG_POISON 0x2u           /* fill intermediate buffers with NaN before each call */
 #define ETC_DEBUG_TRACE 0x4u            /* record every task's dispatch/start/end time and SM */
 
@@ -212,8 +213,9 @@ typedef struct {
   int t_max;         /* largest token count a call may pass: 1..65536 */
   int sched;         /* ETC_SCHED_STATIC or ETC_SCHED_DYNAMIC */
   unsigned long long wait_timeout_ns; /* device wait limit (0 -> 2 s) */
-  unsigned debug_flags;              /* ETC_DEBUG_POISON, ETC_DEBUG_TRACE */
+  unsigned debug_flags;              /* ETC_DEBUG_POISON, ETC_DEBUG_TRACE, ETC_DEBUG_FAULT_EXTRA_WAIT */
   int out_dtype;                     /* ETC_OUT_F32 (default) or ETC_OUT_BF16 */
+  int debug_arg;                     /* chunk (128-row slice) for ETC_DEBUG_FAULT_EXTRA_WAIT */
 } etc_mlp_opts;
 
 /*

@@ -58,7 +58,7 @@ class etc_mlp_opts(ctypes.Structure):
     _fields_ = [
         ("hidden", ctypes.c_int), ("inter", ctypes.c_int), ("t_max", ctypes.c_int),
         ("sched", ctypes.c_int), ("wait_timeout_ns", ctypes.c_ulonglong),
-        ("debug_flags", ctypes.c_uint), ("out_dtype", ctypes.c_int),
+        ("debug_flags", ctypes.c_uint), ("out_dtype", ctypes.c_int), ("debug_arg", ctypes.c_int),
     ]
 
 
@@ -182,8 +182,8 @@ def etc_moe_forward_unfused(plan: Plan, x, gate_w, w_gate_up, w_down, T, out, st
 
 
 def etc_mlp_plan(hidden, inter, t_max, sched=ETC_SCHED_STATIC, wait_timeout_ns=0, debug_flags=0,
-                 out_dtype=ETC_OUT_F32) -> Plan:
-    o = etc_mlp_opts(hidden, inter, t_max, sched, wait_timeout_ns, debug_flags, out_dtype)
+                 out_dtype=ETC_OUT_F32, debug_arg=0) -> Plan:
+    o = etc_mlp_opts(hidden, inter, t_max, sched, wait_timeout_ns, debug_flags, out_dtype, debug_arg)
     h = ctypes.c_void_p()
     _check(load().etc_mlp_plan(ctypes.byref(h), ctypes.byref(o)))
     return Plan(h.value, o)

@@ -421,6 +421,7 @@ int run_dense_call(etc_plan_t p, void* stream, const void* x, const void* wgu, c
   prm.mode = unfused ? ETC_SCHED_STATIC : p->opts.sched;
   prm.timeout_ns = p->opts.wait_timeout_ns ? p->opts.wait_timeout_ns : 2000000000ull;
   prm.debug_flags = static_cast<int>(p->opts.debug_flags);
+  prm.debug_arg = p->opts.debug_arg;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p->ws.trace) ETC_CUDA_TRY(cudaMemsetAsync(p->ws.trace, 0, 8, s));
   if (p->opts.debug_flags & ETC_DEBUG_POISON)
@@ -591,7 +592,8 @@ int etc_mlp_plan(etc_plan_t* out, const etc_mlp_opts* opts) {
   o.sched = opts->sched;
   o.n_blocks = 1;
   o.wait_timeout_ns = opts->wait_timeout_ns;
-  o.debug_flags = opts->debug_flags & (ETC_DEBUG_POISON | ETC_DEBUG_TRACE);
+  o.debug_flags = opts->debug_flags & (ETC_DEBUG_POISON | ETC_DEBUG_TRACE | ETC_DEBUG_FAULT_EXTRA_WAIT);
+  o.debug_arg = opts->debug_arg;
   o.out_dtype = opts->out_dtype;
   return make_plan(out, &o, true);
 }

@@ -116,6 +116,12 @@ __device__ __forceinline__ bool needs_comb(const MegaParams& p, int blk) {
   return !p.dense && (blk < p.n_blocks - 1 || p.out_bf16 != 0);
 }
 
+// Dense MLP: the finished gate/up tiles chunk c's down tiles wait for (one more for the
+// chunk a fault-injection call names, so that its wait runs out).
+__device__ __forceinline__ int dense_gu_target(const MegaParams& p, int c) {
+  return p.NT_gu + (((p.debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT) && c == p.debug_arg) ? 1 : 0);
+}
+
 // Operand stages of a call: narrow tiles 6 x 32 KB (16 KB of weights, then up
 // to 16 KB of token rows), wide tiles 4 x 48 KB (32 KB of weights, then the
 // token rows).  Calls whose chunks hold at most 32 rows (T <= 32) take 9 x
@@ -877,7 +883,7 @@ __device__ __forceinline__ int notify_primary(const MegaParams& p, const Task& t
           red_add_relaxed(&B.ev_act[t.a], 1);
           return 0;
         }
-        return atom_add_acq_rel(&B.ev_act[t.a], 1) + 1 == p.NT_gu;
+        return atom_add_acq_rel(&B.ev_act[t.a], 1) + 1 == dense_gu_target(p, t.a);
       }
       if (!tiles_queued(p)) {
         red_add_relaxed(&B.ev_act[t.a], -1);
@@ -1311,7 +1317,7 @@ __device__ bool sched_static_dense(const MegaParams& p, Ctrl* c, const Clock& cl
   if (p.stage_lo <= TK_DN && p.stage_hi >= TK_DN)
     for (int d = cta; d < p.n_chunks * p.NT_dn && ok; d += G) {
       Task t = make_task(TK_DN, 0, d / p.NT_dn, d % p.NT_dn);
-      ok = wait_geq(&B.ev_act[t.a], p.NT_gu, clk, TK_DN, t.a);
+      ok = wait_geq(&B.ev_act[t.a], dense_gu_target(p, t.a), clk, TK_DN, t.a);
       resolve_chunk(p, t);
       ok = ok && rw.emit(t, clk);
     }

@@ -60,3 +60,38 @@ def test_splitk_wait_times_out_and_recovers(oracle_lib):
     assert B.etc_splitk_check() == B.ETC_OK
     _, Cref = oracle_lib.splitk(A.numpy(), 4)
     assert np.linalg.norm(C.cpu().numpy() - Cref) <= 1e-5 * np.linalg.norm(Cref)
+
+
+@pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC], ids=["static", "dynamic"])
+def test_dense_mlp_wait_times_out_and_recovers(oracle_lib, sched):
+    """Dense MLP: chunk 1's down tiles wait for one gate/up tile more than it
+    has (static: their counter wait; dynamic: they are never pushed, so a
+    queue pop waits).  The bounded waits end the kernel, the status reports
+    the timeout, the plan refuses calls until reset, and the context still
+    computes a correct MLP."""
+    H, I, T = 256, 256, 300  # 3 chunks, the last one ragged
+    w = inputs.mlp_weights(H, I, seed=21)
+    x = inputs.tokens(T, H, seed=22)
+    xd, wgu, wd = x.cuda(), w.w_gate_up.cuda(), w.w_down.cuda()
+    plan = B.etc_mlp_plan(H, I, t_max=T, sched=sched, wait_timeout_ns=100_000_000,
+                          debug_flags=B.ETC_DEBUG_FAULT_EXTRA_WAIT, debug_arg=1)
+    out = torch.zeros(T, H, device="cuda")
+    B.etc_mlp_forward(plan, xd, wgu, wd, T, out)
+    torch.cuda.synchronize()  # the kernel ends: no hang
+    assert B.etc_plan_check(plan) == B.ETC_ERR_TIMEOUT
+    assert "timed out" in B.etc_last_error()
+    with pytest.raises(B.EtcError) as ei:  # sticky until reset
+        B.etc_mlp_forward(plan, xd, wgu, wd, T, out)
+    assert ei.value.code == B.ETC_ERR_STATE
+    B.etc_plan_reset(plan)
+    assert B.etc_plan_check(plan) == B.ETC_OK
+    plan.close()
+    good = B.etc_mlp_plan(H, I, t_max=T, sched=sched)
+    out = torch.full((T, H), float("nan"), device="cuda")
+    B.etc_mlp_forward(good, xd, wgu, wd, T, out)
+    torch.cuda.synchronize()
+    assert B.etc_plan_check(good) == B.ETC_OK
+    ref = oracle_lib.mlp(x, w.w_gate_up, w.w_down)
+    got = out.double().cpu().numpy()
+    assert np.max(np.abs(got - ref)) <= 2e-2 * np.sqrt(np.mean(ref * ref))
+    good.close()
