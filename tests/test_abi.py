@@ -139,3 +139,35 @@ def test_task_descriptor_fields_round_trip():
     for t, blk, a, b in [(6, 0, 383, 11), (7, 3, 131071, 255), (2, 1, 0, 31)]:
         d = enc(t, blk, a, b)
         assert (d >> 28, (d >> 25) & 7, (d >> 8) & 0x1FFFF, d & 0xFF) == (t, blk, a, b)
+
+
+def _header_struct_fields(name):
+    """(field, C type) pairs of `typedef struct { ... } name;` in the header, in order."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    m = re.search(r"typedef struct \{([^{}]*)\}\s*" + name + r"\s*;", src)
+    assert m, name
+    fields = []
+    for decl in m.group(1).split(";"):
+        decl = " ".join(decl.split())
+        if not decl:
+            continue
+        ctype, _, rest = decl.rpartition(" ")
+        for f in rest.split(","):
+            f = f.strip()
+            stars = len(f) - len(f.lstrip("*"))
+            fields.append((f.lstrip("*"), ctype + "*" * stars))
+    return fields
+
+
+@pytest.mark.parametrize("struct", ["etc_moe_opts", "etc_mlp_opts"])
+def test_binding_structs_match_the_header(struct):
+    import ctypes as C
+
+    from moe_layer_scheduling_gb300 import binding
+    ctype_of = {"int": C.c_int, "unsigned": C.c_uint, "float": C.c_float,
+                "unsigned long long": C.c_ulonglong, "const float*": C.c_void_p}
+    hdr = _header_struct_fields(struct)
+    py = getattr(binding, struct)._fields_
+    assert [f for f, _ in hdr] == [f for f, _ in py], struct
+    for (f, ct), (_, pt) in zip(hdr, py):
+        assert ctype_of[ct] is pt, (struct, f, ct, pt)
