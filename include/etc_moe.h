@@ -51,7 +51,7 @@ extern "C" {
 #define ETC_ERR_INVALID (-1)       /* bad shape, pointer, alignment or T */
 #define ETC_ERR_CUDA (-2)          /* a CUDA runtime call failed */
 #define ETC_ERR_TIMEOUT (-3)       /* a device wait gave up (see etc_plan_check) */
-#define ETC_ERR_UNIMPLEMENTED (-4) /* option not supported by this build */
+#define ETC_ERR_UNIMPLEMENTED (-4) /* option not supported by this library */
 #define ETC_ERR_STATE (-5)         /* plan needs etc_plan_reset after a timeout */
 
 /*
