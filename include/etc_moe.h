@@ -180,6 +180,13 @@ int etc_moe_debug_buffer(etc_plan_t plan, void* stream, int which, void* dst,
 int etc_moe_debug_trace(etc_plan_t plan, void* stream, void* dst, int max_records);
 
 /*
+ * A plan for a chain of n_blocks blocks (1..4) of the layer that opts
+ * describes: the same as etc_moe_plan with opts->n_blocks replaced by
+ * n_blocks (opts itself is not modified).  Same errors as etc_moe_plan.
+ */
+int etc_chain_plan(etc_plan_t* plan, const etc_moe_opts* opts, int n_blocks);
+
+/*
  * Chain of opts.n_blocks blocks  x <- x + MoE_b(RMSNorm_b(x))  in ONE launch.
  * Arguments are HOST arrays of n_blocks DEVICE pointers:
  *   norm_w[b] bf16 [H], gate_w[b] bf16 [H,E], router_bias[b] fp32 [E] (the

@@ -33,7 +33,7 @@ EXPORTED = [
     "etc_plan_check", "etc_plan_reset",
     "etc_plan_stats", "etc_plan_destroy", "etc_splitk_rowsum", "etc_splitk_rowsum_ex",
     "etc_splitk_check", "etc_splitk_rowsum_noalloc", "etc_launch_count", "etc_last_error",
-    "etc_mlp_plan", "etc_mlp_forward", "etc_mlp_forward_unfused",
+    "etc_mlp_plan", "etc_mlp_forward", "etc_mlp_forward_unfused", "etc_chain_plan",
 ]
 
 
@@ -88,6 +88,7 @@ def load(build_if_missing: bool = True):
     L.etc_moe_debug_trace.argtypes = [P, P, P, I]
     L.etc_chain_forward.argtypes = [P, P, P, P, P, P, P, P, I, P]
     L.etc_mlp_plan.argtypes = [ctypes.POINTER(P), ctypes.POINTER(etc_mlp_opts)]
+    L.etc_chain_plan.argtypes = [ctypes.POINTER(P), ctypes.POINTER(etc_moe_opts), I]
     L.etc_mlp_forward.argtypes = [P, P, P, P, P, I, P]
     L.etc_mlp_forward_unfused.argtypes = [P, P, P, P, P, I, P]
     L.etc_plan_check.argtypes = [P]
@@ -179,6 +180,17 @@ def etc_moe_forward_unfused(plan: Plan, x, gate_w, w_gate_up, w_down, T, out, st
     return _check(load().etc_moe_forward_unfused(plan.handle, _stream(stream), _ptr(x),
                                                  _ptr(gate_w), _ptr(w_gate_up), _ptr(w_down),
                                                  int(T), _ptr(out)))
+
+
+def etc_chain_plan(n_blocks, hidden, n_experts, top_k, inter, t_max, sched=ETC_SCHED_STATIC,
+                   rms_eps=1e-6, wait_timeout_ns=0, debug_flags=0, debug_arg=0,
+                   out_dtype=ETC_OUT_F32) -> Plan:
+    o = etc_moe_opts(hidden, n_experts, top_k, inter, t_max, sched, 1, rms_eps, None,
+                     wait_timeout_ns, debug_flags, debug_arg, out_dtype)
+    h = ctypes.c_void_p()
+    _check(load().etc_chain_plan(ctypes.byref(h), ctypes.byref(o), int(n_blocks)))
+    o.n_blocks = int(n_blocks)
+    return Plan(h.value, o)
 
 
 def etc_mlp_plan(hidden, inter, t_max, sched=ETC_SCHED_STATIC, wait_timeout_ns=0, debug_flags=0,

@@ -1,4 +1,5 @@
-// etc_common.cu -- error reporting, launch accounting, TMA descriptor encoding.
+// etc_common.cu -- error reporting, launch accounting, TMA descriptor encoding,
+// and the chain's plan entry point.
 #include <cstdio>
 #include <mutex>
 
@@ -77,3 +78,14 @@ const char* etc_last_error(void) { return etc::last_error(); }
 long long etc_launch_count(void) { return etc::g_launches.load(); }
 
 }  // extern "C"
+
+extern "C" int etc_chain_plan(etc_plan_t* plan, const etc_moe_opts* opts, int n_blocks) {
+  if (!opts) {
+    etc::clear_error();
+    if (plan) *plan = nullptr;
+    return etc::set_error(ETC_ERR_INVALID, "opts is NULL");
+  }
+  etc_moe_opts o = *opts;
+  o.n_blocks = n_blocks;
+  return etc_moe_plan(plan, &o);
+}

@@ -27,7 +27,8 @@ def test_header_declares_the_boundary():
     names = _declared()
     for required in ("etc_moe_plan", "etc_moe_forward", "etc_splitk_rowsum", "etc_chain_forward",
                      "etc_moe_forward_unfused", "etc_plan_destroy", "etc_last_error",
-                     "etc_mlp_plan", "etc_mlp_forward", "etc_mlp_forward_unfused"):
+                     "etc_mlp_plan", "etc_mlp_forward", "etc_mlp_forward_unfused",
+                     "etc_chain_plan"):
         assert required in names
 
 
@@ -88,6 +89,17 @@ def test_mlp_plan_rejects_bad_options_on_the_host(lib, bad):
     assert lib.etc_mlp_plan(ctypes.byref(h), ctypes.byref(o)) == binding.ETC_ERR_INVALID
     assert h.value is None
     assert lib.etc_last_error().decode() != ""
+
+
+@pytest.mark.parametrize("n_blocks", [0, 5, -1])
+def test_chain_plan_rejects_bad_block_counts_on_the_host(lib, n_blocks):
+    from moe_layer_scheduling_gb300 import binding
+    h = ctypes.c_void_p()
+    o = _opts()
+    assert lib.etc_chain_plan(ctypes.byref(h), ctypes.byref(o), n_blocks) == binding.ETC_ERR_INVALID
+    assert h.value is None
+    assert o.n_blocks == 1  # the caller's options are not modified
+    assert lib.etc_chain_plan(ctypes.byref(h), None, 2) == binding.ETC_ERR_INVALID
 
 
 def test_mlp_null_plan_is_rejected(lib):

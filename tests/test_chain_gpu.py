@@ -108,3 +108,13 @@ def test_chain_dynamic_t_sequence(oracle_lib, blocks, blocks_dev, sched):
             _check_chain(plan, blocks, x, out, oracle_lib)
     assert B.etc_plan_stats(plan)["launches"] - launches0 == len(seq)
     plan.close()
+
+
+def test_chain_plan_entry_point(oracle_lib, blocks, blocks_dev):
+    """etc_chain_plan(opts, n_blocks=2): a two-block chain in one launch."""
+    plan = B.etc_chain_plan(2, 2048, 128, 8, 768, t_max=64)
+    x = inputs.tokens(40, 2048, 7200)
+    bd = {k: v[:2] for k, v in blocks_dev.items()}
+    out = _run_chain(plan, bd, x)
+    _check_chain(plan, blocks[:2], x, out, oracle_lib)
+    plan.close()
