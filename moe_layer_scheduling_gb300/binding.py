@@ -312,8 +312,13 @@ def etc_moe_debug_trace(plan: Plan, max_records: int = 65536, stream=None):
     buf = torch.zeros(1 + 4 * max_records, dtype=torch.int64, device="cuda")
     _check(load().etc_moe_debug_trace(plan.handle, _stream(stream), _ptr(buf), int(max_records)))
     torch.cuda.synchronize()
-    v = buf.cpu().numpy().astype("uint64")
-    n = int(min(v[0], max_records))
+    return decode_trace(buf.cpu().numpy().astype("uint64"), max_records)
+
+
+def decode_trace(v, max_records: int) -> list[dict]:
+    """Records of a trace buffer (uint64 [1 + 4n]): v[0] = count, then per task the
+    word (type<<56 | block<<48 | sm<<32 | a<<8 | b), dispatch, start and end times."""
+    n = int(min(int(v[0]), max_records))
     recs = []
     for i in range(n):
         w0, t_disp, t0, t1 = (int(x) for x in v[1 + 4 * i: 5 + 4 * i])

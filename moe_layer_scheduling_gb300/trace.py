@@ -6,6 +6,7 @@ warps, and when the stage started and ended relative to the first task;
 also the time from the first to the last task and how busy the SMs were.
 
     python -m moe_layer_scheduling_gb300.trace --tokens 4096 --skew --sched dynamic
+    python -m moe_layer_scheduling_gb300.trace --mlp MLP-1 --sched static   # dense MLP
 """
 from __future__ import annotations
 
@@ -54,13 +55,32 @@ def main():
     ap.add_argument("--sched", default="dynamic", choices=["static", "dynamic", "mixed"])
     ap.add_argument("--repeat", type=int, default=3, help="calls before the traced one")
     ap.add_argument("--raw", default=None, help="also write the task records (JSON) to this file")
+    ap.add_argument("--mlp", default=None, help="trace the dense MLP of this Table 4 shape instead")
     args = ap.parse_args()
     dev = torch.device("cuda")
+    sched = {"static": B.ETC_SCHED_STATIC, "dynamic": B.ETC_SCHED_DYNAMIC,
+             "mixed": B.ETC_SCHED_MIXED}[args.sched]
+    if args.mlp:
+        if sched == B.ETC_SCHED_MIXED:
+            raise SystemExit("the dense MLP takes static or dynamic scheduling")
+        mw, mx = inputs.mlp_layer(args.mlp)
+        S, Hm = mx.shape
+        plan = B.etc_mlp_plan(Hm, mw.inter, S, sched=sched, debug_flags=B.ETC_DEBUG_TRACE)
+        xd, wgu, wd = mx.to(dev), mw.w_gate_up.to(dev), mw.w_down.to(dev)
+        out = torch.empty(S, Hm, device=dev)
+        for _ in range(args.repeat + 1):
+            B.etc_mlp_forward(plan, xd, wgu, wd, S, out)
+        name = f"dense_mlp_{args.mlp}_S{S}_H{Hm}_I{mw.inter}"
+    else:
+        plan, name = None, None
+    if plan is not None:
+        torch.cuda.synchronize()
+        assert B.etc_plan_check(plan) == B.ETC_OK, B.etc_last_error()
+        _report(B, plan, name, args)
+        return
     w = inputs.qwen_weights(0)
     wl = inputs.prefill_skew_layer(args.tokens, w) if args.skew else inputs.decode_layer(args.tokens, w)
     bias = wl.weights.router_bias.to(dev) if wl.weights.router_bias is not None else None
-    sched = {"static": B.ETC_SCHED_STATIC, "dynamic": B.ETC_SCHED_DYNAMIC,
-             "mixed": B.ETC_SCHED_MIXED}[args.sched]
     plan = B.etc_moe_plan(w.hidden, w.n_experts, w.top_k, w.inter, t_max=args.tokens, sched=sched,
                           router_bias=bias, debug_flags=B.ETC_DEBUG_TRACE)
     x = wl.x.to(dev)
@@ -70,12 +90,16 @@ def main():
         B.etc_moe_forward(plan, x, gw, wgu, wd, args.tokens, out)
     torch.cuda.synchronize()
     assert B.etc_plan_check(plan) == B.ETC_OK, B.etc_last_error()
+    _report(B, plan, wl.name, args)
+
+
+def _report(B, plan, name, args):
     recs = B.etc_moe_debug_trace(plan, max_records=200000)
     if args.raw:
         with open(args.raw, "w") as f:
             json.dump(recs, f)
     s = summarize(recs)
-    s["workload"] = wl.name
+    s["workload"] = name
     s["sched"] = args.sched
     print(json.dumps(s, indent=1))
     plan.close()
