@@ -81,12 +81,14 @@ __device__ __forceinline__ bool wait_flag(const unsigned* f, unsigned epoch, con
 // CTA's) writes and acquires those of earlier notifiers.
 __device__ __forceinline__ int notify(int* ev, int n) { return atom_add_acq_rel(ev, -n) - n; }
 
-// Bounded mbarrier wait used inside a CTA.
+// Bounded mbarrier wait used inside a CTA.  `cluster`: the barrier may be
+// completed from the pair peer CTA or by a pair MMA (cluster-scope acquire).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Clock& c,
-                                          int where) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                          int where, bool cluster = false) {
+  auto tw = [&] { return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (tw()) return true;
   uint32_t it = 0;
-  while (!mbar_try_wait(bar, parity)) {
+  while (!tw()) {
     if ((++it & 255u) == 0 && globaltimer_ns() > c.deadline + 1000000000ull) {
       raise_error(c, DERR_TIMEOUT_MBAR, where, 0);
       return false;

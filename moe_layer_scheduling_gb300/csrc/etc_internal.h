@@ -24,6 +24,7 @@ constexpr int kRing = 8;            // smem task ring depth
 constexpr int kTB = 32;             // tokens per router/top-k/permute/combine task
 constexpr int kMaxPermParts = 4;    // permute tasks per token block when blocks are few
 constexpr int kBT = 128;            // max rows (tokens) per expert chunk = max MMA N
+constexpr int kBT2 = 256;           // pair tiles: max rows per chunk (128 token rows per CTA)
 constexpr int kBK = 64;             // K elements per stage (one 128-byte swizzle row)
 // Expert tiles come in two widths.  Narrow (decode-sized calls): one M=128
 // MMA per K step.  Wide (calls with many rows per expert): two M=128 MMAs
@@ -179,6 +180,11 @@ struct MegaParams {
   int fuse_scan; // one token block with H split: its top-k task runs the scan
   int NT_gu, NT_dn;
   int wide;      // expert tiles of 256 weight rows (two MMAs per K step)
+  int pair;      // CTA-pair tiles (cta_group::2): 128 weight rows x up to 128 token rows per
+                 // CTA; every task belongs to a pair, whose two CTAs each take half of it
+  int cw;        // rows per expert chunk (kBT, or kBT2 with pair tiles)
+  int nbp;       // token blocks as tasks see them: nb, or ceil(nb / 2) pair blocks
+  int ev_mul;    // notifies per tile or routing task (2 with pair tiles: one per CTA)
   int thin;      // narrow tiles whose chunks hold at most kTB rows: 20 KB stages
   unsigned epoch;
   int mode;  // 0 static, 1 dynamic, 2 mixed

@@ -17,6 +17,7 @@
 
 namespace etc {
 int megakernel_occupancy();
+int megakernel_pair_clusters(int sms);
 }
 
 using namespace etc;
@@ -26,6 +27,7 @@ struct etc_plan_s {
   etc_moe_opts opts{};
   int H = 0, E = 0, k = 0, I = 0, T_max = 0, n_blocks = 1;
   int grid = 0;
+  int pair_grid = 0;          // CTAs of a launch in CTA pairs (0: cluster launches unavailable)
   int nb_max = 0, C_max = 0, R_max = 0;
   long long partial_max = 0;  // max NC * T_pad over T
   std::vector<void*> allocs;
@@ -295,16 +297,24 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   // One token block with H split: the top-k task runs the scan (not in the
   // per-stage ablation, which launches every stage on its own).
   prm.fuse_scan = (prm.nb == 1 && prm.NC > 1 && !unfused) ? 1 : 0;
-  prm.n_router = prm.nb * prm.NC;
   prm.T_pad = prm.nb * kTB;
   // Wide expert tiles once experts average 64 rows or more (and the shapes divide).
   prm.wide = (static_cast<long long>(a.T) * p->k >= 64LL * p->E && p->I % kGuRowsW == 0 &&
               p->H % kDnRowsW == 0) ? 1 : 0;
-  prm.NT_gu = p->I / (prm.wide ? kGuRowsW : kGuRows);
-  prm.NT_dn = p->H / (prm.wide ? kDnRowsW : kDnRows);
+  // The same calls run on CTA pairs (one cta_group::2 MMA over two SMs: 256
+  // weight rows x up to 256 chunk rows per tile) when clusters are available.
+  prm.pair = (prm.wide && a.n_blocks == 1 && !a.use_norm && router_tiles && p->pair_grid > 0 &&
+              !(p->opts.debug_flags & ETC_DEBUG_NO_PAIR)) ? 1 : 0;
+  if (prm.pair) prm.wide = 0;
+  prm.cw = prm.pair ? kBT2 : kBT;
+  prm.nbp = prm.pair ? (prm.nb + 1) / 2 : prm.nb;
+  prm.ev_mul = prm.pair ? 2 : 1;
+  prm.n_router = prm.nbp * prm.NC;
+  prm.NT_gu = p->I / (prm.wide || prm.pair ? kGuRowsW : kGuRows);
+  prm.NT_dn = p->H / (prm.wide || prm.pair ? kDnRowsW : kDnRows);
   // An expert holds at most one row per token: with T <= kTB no chunk is
   // above kTB rows, and the thin stages hold a whole token operand.
-  prm.thin = (!prm.wide && a.T <= kTB) ? 1 : 0;
+  prm.thin = (!prm.wide && !prm.pair && a.T <= kTB) ? 1 : 0;
   if (++p->epoch == 0) p->epoch = 1;
   prm.epoch = p->epoch;
   prm.mode = mode;
@@ -321,10 +331,11 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
     if (p->ws.acc)
       ETC_CUDA_TRY(cudaMemsetAsync(p->ws.acc, 0xFF, static_cast<size_t>(p->T_max) * p->H * 4, s));
   }
+  const int grid = prm.pair ? p->pair_grid : p->grid;
   if (!unfused) {
     prm.stage_lo = stage_lo;
     prm.stage_hi = stage_hi;
-    ETC_CUDA_TRY(launch_megakernel(prm, p->grid, s));
+    ETC_CUDA_TRY(launch_megakernel(prm, grid, s));
     ++p->launches;
     g_launches.fetch_add(1);
   } else {
@@ -332,7 +343,7 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
       if (stg == TK_TOPK && prm.NC == 1) continue;  // top-k ran inside the router stage
       if (stg == TK_COMB && !prm.out_bf16 && a.n_blocks == 1) continue;  // nothing to finalise
       prm.stage_lo = prm.stage_hi = stg;
-      ETC_CUDA_TRY(launch_megakernel(prm, p->grid, s));
+      ETC_CUDA_TRY(launch_megakernel(prm, grid, s));
       ++p->launches;
       g_launches.fetch_add(1);
     }
@@ -410,11 +421,16 @@ int run_dense_call(etc_plan_t p, void* stream, const void* x, const void* wgu, c
   prm.PP = 1;
   prm.T_pad = prm.nb * kTB;
   prm.wide = (T >= 64 && p->I % kGuRowsW == 0 && p->H % kDnRowsW == 0) ? 1 : 0;
-  prm.NT_gu = p->I / (prm.wide ? kGuRowsW : kGuRows);
-  prm.NT_dn = p->H / (prm.wide ? kDnRowsW : kDnRows);
-  prm.thin = (!prm.wide && T <= kTB) ? 1 : 0;  // chunks of at most kTB rows
+  prm.pair = (prm.wide && p->pair_grid > 0 && !(p->opts.debug_flags & ETC_DEBUG_NO_PAIR)) ? 1 : 0;
+  if (prm.pair) prm.wide = 0;
+  prm.cw = prm.pair ? kBT2 : kBT;
+  prm.nbp = prm.nb;
+  prm.ev_mul = prm.pair ? 2 : 1;
+  prm.NT_gu = p->I / (prm.wide || prm.pair ? kGuRowsW : kGuRows);
+  prm.NT_dn = p->H / (prm.wide || prm.pair ? kDnRowsW : kDnRows);
+  prm.thin = (!prm.wide && !prm.pair && T <= kTB) ? 1 : 0;  // chunks of at most kTB rows
   prm.dense = 1;
-  prm.n_chunks = (T + kBT - 1) / kBT;
+  prm.n_chunks = (T + prm.cw - 1) / prm.cw;
   prm.q_total = prm.n_chunks * (prm.NT_gu + prm.NT_dn);
   if (++p->epoch == 0) p->epoch = 1;
   prm.epoch = p->epoch;
@@ -431,7 +447,7 @@ int run_dense_call(etc_plan_t p, void* stream, const void* x, const void* wgu, c
   for (int i = 0; i < (unfused ? 2 : 1); ++i) {
     prm.stage_lo = unfused ? stage[i] : TK_GU;
     prm.stage_hi = unfused ? stage[i] : TK_DN;
-    ETC_CUDA_TRY(launch_megakernel(prm, p->grid, s));
+    ETC_CUDA_TRY(launch_megakernel(prm, prm.pair ? p->pair_grid : p->grid, s));
     ++p->launches;
     g_launches.fetch_add(1);
   }
@@ -464,6 +480,7 @@ int make_plan(etc_plan_t* out, const etc_moe_opts* opts, bool dense) {
   if (occ < 1) return fail(set_error(ETC_ERR_CUDA, "megakernel does not fit on an SM"));
   p->grid = sm_count(p->device);  // one CTA per SM: TMEM and smem sized for that
   if (p->grid <= 0) return fail(set_error(ETC_ERR_CUDA, "cannot query SM count"));
+  p->pair_grid = 2 * std::min(megakernel_pair_clusters(p->grid), p->grid / 2);
 
   p->nb_max = (p->T_max + kTB - 1) / kTB;
   p->R_max = p->T_max * p->k;
@@ -592,7 +609,8 @@ int etc_mlp_plan(etc_plan_t* out, const etc_mlp_opts* opts) {
   o.sched = opts->sched;
   o.n_blocks = 1;
   o.wait_timeout_ns = opts->wait_timeout_ns;
-  o.debug_flags = opts->debug_flags & (ETC_DEBUG_POISON | ETC_DEBUG_TRACE | ETC_DEBUG_FAULT_EXTRA_WAIT);
+  o.debug_flags = opts->debug_flags & (ETC_DEBUG_POISON | ETC_DEBUG_TRACE | ETC_DEBUG_FAULT_EXTRA_WAIT |
+                                      ETC_DEBUG_NO_PAIR);
   o.debug_arg = opts->debug_arg;
   o.out_dtype = opts->out_dtype;
   return make_plan(out, &o, true);

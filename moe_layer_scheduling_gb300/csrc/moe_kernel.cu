@@ -60,6 +60,7 @@ struct Task {
 };
 
 constexpr int kNoti = 8;  // finished tasks waiting for the notifier warp
+constexpr int kMbox = 4;  // pair tiles, dynamic queue: tasks the even CTA forwards to its peer
 constexpr int kPermSlots = 6;                         // token rows in flight in a permute task
 constexpr int kPermRowOff = 8 * 1024;                 // row slots' offset in the worker scratch
 constexpr int kPermBytes = kSimtBytes - kPermRowOff;  // row slots' bytes
@@ -77,6 +78,9 @@ struct Ctrl {
   Task ring[kRing];
   Task wtask[2];     // workers' broadcast of the current task (double-buffered)
   Task noti[kNoti];  // workers -> notifier
+  Task mbox[kMbox];  // pair peer's scheduler -> this CTA's scheduler (dynamic queue)
+  uint64_t mb_full[kMbox];
+  uint64_t mb_empty[kMbox];
   uint32_t tmem_base;
   int wflag[2];      // workers' broadcast flags
   int started;       // tasks the workers have taken from the ring
@@ -104,6 +108,26 @@ __device__ __forceinline__ QueueView queue_of(const MegaParams& p) {
 }
 
 __device__ __forceinline__ bool dynamic_mode(const MegaParams& p) { return p.mode == ETC_SCHED_DYNAMIC; }
+
+// CTA pairs.  With pair tiles every task belongs to a pair of CTAs (a cluster
+// of two): an expert or router tile is one cta_group::2 MMA over both CTAs'
+// operands, and a SIMT task on pair token block a is split into the 32-token
+// blocks 2a (even CTA) and 2a + 1 (odd CTA).
+__device__ __forceinline__ int pair_rank(const MegaParams& p) {
+  return p.pair ? static_cast<int>(cluster_ctarank()) : 0;
+}
+// This CTA's token block of a routing task on (pair) block a.
+__device__ __forceinline__ int my_tb(const MegaParams& p, int a) { return p.pair ? 2 * a + pair_rank(p) : a; }
+// Scheduling unit of this CTA (its own index, or its pair's) and the number of units.
+__device__ __forceinline__ int sched_unit(const MegaParams& p) {
+  return p.pair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+}
+__device__ __forceinline__ int sched_units(const MegaParams& p) {
+  return p.pair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+}
+// Token rows a pair expert tile's MMA covers: the chunk rounded to 32, i.e.
+// a multiple of 16 rows from each CTA.
+__device__ __forceinline__ int pair_npad(int rows) { return (rows + 31) & ~31; }
 // Whether the expert tiles and the finaliser go through the queue (DYNAMIC and
 // MIXED); the routing tasks do only in DYNAMIC.
 __device__ __forceinline__ bool tiles_queued(const MegaParams& p) { return p.mode != ETC_SCHED_STATIC; }
@@ -119,7 +143,7 @@ __device__ __forceinline__ bool needs_comb(const MegaParams& p, int blk) {
 // Dense MLP: the finished gate/up tiles chunk c's down tiles wait for (one more for the
 // chunk a fault-injection call names, so that its wait runs out).
 __device__ __forceinline__ int dense_gu_target(const MegaParams& p, int c) {
-  return p.NT_gu + (((p.debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT) && c == p.debug_arg) ? 1 : 0);
+  return p.ev_mul * p.NT_gu + (((p.debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT) && c == p.debug_arg) ? 1 : 0);
 }
 
 // Operand stages of a call: narrow tiles 6 x 32 KB (16 KB of weights, then up
@@ -133,7 +157,10 @@ struct StageGeom {
   uint32_t boff;  // token operand offset in a stage
 };
 __device__ __forceinline__ StageGeom stage_geom(const MegaParams& p) {
-  return p.wide   ? StageGeom{4, kStageABytes + kStageBBytes, kStageABytes}
+  // Pair tiles: 6 x 32 KB per CTA, 16 KB of weights (its 128 of the pair's
+  // 256 weight rows) and up to 16 KB of token rows (its half of the chunk).
+  return p.pair   ? StageGeom{kStagesNarrow, kOpABytes + kStageBBytes, kOpABytes}
+         : p.wide ? StageGeom{4, kStageABytes + kStageBBytes, kStageABytes}
          : p.thin ? StageGeom{kStagesMax, kStageThinBytes, kOpABytes}
                   : StageGeom{kStagesNarrow, kOpABytes + kStageBBytes, kOpABytes};
 }
@@ -320,29 +347,44 @@ __device__ __forceinline__ void publish_block_counts(const MegaParams& p, const 
   }
 }
 
+// The workers are done with accumulator buffer `acc`: the MMA issuer may
+// reuse it.  Pair tiles: the issuer sits in the even CTA and waits for both
+// CTAs' workers.
+// (PAIR, here and below, is the kernel instantiation's compile-time copy of
+// p.pair: the single-CTA kernel holds no pair-only instruction at all.)
+template <bool PAIR>
+__device__ __forceinline__ void release_acc(Ctrl* c, int acc) {
+  if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(&c->tempty[acc], 0));
+  else mbar_arrive(&c->tempty[acc]);
+}
+
 // Epilogue of a router tile of token block tb (TMEM lane = expert, column =
-// token; each worker warp reads its 32 lanes x 16 columns).
+// token; each worker warp reads its 32 lanes x 16 columns).  Pair tiles: the
+// MMA covered 64 tokens, columns 32r..32r+31 being CTA r's block 2a + r.
+template <bool PAIR>
 __device__ void task_router_epilogue(const MegaParams& p, Ctrl* c, uint8_t* simt, const Task& t,
                                      uint32_t& gemm_i, const Clock& clk, int wt, uint32_t iter) {
   const int acc = gemm_i & 1;
   const uint32_t aph = (gemm_i >> 1) & 1;
   ++gemm_i;
+  const int tb = my_tb(p, t.a);
   // While the tile is still on the tensor cores: the block's combine rows.
-  if (t.b == 0) init_acc_rows(p, t.blk, t.a, wt);
+  if (t.b == 0) init_acc_rows(p, t.blk, tb, wt);
   int* flag = &c->wflag[iter & 1];
-  if (wt == 0) *flag = mbar_wait(&c->tfull[acc], aph, clk, 231) ? 1 : 0;
+  if (wt == 0) *flag = mbar_wait(&c->tfull[acc], aph, clk, 231, PAIR) ? 1 : 0;
   named_bar(1, kNumWorkers);
   const bool ok = *flag != 0;
   tc_fence_after();
   const BlockWs& B = p.ws.blk[t.blk];
   const int w = warp_id(), q = w & 3, h = (w - kWorkerWarp0) >> 2, lane = lane_id();
-  const int E = p.E, tb = t.a, e = 32 * q + lane, ww = wt >> 5;
+  const int E = p.E, e = 32 * q + lane, ww = wt >> 5;
+  const uint32_t col0 = p.pair ? 32u * pair_rank(p) : 0u;
   int* s_cnt = reinterpret_cast<int*>(simt);             // [E]
   float* s_log = reinterpret_cast<float*>(simt + 1024);  // [kTB][E]
   for (int i = wt; i < E; i += kNumWorkers) s_cnt[i] = 0;
   if (ok) {
     float v[16];
-    tmem_ld16(c->tmem_base + acc * kAccCols + (static_cast<uint32_t>(32 * q) << 16) + h * 16, v);
+    tmem_ld16(c->tmem_base + acc * kAccCols + (static_cast<uint32_t>(32 * q) << 16) + col0 + h * 16, v);
     if (e < E) {
       if (p.NC == 1) {
         const float b = p.bias[t.blk] ? __ldg(p.bias[t.blk] + e) : 0.f;
@@ -365,8 +407,8 @@ __device__ void task_router_epilogue(const MegaParams& p, Ctrl* c, uint8_t* simt
   }
   tc_fence_before();
   named_bar(1, kNumWorkers);
-  if (wt == 0) mbar_arrive(&c->tempty[acc]);  // accumulator free for the next tile
-  if (ok && p.NC == 1) {
+  if (wt == 0) release_acc<PAIR>(c, acc);  // accumulator free for the next tile
+  if (ok && p.NC == 1 && tb < p.nb) {
     const int tok0 = tb * kTB;
     for (int idx = wt; idx < kTB * E; idx += kNumWorkers) {
       const int r = idx / E;
@@ -382,7 +424,7 @@ __device__ void task_router_epilogue(const MegaParams& p, Ctrl* c, uint8_t* simt
 // Top-k of token block tb as a SIMT task: from the NC summed partials (H
 // split), or from logits the caller gave (routing-only calls).
 __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
-  const int blk = t.blk, tb = t.a;
+  const int blk = t.blk, tb = my_tb(p, t.a);
   const BlockWs& B = p.ws.blk[blk];
   const int E = p.E, ww = wt >> 5, lane = wt & 31;
   int* s_cnt = reinterpret_cast<int*>(simt);             // [E]
@@ -412,7 +454,7 @@ __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int
   named_bar(1, kNumWorkers);
   topk_rows(p, B, s_log, tok0, s_cnt, ww, lane);
   named_bar(1, kNumWorkers);
-  publish_block_counts(p, B, tb, s_cnt, wt, !p.fuse_scan);
+  if (tb < p.nb) publish_block_counts(p, B, tb, s_cnt, wt, !p.fuse_scan);
   if (p.fuse_scan) {
     // One token block: its histogram (in shared memory) is the call's counts,
     // so the scan runs here, one hop sooner (no separate scan task, no
@@ -429,7 +471,7 @@ __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int
 __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
                            const int* s_counts) {
   const BlockWs& B = p.ws.blk[blk];
-  const int E = p.E, nb = p.nb;
+  const int E = p.E;
   int cnt = 0;
   if (wt < E) {
     if (s_counts) {
@@ -441,7 +483,8 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
   }
   named_bar(1, kNumWorkers);  // the counts are read before the scan scratch is reused
   int* tmp = reinterpret_cast<int*>(simt);  // scan scratch [32]
-  const int nch = (cnt + kBT - 1) / kBT;
+  const int cw = p.cw;
+  const int nch = (cnt + cw - 1) / cw;
   const int row0 = workers_excl_scan(cnt, tmp, wt);
   const int ch0 = workers_excl_scan(nch, tmp + 16, wt);
   if (wt < E) {
@@ -458,18 +501,22 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
     for (int c = 0; c < nch; ++c) {
       const int chn = ch0 + c;
       B.chunk_expert[chn] = wt;
-      B.chunk_row0[chn] = row0 + c * kBT;
-      B.chunk_rows[chn] = min(kBT, cnt - c * kBT);
-      B.ev_act[chn] = p.NT_gu;
-      B.ev_down[chn] = p.NT_dn;
+      B.chunk_row0[chn] = row0 + c * cw;
+      B.chunk_rows[chn] = min(cw, cnt - c * cw);
+      // one notify per tile, or per CTA of a pair tile
+      B.ev_act[chn] = p.ev_mul * p.NT_gu;
+      B.ev_down[chn] = p.ev_mul * p.NT_dn;
     }
     // Data-dependent event update: expert e waits for its counts[e] rows.
     const int extra = ((p.debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT) && wt == p.debug_arg) ? 1 : 0;
     B.ev_expert[wt] = cnt + extra;
   }
-  if (needs_comb(p, blk))
-    for (int tb = wt; tb < nb; tb += kNumWorkers)
-      B.ev_tok[tb] = p.k * (min(p.T, tb * kTB + kTB) - tb * kTB);
+  if (needs_comb(p, blk)) {
+    // token rows the finaliser of (pair) token block tb waits for
+    const int tbw = p.pair ? 2 * kTB : kTB;
+    for (int tb = wt; tb < p.nbp; tb += kNumWorkers)
+      B.ev_tok[tb] = p.k * (min(p.T, tb * tbw + tbw) - tb * tbw);
+  }
   __threadfence();
   named_bar(1, kNumWorkers);
   if (wt == 0) {
@@ -479,10 +526,11 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
       // Tasks of the block that pass through the queue: all of them in
       // DYNAMIC, the expert tiles and the finaliser in MIXED.
       const int n_chunks = B.meta[0];
-      const int routing = dyn ? (p.use_norm ? nb : 0) + p.n_router + (p.NC > 1 ? nb : 0) +
-                                    (p.fuse_scan ? 0 : 1) + nb * p.PP
+      const int nbp = p.nbp;
+      const int routing = dyn ? (p.use_norm ? nbp : 0) + p.n_router + (p.NC > 1 ? nbp : 0) +
+                                    (p.fuse_scan ? 0 : 1) + nbp * p.PP
                               : 0;
-      const int blk_tasks = routing + n_chunks * (p.NT_gu + p.NT_dn) + (needs_comb(p, blk) ? nb : 0);
+      const int blk_tasks = routing + n_chunks * (p.NT_gu + p.NT_dn) + (needs_comb(p, blk) ? nbp : 0);
       const int acc = (blk == 0 ? 0 : *p.ws.qacc) + blk_tasks;
       *p.ws.qacc = acc;
       if (blk == p.n_blocks - 1) *p.ws.qtotal = acc;
@@ -496,7 +544,7 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
     if (tiles_queued(p) && blk == p.n_blocks - 1) st_release(p.ws.qtotal_flag, p.epoch);
     if (dyn) {
       const QueueView q = queue_of(p);
-      tmp[0] = q.n_seed + atom_add_relaxed(q.tail, nb * p.PP);  // the block's permute tasks
+      tmp[0] = q.n_seed + atom_add_relaxed(q.tail, p.nbp * p.PP);  // the block's permute tasks
     }
   }
   if (dynamic_mode(p)) {
@@ -505,7 +553,7 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
     const int base = tmp[0];
     const QueueView q = queue_of(p);
     __threadfence();  // the plan above is published with the slots
-    for (int i = wt; i < nb * p.PP; i += kNumWorkers) {
+    for (int i = wt; i < p.nbp * p.PP; i += kNumWorkers) {
       if (base + i >= q.cap) {
         const Clock c0{~0ull, p.ws.status, p.ws.status_host};
         raise_error(c0, DERR_QUEUE_OVERFLOW, 3, base + i);
@@ -559,7 +607,7 @@ __device__ void init_acc_rows(const MegaParams& p, int blk, int tb, int wt) {
 // expert-sorted rows.
 __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* simt, int wt,
                           uint32_t& li, const Clock& clk) {
-  const int blk = t.blk, tb = t.a, part = t.b;
+  const int blk = t.blk, tb = my_tb(p, t.a), part = t.b;
   const BlockWs& B = p.ws.blk[blk];
   const int E = p.E, k = p.k, ww = wt >> 5, lane = wt & 31;
   int* s_run = reinterpret_cast<int*>(simt);
@@ -568,7 +616,7 @@ __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* 
   int* s_part = s_ids + kTB * kMaxK;  // [kNumWorkers]
   int* s_pcnt = s_part + kNumWorkers; // [E]
   uint8_t* rows = simt + kPermRowOff;
-  const int t0 = tb * kTB, ntok = min(kTB, p.T - t0);
+  const int t0 = tb * kTB, ntok = max(0, min(kTB, p.T - t0));  // (odd CTA of the last pair block: none)
   const int TP = kTB / p.PP, r_lo = min(ntok, part * TP), r_hi = min(ntok, r_lo + TP);
   const int nmine = r_hi - r_lo;
   const __nv_bfloat16* src = p.use_norm ? p.ws.xn : p.x;
@@ -626,7 +674,8 @@ __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* 
     B.row_token[row] = t0 + i / k;
     B.row_w[row] = __ldcg(B.wts + t0 * k + i);
   }
-  for (int e = wt; e < E; e += kNumWorkers) B.part_cnt[(tb * p.PP + part) * E + e] = s_pcnt[e];
+  if (tb < p.nb)
+    for (int e = wt; e < E; e += kNumWorkers) B.part_cnt[(tb * p.PP + part) * E + e] = s_pcnt[e];
   if (wt == 0) {
     for (int r = 0; r < nmine; ++r) {
       const uint32_t L = li + r;
@@ -654,7 +703,7 @@ __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* 
 // weighted expert rows: rounds the rows to bf16 when the output is bf16, and
 // in the chain releases the next block's RMSNorm of tb.
 __device__ void task_comb(const MegaParams& p, const Task& t, int wt) {
-  const int blk = t.blk, tb = t.a;
+  const int blk = t.blk, tb = my_tb(p, t.a);
   const BlockWs& B = p.ws.blk[blk];
   const int ww = wt >> 5, lane = wt & 31, n8 = p.H / 8;
   if (blk == p.n_blocks - 1 && p.out_bf16) {
@@ -684,6 +733,7 @@ __device__ __forceinline__ void store_act(const MegaParams& p, uint4* dst, const
   else *dst = v;
 }
 
+template <bool PAIR>
 __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, uint8_t* simt,
                                    const Task& t, uint32_t& gemm_i, const Clock& clk, int wt,
                                    uint32_t iter) {
@@ -691,7 +741,7 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
   const uint32_t aph = (gemm_i >> 1) & 1;
   ++gemm_i;
   int* flag = &c->wflag[iter & 1];
-  if (wt == 0) *flag = mbar_wait(&c->tfull[acc], aph, clk, 230) ? 1 : 0;
+  if (wt == 0) *flag = mbar_wait(&c->tfull[acc], aph, clk, 230, PAIR) ? 1 : 0;
   named_bar(1, kNumWorkers);
   const bool ok = *flag != 0;
   tc_fence_after();
@@ -703,8 +753,11 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
   const int ncb = (t.rows + 15) >> 4;
   const BlockWs& B = p.ws.blk[t.blk];
   // Down tiles: each chunk row's token and routing weight, for the combine.
-  int* s_rtok = reinterpret_cast<int*>(simt + 2 * kEpiHalfBytes);                 // [128]
-  float* s_rw = reinterpret_cast<float*>(simt + 2 * kEpiHalfBytes + 4 * kBT);     // [128]
+  int* s_rtok = reinterpret_cast<int*>(simt + 2 * kEpiHalfBytes);                 // [256]
+  float* s_rw = reinterpret_cast<float*>(simt + 2 * kEpiHalfBytes + 4 * kBT2);    // [256]
+  // Pair tiles: this CTA's 64 intermediate columns (gate/up) or 128 output
+  // columns (down) of the pair's tile; the accumulator holds all chunk rows.
+  const int rank = pair_rank(p);
   if (t.type == TK_DN && !p.dense) {
     for (int r = wt; r < t.rows; r += kNumWorkers) {
       s_rtok[r] = __ldcg(B.row_token + t.row0 + r);
@@ -758,8 +811,9 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
         const int tok = cb * 16 + (i128 >> 3), chunk = i128 & 7;
         if (tok < t.rows) {
           const uint4 val = *reinterpret_cast<const uint4*>(S + (i128 >> 3) * 64 + chunk * 8);
+          const int gcol = p.pair ? t.b * 2 * kGuRows + kGuRows * rank : t.b * kGuRows;
           store_act(p, reinterpret_cast<uint4*>(p.ws.act + static_cast<size_t>(t.row0 + tok) * p.I +
-                                                t.b * kGuRows + chunk * 8), val);
+                                                gcol + chunk * 8), val);
         }
         named_bar(2 + h, 128);
       }
@@ -772,7 +826,8 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
       for (int hc = 0; hc < nhalf * ncb; ++hc) {
         const int half = hc / ncb, cb = hc - half * ncb;
         if ((cb & 1) != h) continue;  // the two worker halves take alternate column blocks
-        const int col0 = t.b * (p.wide ? kDnRowsW : kDnRows) + half * 128;
+        const int col0 = p.pair ? t.b * kDnRowsW + kDnRows * rank
+                                : t.b * (p.wide ? kDnRowsW : kDnRows) + half * 128;
         float* accr = p.dense ? nullptr : acc_rows(p, t.blk) + col0;
         float v[16];
         tmem_ld16(tbase + half * (kAccCols / 2) + cb * 16, v);
@@ -810,7 +865,7 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
   fence_proxy_async_global();  // act is read next by TMA
   tc_fence_before();
   named_bar(1, kNumWorkers);  // notify: ev_act / ev_down (by the notifier warp)
-  if (wt == 0) mbar_arrive(&c->tempty[acc]);
+  if (wt == 0) release_acc<PAIR>(c, acc);
 }
 
 // ---------------------------------------------------------------------------
@@ -861,14 +916,14 @@ __device__ __forceinline__ int notify_primary(const MegaParams& p, const Task& t
           red_add_relaxed(B.ev_route, 1);
           return 0;
         }
-        return atom_add_acq_rel(B.ev_route, 1) + 1 == p.nb;
+        return atom_add_acq_rel(B.ev_route, 1) + 1 == p.ev_mul * p.nbp;
       }
       // partial logits of block tb landed ("ij->i" on ev_rblk)
       if (!dyn) {
         red_add_relaxed(&B.ev_rblk[t.a], 1);
         return 0;
       }
-      return atom_add_acq_rel(&B.ev_rblk[t.a], 1) + 1 == p.NC;
+      return atom_add_acq_rel(&B.ev_rblk[t.a], 1) + 1 == p.ev_mul * p.NC;
     case TK_TOPK:
       st_relaxed(&B.ev_rblk[t.a], 0);  // consumed: re-armed for the next call
       if (p.fuse_scan) return 0;       // the task ran the scan itself
@@ -876,7 +931,7 @@ __device__ __forceinline__ int notify_primary(const MegaParams& p, const Task& t
         red_add_relaxed(B.ev_route, 1);
         return 0;
       }
-      return atom_add_acq_rel(B.ev_route, 1) + 1 == p.nb;
+      return atom_add_acq_rel(B.ev_route, 1) + 1 == p.ev_mul * p.nbp;
     case TK_GU:
       if (p.dense) {  // count-up chunk counters (no scan to arm them)
         if (!tiles_queued(p)) {
@@ -891,7 +946,7 @@ __device__ __forceinline__ int notify_primary(const MegaParams& p, const Task& t
       }
       return notify(&B.ev_act[t.a], 1) == 0;
     case TK_DN:  // both modes need to know which tile finished the chunk
-      if (p.dense) return atom_add_acq_rel(&B.ev_down[t.a], 1) + 1 == p.NT_dn;
+      if (p.dense) return atom_add_acq_rel(&B.ev_down[t.a], 1) + 1 == p.ev_mul * p.NT_dn;
       return notify(&B.ev_down[t.a], 1) == 0;
     case TK_COMB:
       if (p.use_norm) st_relaxed(reinterpret_cast<int*>(&B.comb_flag[t.a]), static_cast<int>(p.epoch));
@@ -929,11 +984,13 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
       // expert order (the order the static walk takes them, so that tiles of
       // one expert run side by side and share its weights in L2).
       constexpr int kEL = kMaxE / 32;
+      const int tb = my_tb(p, t.a);
+      if (tb >= p.nb) break;  // the odd CTA's half of the last pair block holds no tokens
       int n[kEL], tiles[kEL], c0[kEL];
 #pragma unroll
       for (int i = 0; i < kEL; ++i) {
         const int e = kEL * lane + i;
-        n[i] = e < p.E ? __ldcg(B.part_cnt + (t.a * p.PP + t.b) * p.E + e) : 0;
+        n[i] = e < p.E ? __ldcg(B.part_cnt + (tb * p.PP + t.b) * p.E + e) : 0;
       }
       int mine = 0;
 #pragma unroll
@@ -1005,8 +1062,9 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
             queue_push(q, 1, [&](int) { return task_enc(TK_COMB, t.blk, run_tb, 0); }, clk);
           }
         };
+        const int tbw = p.pair ? 2 * kTB : kTB;  // rows of a (pair) token block
         for (int r = r0; r < r1; ++r) {
-          const int tb = __ldcg(B.row_token + t.row0 + r) / kTB;
+          const int tb = __ldcg(B.row_token + t.row0 + r) / tbw;
           if (tb != run_tb) {
             flush_run();
             run_tb = tb;
@@ -1069,6 +1127,7 @@ __device__ void run_notifier(const MegaParams& p, Ctrl* c, const Clock& clk) {
   }
 }
 
+template <bool PAIR>
 __device__ void run_workers(const MegaParams& p, Ctrl* c, uint8_t* simt, uint8_t* epi,
                             const Clock& clk) {
   const int wt = threadIdx.x - kWorkerWarp0 * 32;
@@ -1092,13 +1151,15 @@ __device__ void run_workers(const MegaParams& p, Ctrl* c, uint8_t* simt, uint8_t
       case TK_NORM: task_norm(p, t, wt); break;
       case TK_ROUTER:
         if (p.logits_in) task_topk(p, t, simt, wt);
-        else task_router_epilogue(p, c, simt, t, gemm_i, clk, wt, ri);
+        else task_router_epilogue<PAIR>(p, c, simt, t, gemm_i, clk, wt, ri);
         break;
       case TK_TOPK: task_topk(p, t, simt, wt); break;
-      case TK_SCAN: task_scan(p, t, simt, wt); break;
+      case TK_SCAN:  // pair tiles: the even CTA of the pair runs it
+        if (pair_rank(p) == 0) task_scan(p, t, simt, wt);
+        break;
       case TK_PERM: task_perm(p, c, t, simt, wt, perm_li, clk); break;
       case TK_GU:
-      case TK_DN: task_gemm_epilogue(p, c, epi, simt, t, gemm_i, clk, wt, ri); break;
+      case TK_DN: task_gemm_epilogue<PAIR>(p, c, epi, simt, t, gemm_i, clk, wt, ri); break;
       case TK_COMB: task_comb(p, t, wt); break;
       default: break;
     }
@@ -1134,10 +1195,22 @@ __device__ __forceinline__ bool ring_take(Ctrl* c, uint32_t& ri, Task& t, const 
   return ok;
 }
 
+template <bool PAIR>
 __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock& clk) {
   uint32_t ri = 0, ph = 0;  // stage slot and its phase, advanced without division
   int st = 0;
   const StageGeom g = stage_geom(p);
+  // Pair tiles: each CTA loads its half of the operands into its own stages;
+  // every copy completes on the even CTA's `full` barrier, where the pair MMA
+  // waits, and the even CTA's producer announces both CTAs' bytes.
+  constexpr bool pair = PAIR;
+  const int rank = pair_rank(p);
+  const bool announce = !pair || rank == 0;
+  const uint32_t tx_mul = pair ? 2u : 1u;
+  auto load = [&](void* dst, const CUtensorMap* m, int s, int x, int y) {
+    if constexpr (PAIR) tma_load_2d_pair(dst, m, mapa_shared(&c->full[s], 0), x, y);
+    else tma_load_2d(dst, m, &c->full[s], x, y);
+  };
   for (;;) {
     Task t;
     if (!ring_take(c, ri, t, clk, 220) || t.type == TK_TERM) break;
@@ -1145,19 +1218,21 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
       // Router tile: per 64-row K block of H, the router weight's rows for
       // experts 0-63 and 64-127 (two MN-major boxes; experts >= E read as
       // zero) and the block's 32 input rows (the lo part second in the chain).
+      // Pair tiles: both CTAs load the router weight, each its own 32 rows.
       const int KB = p.KBr * (p.use_norm ? 2 : 1);
       const uint32_t bytes = kOpABytes + kTB * kBK * 2;  // two 64-expert boxes + 32 token rows
+      const int tok0 = my_tb(p, t.a) * kTB;
       fence_proxy_async_global();
       for (int kb = 0; kb < KB; ++kb, st = st + 1 == g.n ? (ph ^= 1, 0) : st + 1) {
         const int s = st;
-        if (!mbar_wait(&c->empty[s], ph ^ 1, clk, 222)) return;
+        if (!mbar_wait(&c->empty[s], ph ^ 1, clk, 222, pair)) return;
         uint8_t* sa = base + s * g.bytes;
         const int part = kb >= p.KBr ? 1 : 0;
         const int h = t.b * p.HC + (kb - part * p.KBr) * kBK;
-        mbar_arrive_expect_tx(&c->full[s], bytes);
-        tma_load_2d(sa, &p.tm_wg[t.blk], &c->full[s], 0, h);
-        tma_load_2d(sa + kOpABytes / 2, &p.tm_wg[t.blk], &c->full[s], 64, h);
-        tma_load_2d(sa + g.boff, part ? &p.tm_xrlo : &p.tm_xr, &c->full[s], h, t.a * kTB);
+        if (announce) mbar_arrive_expect_tx(&c->full[s], bytes * tx_mul);
+        load(sa, &p.tm_wg[t.blk], s, 0, h);
+        load(sa + kOpABytes / 2, &p.tm_wg[t.blk], s, 64, h);
+        load(sa + g.boff, part ? &p.tm_xrlo : &p.tm_xr, s, h, tok0);
       }
       continue;
     }
@@ -1167,67 +1242,89 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
     const CUtensorMap* tb = gu ? &p.tm_xperm : &p.tm_act;
     const CUtensorMap* tb64 = gu ? &p.tm_xperm64 : &p.tm_act64;
     const int KB = (gu ? p.H : p.I) / kBK;
-    const int nb16 = (t.rows + 15) >> 4;
+    // Token rows of this CTA: the whole chunk, or its half of a pair tile
+    // (the MMA takes rows [0, npad/2) from the even CTA, the rest from the odd).
+    const int half = pair ? pair_npad(t.rows) / 2 : 0;
+    const int brow0 = pair ? t.row0 + rank * half : t.row0;
+    const int nb16 = pair ? half >> 4 : (t.rows + 15) >> 4;
     const int n64 = nb16 >> 2, r16 = nb16 & 3;  // token rows as 64-row boxes, then 16-row boxes
     // Weight rows as 64-row boxes, 8 KB apart.  Narrow gate/up: 64 gate + 64
     // up rows (one M=128 operand); wide: 128 gate rows, then 128 up rows (two
-    // operands); down tiles: consecutive output rows of w_down.
+    // operands); pair: 64 gate + 64 up rows of this CTA's half of the 128
+    // intermediate columns; down tiles: consecutive output rows of w_down.
     const bool wide = p.wide != 0;
     const int nA = wide ? 4 : 2;
     int rowA[4];
     if (gu) {
-      const int g0 = t.e * 2 * p.I + t.b * (wide ? kGuRowsW : kGuRows);
+      const int g0 = t.e * 2 * p.I + (pair ? t.b * 2 * kGuRows + kGuRows * rank : t.b * (wide ? kGuRowsW : kGuRows));
       rowA[0] = g0;
       rowA[1] = wide ? g0 + 64 : g0 + p.I;
       rowA[2] = g0 + p.I;
       rowA[3] = g0 + p.I + 64;
     } else {
-      const int r0 = t.e * p.H + t.b * (wide ? kDnRowsW : kDnRows);
+      const int r0 = t.e * p.H + (pair ? t.b * kDnRowsW + kDnRows * rank : t.b * (wide ? kDnRowsW : kDnRows));
       for (int i = 0; i < 4; ++i) rowA[i] = r0 + 64 * i;
     }
     const uint32_t bytes = nA * (kOpABytes / 2) + nb16 * 16 * kBK * 2;
     fence_proxy_async_global();
     for (int kb = 0; kb < KB; ++kb, st = st + 1 == g.n ? (ph ^= 1, 0) : st + 1) {
       const int s = st;
-      if (!mbar_wait(&c->empty[s], ph ^ 1, clk, 221)) return;
+      if (!mbar_wait(&c->empty[s], ph ^ 1, clk, 221, pair)) return;
       uint8_t* sa = base + s * g.bytes;
       uint8_t* sb = sa + g.boff;
-      mbar_arrive_expect_tx(&c->full[s], bytes);
-      for (int i = 0; i < nA; ++i) tma_load_2d(sa + i * (kOpABytes / 2), ta, &c->full[s], kb * kBK, rowA[i]);
-      for (int i = 0; i < n64; ++i)
-        tma_load_2d(sb + i * 64 * kBK * 2, tb64, &c->full[s], kb * kBK, t.row0 + 64 * i);
+      if (announce) mbar_arrive_expect_tx(&c->full[s], bytes * tx_mul);
+      for (int i = 0; i < nA; ++i) load(sa + i * (kOpABytes / 2), ta, s, kb * kBK, rowA[i]);
+      for (int i = 0; i < n64; ++i) load(sb + i * 64 * kBK * 2, tb64, s, kb * kBK, brow0 + 64 * i);
       for (int i = 0; i < r16; ++i)
-        tma_load_2d(sb + (n64 * 64 + i * 16) * kBK * 2, tb, &c->full[s], kb * kBK,
-                    t.row0 + n64 * 64 + 16 * i);
+        load(sb + (n64 * 64 + i * 16) * kBK * 2, tb, s, kb * kBK, brow0 + n64 * 64 + 16 * i);
     }
   }
 }
 
+// PAIR (a compile-time copy of p.pair): a kernel uses tcgen05 with one CTA
+// group only, so the pair and single-CTA issuers are separate instantiations.
+template <bool PAIR>
 __device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock& clk) {
   uint32_t ri = 0, tc = 0, ph = 0;  // stage slot and its phase, advanced without division
   int st = 0;
   const StageGeom g = stage_geom(p);
   const uint32_t tmem = c->tmem_base;
+  // Pair tiles: the even CTA's issuer runs every MMA of the pair; the odd
+  // CTA's only keeps its place in the task ring.
+  constexpr bool pair = PAIR;
+  const bool issuer = !pair || pair_rank(p) == 0;
   for (;;) {
     Task t;
     if (!ring_take(c, ri, t, clk, 240) || t.type == TK_TERM) break;
     const bool rt = t.type == TK_ROUTER && !p.logits_in;
-    if (!rt && t.type != TK_GU && t.type != TK_DN) continue;
+    if (!issuer || (!rt && t.type != TK_GU && t.type != TK_DN)) continue;
     const int acc = tc & 1;
-    if (!mbar_wait(&c->tempty[acc], ((tc >> 1) & 1) ^ 1, clk, 241)) return;
+    if (!mbar_wait(&c->tempty[acc], ((tc >> 1) & 1) ^ 1, clk, 241, pair)) return;
     tc_fence_after();
     const uint32_t d = tmem + acc * kAccCols;
-    const int npad = rt ? kTB : (t.rows + 15) & ~15;
+    // N = token columns: the 32-token router block (64 over a pair), the
+    // chunk rounded to 16 (a pair's chunk rounded to 32).
+    const int npad = rt ? (pair ? 2 * kTB : kTB) : pair ? pair_npad(t.rows) : (t.rows + 15) & ~15;
+    const int M = pair ? 256 : 128;
     // Router tiles read A (the router weight) MN-major; expert tiles K-major.
-    const uint32_t idesc = rt ? idesc_bf16_f32_amn(128, npad) : idesc_bf16_f32(128, npad);
+    const uint32_t idesc = rt ? idesc_bf16_f32_amn(M, npad) : idesc_bf16_f32(M, npad);
     const int KB = rt ? p.KBr * (p.use_norm ? 2 : 1) : (t.type == TK_GU ? p.H : p.I) / kBK;
     for (int kb = 0; kb < KB; ++kb, st = st + 1 == g.n ? (ph ^= 1, 0) : st + 1) {
       const int s = st;
-      if (!mbar_wait(&c->full[s], ph, clk, 242)) return;
+      if (!mbar_wait(&c->full[s], ph, clk, 242, pair)) return;
       tc_fence_after();
       const uint32_t sa = smem_u32(base + s * g.bytes);
       const uint64_t bd = desc_kmajor_sw128(sa + g.boff);
-      if (rt) {
+      if constexpr (PAIR) {
+        // 128 weight rows from each CTA, npad/2 token rows from each.
+        const uint64_t ad = rt ? desc_mnmajor_sw128(sa, kOpABytes / 2) : desc_kmajor_sw128(sa);
+        const uint64_t astep = rt ? (2048 >> 4) : 2;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          umma_bf16_pair(d, ad + astep * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+        umma_commit_pair(&c->empty[s]);  // both CTAs' stages free once these MMAs have read them
+        continue;
+      } else if (rt) {
         // 16 K rows per MMA: 2 KB further into each 64-expert box.
         const uint64_t ad = desc_mnmajor_sw128(sa, kOpABytes / 2);
 #pragma unroll
@@ -1245,9 +1342,10 @@ __device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock
             umma_bf16(d + kAccCols / 2, ad1 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
         }
       }
-      umma_commit(&c->empty[s]);  // stage free once these MMAs have read it
+      if constexpr (!PAIR) umma_commit(&c->empty[s]);  // stage free once these MMAs have read it
     }
-    umma_commit(&c->tfull[acc]);  // accumulator ready
+    if constexpr (PAIR) umma_commit_pair(&c->tfull[acc]);  // accumulator ready in both CTAs
+    else umma_commit(&c->tfull[acc]);                      // accumulator ready
     ++tc;
   }
 }
@@ -1280,10 +1378,10 @@ __device__ __forceinline__ Task make_task(int type, int blk, int a, int b) {
 }
 
 __device__ __forceinline__ void resolve_chunk(const MegaParams& p, Task& t) {
-  if (p.dense) {  // chunk a = rows [128a, min(128a + 128, T)) of x
+  if (p.dense) {  // chunk a = rows [cw*a, min(cw*a + cw, T)) of x
     t.e = 0;
-    t.row0 = t.a * kBT;
-    t.rows = min(kBT, p.T - t.row0);
+    t.row0 = t.a * p.cw;
+    t.rows = min(p.cw, p.T - t.row0);
     return;
   }
   const BlockWs& B = p.ws.blk[t.blk];
@@ -1298,7 +1396,7 @@ __device__ __forceinline__ void resolve_chunk(const MegaParams& p, Task& t) {
 // of x (32 MB at H = 4096), which stay in L2; walking all of x at once
 // (67 MB at H = 4096) had x re-read from HBM for every slice.
 __device__ __forceinline__ Task dense_gu_task(const MegaParams& p, int g) {
-  constexpr int kGc = 32;  // chunks per group
+  const int kGc = p.pair ? 16 : 32;  // chunks per group (4096 rows of x)
   const int per_group = kGc * p.NT_gu, grp = g / per_group, w = g - grp * per_group;
   const int c0 = grp * kGc, gs = min(kGc, p.n_chunks - c0);
   Task t = make_task(TK_GU, 0, c0 + w % gs, w / gs);
@@ -1309,7 +1407,7 @@ __device__ __forceinline__ Task dense_gu_task(const MegaParams& p, int g) {
 // Static walk of the dense MLP: gate/up tiles (no input event), then the down
 // tiles chunk by chunk, each after its chunk's gate/up tiles (count-up event).
 __device__ bool sched_static_dense(const MegaParams& p, Ctrl* c, const Clock& clk, RingWriter& rw) {
-  const int G = gridDim.x, cta = blockIdx.x;
+  const int G = sched_units(p), cta = sched_unit(p);
   const BlockWs& B = p.ws.blk[0];
   bool ok = true;
   if (p.stage_lo <= TK_GU && p.stage_hi >= TK_GU)
@@ -1329,7 +1427,8 @@ __device__ bool sched_static_dense(const MegaParams& p, Ctrl* c, const Clock& cl
 // after a failed wait.
 __device__ bool sched_static(const MegaParams& p, Ctrl* c, const Clock& clk, RingWriter& rw,
                              bool routing_only) {
-  const int G = gridDim.x, cta = blockIdx.x;
+  // Pair tiles: both CTAs of a pair walk the same list of pair tasks.
+  const int G = sched_units(p), cta = sched_unit(p);
   auto in = [&](int stage) { return stage >= p.stage_lo && stage <= p.stage_hi; };
   bool ok = true;
   for (int blk = 0; blk < p.n_blocks && ok; ++blk) {
@@ -1348,13 +1447,13 @@ __device__ bool sched_static(const MegaParams& p, Ctrl* c, const Clock& clk, Rin
       }
     }
     if (in(TK_TOPK) && p.NC > 1) {
-      for (int tb = cta; tb < p.nb && ok; tb += G) {
-        ok = wait_geq(&B.ev_rblk[tb], p.NC, clk, TK_TOPK, tb);
+      for (int tb = cta; tb < p.nbp && ok; tb += G) {
+        ok = wait_geq(&B.ev_rblk[tb], p.ev_mul * p.NC, clk, TK_TOPK, tb);
         ok = ok && rw.emit(make_task(TK_TOPK, blk, tb, 0), clk);
       }
     }
     if (in(TK_SCAN) && !p.fuse_scan && cta == blk % G && ok) {
-      ok = wait_geq(B.ev_route, p.nb, clk, TK_SCAN, 0);
+      ok = wait_geq(B.ev_route, p.ev_mul * p.nbp, clk, TK_SCAN, 0);
       ok = ok && rw.emit(make_task(TK_SCAN, blk, 0, 0), clk);
     }
     if (p.stage_hi < TK_PERM || !ok) continue;
@@ -1362,7 +1461,7 @@ __device__ bool sched_static(const MegaParams& p, Ctrl* c, const Clock& clk, Rin
     if (!ok) break;
     const int n_chunks = ld_acquire(&B.meta[0]);
     if (in(TK_PERM))
-      for (int i = cta; i < p.nb * p.PP && ok; i += G)
+      for (int i = cta; i < p.nbp * p.PP && ok; i += G)
         ok = rw.emit(make_task(TK_PERM, blk, i / p.PP, i % p.PP), clk);
     if (routing_only) continue;
     if (in(TK_GU)) {
@@ -1384,7 +1483,7 @@ __device__ bool sched_static(const MegaParams& p, Ctrl* c, const Clock& clk, Rin
       }
     }
     if (in(TK_COMB) && needs_comb(p, blk)) {
-      for (int tb = cta; tb < p.nb && ok; tb += G) {
+      for (int tb = cta; tb < p.nbp && ok; tb += G) {
         ok = wait_zero(&B.ev_tok[tb], clk, TK_COMB, tb);
         ok = ok && rw.emit(make_task(TK_COMB, blk, tb, 0), clk);
       }
@@ -1393,11 +1492,52 @@ __device__ bool sched_static(const MegaParams& p, Ctrl* c, const Clock& clk, Rin
   return ok;
 }
 
+// Pair tiles, dynamic queue: the even CTA pops each task and forwards it to
+// the odd CTA's mailbox (shared memory written across the pair, completed on
+// the peer's mbarrier); the odd CTA's scheduler hands the forwarded tasks to
+// its own roles in the same order.
+__device__ bool forward_task(Ctrl* c, uint32_t& fi, const Task& t, const Clock& clk) {
+  const int s = fi % kMbox;
+  if (!mbar_wait(&c->mb_empty[s], ((fi / kMbox) & 1) ^ 1, clk, 205, true)) return false;
+  const uint32_t dst = mapa_shared(&c->mbox[s], 1);
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(&t);
+#pragma unroll
+  for (int i = 0; i < static_cast<int>(sizeof(Task) / 4); ++i) st_cluster_u32(dst + 4 * i, src[i]);
+  mbar_arrive_cluster(mapa_shared(&c->mb_full[s], 1));  // release: the task is visible first
+  ++fi;
+  return true;
+}
+
+__device__ void relay_pair_tasks(Ctrl* c, const Clock& clk, RingWriter& rw) {
+  for (uint32_t i = 0;; ++i) {
+    const int s = i % kMbox;
+    if (!mbar_wait(&c->mb_full[s], (i / kMbox) & 1, clk, 206, true)) break;
+    const Task t = c->mbox[s];
+    mbar_arrive_cluster(mapa_shared(&c->mb_empty[s], 0));
+    if (t.type == TK_TERM || !rw.emit(t, clk)) break;
+  }
+}
+
 // Queue pops until every task of the call that passes through the queue has
 // been popped (the last scan publishes their number).
+template <bool PAIR>
 __device__ void sched_dynamic(const MegaParams& p, Ctrl* c, const Clock& clk, RingWriter& rw) {
+  if constexpr (PAIR) {
+    if (pair_rank(p) != 0) {
+      relay_pair_tasks(c, clk, rw);
+      return;
+    }
+  }
   const QueueView q = queue_of(p);
   constexpr int kLookahead = 2;  // tasks popped but not yet started by the workers
+  uint32_t fi = 0;
+  // Hands a task to this CTA's roles (and, with pair tiles, to the peer's).
+  auto emit = [&](const Task& t) {
+    if constexpr (PAIR) {
+      if (!forward_task(c, fi, t, clk)) return false;
+    }
+    return rw.emit(t, clk);
+  };
   for (;;) {
     // Pop only when this CTA is about to need work: a CTA that grabbed many
     // ready tasks would leave other SMs idle.
@@ -1409,7 +1549,7 @@ __device__ void sched_dynamic(const MegaParams& p, Ctrl* c, const Clock& clk, Ri
     uint32_t desc = 0;
     bool have = false;
     if (idx < q.n_seed && p.dense) {
-      if (!rw.emit(dense_gu_task(p, idx), clk)) break;
+      if (!emit(dense_gu_task(p, idx))) break;
       continue;
     }
     if (p.dense && idx >= p.q_total) break;  // every task of the call has been popped
@@ -1441,13 +1581,16 @@ __device__ void sched_dynamic(const MegaParams& p, Ctrl* c, const Clock& clk, Ri
     if (!have) break;  // every task of the call has been popped
     Task t = make_task(task_type(desc), task_blk(desc), task_a(desc), task_b(desc));
     if (t.type == TK_GU || t.type == TK_DN) resolve_chunk(p, t);
-    if (!rw.emit(t, clk)) break;
+    if (!emit(t)) break;
   }
+  if constexpr (PAIR) forward_task(c, fi, make_task(TK_TERM, 0, 0, 0), clk);
 }
 
 // ---------------------------------------------------------------------------
 // Kernel
 // ---------------------------------------------------------------------------
+// PAIR = 1: launched as clusters of two CTAs with pair tiles (p.pair == 1).
+template <int PAIR>
 __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_constant__ MegaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1465,7 +1608,11 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&c->tfull[a], 1);
-      mbar_init(&c->tempty[a], 1);
+      mbar_init(&c->tempty[a], PAIR ? 2 : 1);  // pair: the workers of both CTAs release it
+    }
+    for (int s = 0; s < kMbox; ++s) {
+      mbar_init(&c->mb_full[s], 1);
+      mbar_init(&c->mb_empty[s], 1);
     }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&c->rfull[r], 1);
@@ -1494,11 +1641,17 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
     tma_prefetch_desc(&p.tm_act64);
   }
   if (w == kWarpMma) {
-    tmem_alloc(&c->tmem_base, kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {  // the same columns in both CTAs of the pair
+      tmem_alloc_pair(&c->tmem_base, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&c->tmem_base, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // the peer's barriers are initialised before any use
   tc_fence_after();
 
   if (w == kWarpSched) {
@@ -1514,57 +1667,89 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
       if (p.dense && p.mode != ETC_SCHED_DYNAMIC) {
         sched_static_dense(p, c, clk, rw);
       } else if (p.mode == ETC_SCHED_DYNAMIC) {
-        sched_dynamic(p, c, clk, rw);
+        sched_dynamic<PAIR != 0>(p, c, clk, rw);
       } else if (p.mode == ETC_SCHED_MIXED) {
-        if (sched_static(p, c, clk, rw, true)) sched_dynamic(p, c, clk, rw);
+        if (sched_static(p, c, clk, rw, true)) sched_dynamic<PAIR != 0>(p, c, clk, rw);
       } else {
         sched_static(p, c, clk, rw, false);
       }
       rw.emit(make_task(TK_TERM, 0, 0, 0), clk);
     }
   } else if (w == kWarpTma) {
-    if (lane_id() == 0) run_producer(p, c, base, clk);
+    if (lane_id() == 0) run_producer<PAIR != 0>(p, c, base, clk);
   } else if (w == kWarpMma) {
-    if (lane_id() == 0) run_mma(p, c, base, clk);
+    if (lane_id() == 0) run_mma<PAIR != 0>(p, c, base, clk);
   } else if (w == kWarpNotifier) {
     run_notifier(p, c, clk);
   } else if (w >= kWorkerWarp0) {
-    run_workers(p, c, simt, epi, clk);
+    run_workers<PAIR != 0>(p, c, simt, epi, clk);
   }
 
   tc_fence_before();
   __syncthreads();
+  // Pair: neither CTA leaves while the peer may still signal its barriers,
+  // read its operands or write its accumulators.
+  if constexpr (PAIR) cluster_sync_all();
   if (w == kWarpMma) {
     tc_fence_after();
-    tmem_dealloc(c->tmem_base, kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(c->tmem_base, kTmemCols);
+    else tmem_dealloc(c->tmem_base, kTmemCols);
   }
 }
 
 cudaError_t megakernel_configure() {
-  return cudaFuncSetAttribute(etc_moe_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(etc_moe_megakernel<0>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(etc_moe_megakernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemBytes);
 }
 
-cudaError_t launch_megakernel(const MegaParams& p, int grid, cudaStream_t stream) {
+static cudaLaunchConfig_t launch_config(int grid, bool pair, cudaStream_t stream,
+                                        cudaLaunchAttribute (&attr)[2]) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: spin-waits are safe
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, etc_moe_megakernel, p);
+  cfg.numAttrs = pair ? 2 : 1;
+  return cfg;
+}
+
+cudaError_t launch_megakernel(const MegaParams& p, int grid, cudaStream_t stream) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = launch_config(grid, p.pair != 0, stream, attr);
+  if (p.pair) return cudaLaunchKernelEx(&cfg, etc_moe_megakernel<1>, p);
+  return cudaLaunchKernelEx(&cfg, etc_moe_megakernel<0>, p);
 }
 
 int megakernel_occupancy() {
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, etc_moe_megakernel, kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, etc_moe_megakernel<0>, kThreads,
                                                     kSmemBytes) != cudaSuccess)
     return 0;
   return occ;
+}
+
+// CTA pairs that can be resident at once (0 if cluster launches are unavailable).
+int megakernel_pair_clusters(int sms) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = launch_config(2 * (sms / 2), true, nullptr, attr);
+  cfg.attrs = &attr[1];  // the cluster shape alone
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, etc_moe_megakernel<1>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 }  // namespace etc

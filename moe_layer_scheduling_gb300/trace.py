@@ -56,7 +56,9 @@ def main():
     ap.add_argument("--repeat", type=int, default=3, help="calls before the traced one")
     ap.add_argument("--raw", default=None, help="also write the task records (JSON) to this file")
     ap.add_argument("--mlp", default=None, help="trace the dense MLP of this Table 4 shape instead")
+    ap.add_argument("--no-pair", action="store_true", help="wide tiles on single CTAs, not CTA pairs")
     args = ap.parse_args()
+    extra = B.ETC_DEBUG_NO_PAIR if args.no_pair else 0
     dev = torch.device("cuda")
     sched = {"static": B.ETC_SCHED_STATIC, "dynamic": B.ETC_SCHED_DYNAMIC,
              "mixed": B.ETC_SCHED_MIXED}[args.sched]
@@ -65,7 +67,7 @@ def main():
             raise SystemExit("the dense MLP takes static or dynamic scheduling")
         mw, mx = inputs.mlp_layer(args.mlp)
         S, Hm = mx.shape
-        plan = B.etc_mlp_plan(Hm, mw.inter, S, sched=sched, debug_flags=B.ETC_DEBUG_TRACE)
+        plan = B.etc_mlp_plan(Hm, mw.inter, S, sched=sched, debug_flags=B.ETC_DEBUG_TRACE | extra)
         xd, wgu, wd = mx.to(dev), mw.w_gate_up.to(dev), mw.w_down.to(dev)
         out = torch.empty(S, Hm, device=dev)
         for _ in range(args.repeat + 1):
@@ -82,7 +84,7 @@ def main():
     wl = inputs.prefill_skew_layer(args.tokens, w) if args.skew else inputs.decode_layer(args.tokens, w)
     bias = wl.weights.router_bias.to(dev) if wl.weights.router_bias is not None else None
     plan = B.etc_moe_plan(w.hidden, w.n_experts, w.top_k, w.inter, t_max=args.tokens, sched=sched,
-                          router_bias=bias, debug_flags=B.ETC_DEBUG_TRACE)
+                          router_bias=bias, debug_flags=B.ETC_DEBUG_TRACE | extra)
     x = wl.x.to(dev)
     gw, wgu, wd = w.gate_w.to(dev), w.w_gate_up.to(dev), w.w_down.to(dev)
     out = torch.empty(args.tokens, w.hidden, device=dev)

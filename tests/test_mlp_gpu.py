@@ -54,6 +54,18 @@ def test_mlp_parity(oracle_lib, sched, unfused, H, I, T):
     plan.close()
 
 
+@pytest.mark.parametrize("sched,unfused", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("H,I,T", [(512, 1024, 300), (512, 1024, 64)])
+def test_mlp_parity_single_cta_wide_tiles(oracle_lib, sched, unfused, H, I, T):
+    # Wide calls with CTA pairs disabled (256-weight-row tiles on one SM).
+    w = inputs.mlp_weights(H, I, seed=H + I)
+    x = inputs.tokens(T, H, seed=T)
+    plan = B.etc_mlp_plan(H, I, t_max=T, sched=sched, debug_flags=B.ETC_DEBUG_NO_PAIR)
+    out = _run(plan, x.cuda(), w.w_gate_up.cuda(), w.w_down.cuda(), T, unfused)
+    _close(out, oracle_lib.mlp(x, w.w_gate_up, w.w_down))
+    plan.close()
+
+
 @pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC], ids=["static", "dynamic"])
 def test_mlp_bf16_output_and_determinism(oracle_lib, sched):
     H, I, T = 512, 768, 257

@@ -25,8 +25,8 @@ def qwen_dev(qwen):
     return to_dev(qwen)
 
 
-def _full_check(oracle_lib, w, x, sched, unfused, dw=None, t_max=None):
-    out, routing, plan = run_layer(w, x, sched, unfused, dw=dw, t_max=t_max)
+def _full_check(oracle_lib, w, x, sched, unfused, dw=None, t_max=None, debug_flags=0):
+    out, routing, plan = run_layer(w, x, sched, unfused, dw=dw, t_max=t_max, debug_flags=debug_flags)
     ref, ref_logits, ref_ids, ref_w = oracle_lib.moe_layer(x, w.gate_w, w.w_gate_up, w.w_down,
                                                            w.top_k, bias=w.router_bias,
                                                            want_routing=True)
@@ -95,6 +95,15 @@ def test_wide_tiles(oracle_lib, sched, unfused, T, seed):
     w.router_bias = inputs.zipf_bias(16, 1.2, seed)
     x = inputs.tokens(T, 512, seed + 50)
     _full_check(oracle_lib, w, x, sched, unfused)
+
+
+@pytest.mark.parametrize("sched,unfused", MODES, ids=MODE_IDS)
+def test_wide_tiles_single_cta(oracle_lib, sched, unfused):
+    # The same wide calls with CTA pairs disabled: 256-weight-row tiles on one SM.
+    w = inputs.moe_weights(512, 16, 4, 256, seed=5)
+    w.router_bias = inputs.zipf_bias(16, 1.2, 5)
+    x = inputs.tokens(1100, 512, 55)
+    _full_check(oracle_lib, w, x, sched, unfused, debug_flags=B.ETC_DEBUG_NO_PAIR)
 
 
 @pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC, B.ETC_SCHED_MIXED])
