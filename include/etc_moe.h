@@ -72,8 +72,11 @@ typedef enum { ETC_SCHED_STATIC = 0, ETC_SCHED_DYNAMIC = 1, ETC_SCHED_MIXED = 2 
                                            become ready, so a wait times out */
 #define ETC_DEBUG_POISON 0x2u           /* fill intermediate buffers with NaN before each call */
 #define ETC_DEBUG_TRACE 0x4u            /* record every task's dispatch/start/end time and SM */
-#define ETC_DEBUG_NO_PAIR 0x8u          /* run wide expert tiles on single CTAs instead of CTA
-                                           pairs (ablation of the pair tiles) */
+#define ETC_DEBUG_NO_PAIR 0x8u          /* never run expert tiles on CTA pairs (dense MLP: run its
+                                           wide tiles on single CTAs; ablation of the pair tiles) */
+#define ETC_DEBUG_PAIR_MOE 0x10u        /* run the wide expert tiles of MoE calls on CTA pairs too
+                                           (by default only the dense MLP uses them: on the MoE
+                                           layer's skewed chunks they measured no faster) */
 
 typedef struct etc_plan_s* etc_plan_t;
 

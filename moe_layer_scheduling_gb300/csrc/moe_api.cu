@@ -301,10 +301,12 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   // Wide expert tiles once experts average 64 rows or more (and the shapes divide).
   prm.wide = (static_cast<long long>(a.T) * p->k >= 64LL * p->E && p->I % kGuRowsW == 0 &&
               p->H % kDnRowsW == 0) ? 1 : 0;
-  // The same calls run on CTA pairs (one cta_group::2 MMA over two SMs: 256
-  // weight rows x up to 256 chunk rows per tile) when clusters are available.
+  // On request the same calls run on CTA pairs (one cta_group::2 MMA over two
+  // SMs: 256 weight rows x up to 256 chunk rows per tile) when clusters are
+  // available.
   prm.pair = (prm.wide && a.n_blocks == 1 && !a.use_norm && router_tiles && p->pair_grid > 0 &&
-              !(p->opts.debug_flags & ETC_DEBUG_NO_PAIR)) ? 1 : 0;
+              (p->opts.debug_flags & ETC_DEBUG_PAIR_MOE) && !(p->opts.debug_flags & ETC_DEBUG_NO_PAIR))
+                 ? 1 : 0;
   if (prm.pair) prm.wide = 0;
   prm.cw = prm.pair ? kBT2 : kBT;
   prm.nbp = prm.pair ? (prm.nb + 1) / 2 : prm.nb;

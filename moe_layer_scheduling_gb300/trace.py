@@ -56,9 +56,10 @@ def main():
     ap.add_argument("--repeat", type=int, default=3, help="calls before the traced one")
     ap.add_argument("--raw", default=None, help="also write the task records (JSON) to this file")
     ap.add_argument("--mlp", default=None, help="trace the dense MLP of this Table 4 shape instead")
-    ap.add_argument("--no-pair", action="store_true", help="wide tiles on single CTAs, not CTA pairs")
+    ap.add_argument("--no-pair", action="store_true", help="dense MLP: wide tiles on single CTAs")
+    ap.add_argument("--pair", action="store_true", help="MoE layer: wide tiles on CTA pairs")
     args = ap.parse_args()
-    extra = B.ETC_DEBUG_NO_PAIR if args.no_pair else 0
+    extra = (B.ETC_DEBUG_NO_PAIR if args.no_pair else 0) | (B.ETC_DEBUG_PAIR_MOE if args.pair else 0)
     dev = torch.device("cuda")
     sched = {"static": B.ETC_SCHED_STATIC, "dynamic": B.ETC_SCHED_DYNAMIC,
              "mixed": B.ETC_SCHED_MIXED}[args.sched]

@@ -98,12 +98,21 @@ def test_wide_tiles(oracle_lib, sched, unfused, T, seed):
 
 
 @pytest.mark.parametrize("sched,unfused", MODES, ids=MODE_IDS)
-def test_wide_tiles_single_cta(oracle_lib, sched, unfused):
-    # The same wide calls with CTA pairs disabled: 256-weight-row tiles on one SM.
-    w = inputs.moe_weights(512, 16, 4, 256, seed=5)
-    w.router_bias = inputs.zipf_bias(16, 1.2, 5)
-    x = inputs.tokens(1100, 512, 55)
-    _full_check(oracle_lib, w, x, sched, unfused, debug_flags=B.ETC_DEBUG_NO_PAIR)
+@pytest.mark.parametrize("T,seed", [(300, 4), (1100, 5)])
+def test_wide_tiles_on_cta_pairs(oracle_lib, sched, unfused, T, seed):
+    # The same wide calls on CTA pairs (one cta_group::2 MMA per tile over two
+    # SMs, chunks of up to 256 rows), ragged chunk and token tails.
+    w = inputs.moe_weights(512, 16, 4, 256, seed=seed)
+    w.router_bias = inputs.zipf_bias(16, 1.2, seed)
+    x = inputs.tokens(T, 512, seed + 50)
+    _full_check(oracle_lib, w, x, sched, unfused, debug_flags=B.ETC_DEBUG_PAIR_MOE)
+
+
+@pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC, B.ETC_SCHED_MIXED])
+def test_qwen_prefill_on_cta_pairs(oracle_lib, qwen, qwen_dev, sched):
+    # Qwen shape at T=1100 on CTA pairs, every token checked against the oracle.
+    x = inputs.tokens(1100, inputs.QWEN_H, 1100)
+    _full_check(oracle_lib, qwen, x, sched, False, dw=qwen_dev, debug_flags=B.ETC_DEBUG_PAIR_MOE)
 
 
 @pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC, B.ETC_SCHED_MIXED])

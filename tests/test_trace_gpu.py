@@ -79,11 +79,12 @@ def _check_pairs(recs):
 
 @pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC], ids=["static", "dynamic"])
 def test_trace_of_a_pair_tile_layer(sched):
-    # Enough rows per expert for wide tiles, which run on CTA pairs: every
+    # Enough rows per expert for wide tiles, run on CTA pairs on request: every
     # router, gate/up and down task appears on the two CTAs of one pair.
     w = inputs.moe_weights(512, 16, 4, 256, seed=5)
     x = inputs.tokens(1100, 512, 55)
-    plan = B.etc_moe_plan(512, 16, 4, 256, t_max=1100, sched=sched, debug_flags=B.ETC_DEBUG_TRACE)
+    plan = B.etc_moe_plan(512, 16, 4, 256, t_max=1100, sched=sched,
+                          debug_flags=B.ETC_DEBUG_TRACE | B.ETC_DEBUG_PAIR_MOE)
     out = torch.empty(1100, 512, device="cuda")
     B.etc_moe_forward(plan, x.cuda(), w.gate_w.cuda(), w.w_gate_up.cuda(), w.w_down.cuda(), 1100, out)
     torch.cuda.synchronize()
