@@ -304,7 +304,13 @@ int etc_splitk_rowsum_ex(void* stream, const float* A, long long n_rows, long lo
                          int n_split, float* C, int sched, unsigned long long wait_timeout_ns,
                          unsigned debug_flags, long long debug_arg);
 
-/* Status of the last split-K calls on the current device (after a sync). */
+/*
+ * Status of the split-K calls on the current device since the last check,
+ * both entry points (call it after synchronising their stream): ETC_OK, or
+ * ETC_ERR_TIMEOUT with the row in etc_last_error(); the status is cleared.
+ * For etc_splitk_rowsum_noalloc it reads the status word of the fixed array
+ * with one synchronous 16-byte copy (nothing is allocated).
+ */
 int etc_splitk_check(void);
 
 /*
@@ -325,7 +331,11 @@ int etc_splitk_check(void);
  * set-up, with that device current); make that first call before any stream
  * capture.  All calls on a device share the one array, so calls that overlap
  * on the GPU (other streams, other threads) race: order them on one stream.
- * A device wait that gives up (2 s) leaves the affected C rows unwritten.
+ * A device wait that gives up (2 s) leaves the affected C rows unwritten and
+ * records the site in the array's status word, which the calls do not clear:
+ * until etc_splitk_check reports and clears it, the waits of later calls give
+ * up at once and may leave C rows unwritten too.  Check after the calls whose
+ * result matters.
  */
 int etc_splitk_rowsum_noalloc(void* stream, const float* A, long long n_rows, long long n_cols,
                               int n_split, float* C, int sched);

@@ -386,6 +386,10 @@ int etc_splitk_rowsum_ex(void* stream, const float* A, long long n_rows, long lo
   return ETC_OK;
 }
 
+namespace etc {
+int noalloc_check(int dev);
+}
+
 int etc_splitk_rowsum(void* stream, const float* A, long long n_rows, long long n_cols,
                       int n_split, float* C, int sched) {
   return etc_splitk_rowsum_ex(stream, A, n_rows, n_cols, n_split, C, sched, 0, 0, -1);
@@ -395,6 +399,8 @@ int etc_splitk_check(void) {
   clear_error();
   int dev = 0;
   ETC_CUDA_TRY(cudaGetDevice(&dev));
+  const int na = etc::noalloc_check(dev);  // the no-allocation entry point's status word
+  if (na != ETC_OK) return na;
   std::lock_guard<std::mutex> lk(g_sk_mu);
   SkScratch* sc = scratch_for(dev);
   if (!sc->status_host) return ETC_OK;
@@ -430,10 +436,13 @@ namespace {
 constexpr long long kNoAllocMaxRows = 65536;           // n_rows limit
 constexpr long long kNoAllocMaxPartials = 262144;      // n_rows * n_split limit
 constexpr size_t kNoAllocHeader = 256;                 // status + queue counters
+constexpr size_t kNoAllocCleared = 128;                // first byte a call clears (the queue counters)
 constexpr size_t kNoAllocBytes =
     kNoAllocHeader + kNoAllocMaxRows * sizeof(int) + kNoAllocMaxPartials * sizeof(float);
 
-// Layout: [DevStatus | head[2] | pad to 256] [ev: int x 65536] [B: float x 262144]
+// Layout: [DevStatus | pad to 128] [head[2] | pad to 256] [ev: int x 65536] [B: float x 262144].
+// The status word sits outside what a call clears: it keeps the first wait
+// that gave up until etc_splitk_check reads and clears it.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 struct NoAllocDevice {
@@ -444,6 +453,23 @@ std::mutex g_na_mu;
 NoAllocDevice g_na[64];
 
 }  // namespace
+
+// Reads (and clears) the status word the no-allocation calls on device `dev`
+// share: a synchronous 16-byte copy out of the fixed array, nothing allocated.
+int noalloc_check(int dev) {
+  if (dev < 0 || dev >= 64) return ETC_OK;
+  std::lock_guard<std::mutex> lk(g_na_mu);
+  NoAllocDevice& nd = g_na[dev];
+  if (!nd.base) return ETC_OK;  // no call on this device yet
+  DevStatus hs;
+  ETC_CUDA_TRY(cudaMemcpy(&hs, nd.base, sizeof hs, cudaMemcpyDeviceToHost));
+  if (hs.code == 0) return ETC_OK;
+  ETC_CUDA_TRY(cudaMemset(nd.base, 0, sizeof(DevStatus)));
+  return set_error(ETC_ERR_TIMEOUT,
+                   "splitk_noalloc: device wait timed out (code %d, site %d, row %d, cta %d)",
+                   hs.code, hs.where, hs.aux, hs.cta);
+}
+
 }  // namespace etc
 
 extern "C" int etc_splitk_rowsum_noalloc(void* stream, const float* A, long long n_rows,
@@ -485,16 +511,17 @@ extern "C" int etc_splitk_rowsum_noalloc(void* stream, const float* A, long long
   int* ev = reinterpret_cast<int*>(nd.base + kNoAllocHeader);
   float* B = reinterpret_cast<float*>(nd.base + kNoAllocHeader + kNoAllocMaxRows * sizeof(int));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // Status, queue counters and this call's row counters must start at zero;
-  // the array keeps whatever the previous call left there.
-  ETC_CUDA_TRY(cudaMemsetAsync(nd.base, 0, kNoAllocHeader + n_rows * sizeof(int), s));
+  // Queue counters and this call's row counters must start at zero; the array
+  // keeps whatever the previous call left there.  (Not the status word.)
+  ETC_CUDA_TRY(cudaMemsetAsync(nd.base + kNoAllocCleared, 0,
+                               kNoAllocHeader - kNoAllocCleared + n_rows * sizeof(int), s));
 
   SkParams p{};
   p.A = A;
   p.C = C;
   p.B = B;
   p.ev = ev;
-  p.head = reinterpret_cast<int*>(nd.base + sizeof(DevStatus));
+  p.head = reinterpret_cast<int*>(nd.base + kNoAllocCleared);
   p.n_rows = n_rows;
   p.n_cols = n_cols;
   p.n_split = n_split;
