@@ -122,31 +122,33 @@ def test_qwen_wide_tiles_full_parity(oracle_lib, qwen, qwen_dev, sched):
     _full_check(oracle_lib, qwen, x, sched, False, dw=qwen_dev)
 
 
-@pytest.mark.parametrize("sched,unfused", MODES, ids=MODE_IDS)
-def test_prefill_skew_full_size(oracle_lib, qwen, qwen_dev, sched, unfused):
-    # T=4096 with Zipf(1.2)-biased routing: empty experts and experts with
-    # hundreds of rows.  Routing and dispatch are checked for all tokens; the
-    # layer output on a sample of tokens (each token's output depends only on
-    # that token).
+@pytest.fixture(scope="module")
+def prefill(oracle_lib, qwen):
+    """The benchmark's prefill workload and the oracle's result for all its tokens."""
     wl = inputs.prefill_skew_layer(4096, qwen)
+    w = wl.weights
+    ref, Lref, ids_ref, _ = oracle_lib.moe_layer(wl.x, w.gate_w, w.w_gate_up, w.w_down, w.top_k,
+                                                 bias=w.router_bias, want_routing=True)
+    return wl, ref, Lref, ids_ref
+
+
+@pytest.mark.parametrize("sched,unfused", MODES, ids=MODE_IDS)
+def test_prefill_skew_full_size(oracle_lib, qwen_dev, prefill, sched, unfused):
+    # T=4096 with Zipf(1.2)-biased routing, in the launch configuration the
+    # benchmark times: empty experts and experts with thousands of rows.
+    # Routing, dispatch and the output of every one of the 4096 tokens are
+    # checked against the oracle.
+    wl, ref, Lref, ids_ref = prefill
     w = wl.weights
     dw = dict(qwen_dev)
     dw["bias"] = w.router_bias.cuda()
     out, routing, plan = run_layer(w, wl.x, sched, unfused, dw=dw)
     plan.close()
-    Lref = oracle_lib.router_logits(wl.x, w.gate_w, w.router_bias)
-    ids_ref, w_ref = oracle_lib.route(Lref, w.top_k)
     counts = np.bincount(ids_ref.ravel(), minlength=w.n_experts)
     assert (counts == 0).any() and counts.max() > 200  # the skew the workload asks for
     dispatch_properties(routing, w.n_experts)
-    sample = np.unique(np.concatenate([np.arange(0, 4096, 37), [4095]]))
-    ref = oracle_lib.moe_layer(wl.x[sample], w.gate_w, w.w_gate_up, w.w_down, w.top_k,
-                               bias=w.router_bias)
-    sub = {k: v[sample] for k, v in routing.items() if k in ("logits", "ids", "w", "pos")}
-    err, tol, nflip = compare_layer(out[sample], sub, ref, Lref[sample], ids_ref[sample], w.top_k)
-    flips_all = int(np.sum(np.any(routing["ids"] != ids_ref, axis=1)))
-    assert flips_all <= 41  # < 1 % of tokens, all near-ties (sampled ones checked above)
-    if flips_all == 0:
+    err, tol, nflip = compare_layer(out, routing, ref, Lref, ids_ref, w.top_k)
+    if nflip == 0:
         check_dispatch_vs_oracle(routing, oracle_lib, ids_ref, w.n_experts)
 
 
@@ -160,6 +162,23 @@ def test_bf16_output(oracle_lib, qwen, qwen_dev, T):
     ref, L, ids, _ = oracle_lib.moe_layer(x, qwen.gate_w, qwen.w_gate_up, qwen.w_down, 8,
                                           want_routing=True)
     compare_layer(out, routing, ref, L, ids, 8, out_bf16=True)
+
+
+def test_run_to_run_difference_is_bounded(qwen, qwen_dev):
+    # The fused combine adds each token's k weighted expert rows with fp32
+    # reductions in L2, in whatever order the down tiles finish: two runs of the
+    # same call may differ, but only by the rounding of a reordered k-term fp32
+    # sum, at most 2k * 2^-24 * sum_j |w_j y_j| per element.  sum_j |w_j y_j|
+    # is taken as 8x the output's largest magnitude (room for cancellation);
+    # a lost or doubled contribution would be ~|w_j y_j|, far above this.
+    T, k = 517, qwen.top_k
+    x = inputs.tokens(T, inputs.QWEN_H, 5170)
+    plan = B.etc_moe_plan(2048, 128, k, 768, t_max=T, sched=B.ETC_SCHED_DYNAMIC)
+    outs = [run_layer(qwen, x, B.ETC_SCHED_DYNAMIC, plan=plan, dw=qwen_dev)[0] for _ in range(3)]
+    plan.close()
+    scale = 8 * np.max(np.abs(outs[0])) * 2 * k * 2.0 ** -24
+    for o in outs[1:]:
+        assert np.max(np.abs(o.astype(np.float64) - outs[0])) <= scale
 
 
 def test_route_from_logits_bit_exact(oracle_lib):
