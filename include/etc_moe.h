@@ -94,11 +94,27 @@ typedef struct {
   unsigned debug_flags;              /* ETC_DEBUG_* */
   int debug_arg;                     /* expert id for ETC_DEBUG_FAULT_EXTRA_WAIT */
   int out_dtype;                     /* ETC_OUT_F32 (default) or ETC_OUT_BF16 */
+  int combine;                       /* ETC_COMBINE_FUSED (default) or ETC_COMBINE_ORDERED */
 } etc_moe_opts;
 
 /* Element type of `out` (etc_moe_opts.out_dtype). */
 #define ETC_OUT_F32 0  /* the fp32 combine sum, unrounded */
 #define ETC_OUT_BF16 1 /* the same sum rounded to bf16 */
+
+/*
+ * How the k weighted expert rows of a token are added (etc_moe_opts.combine):
+ *   FUSED    each down tile adds w * y into the token's fp32 output row with
+ *            fp32 reductions in L2, in the order the tiles finish (no extra
+ *            memory traffic; the last bits may differ from run to run);
+ *   ORDERED  down tiles store their rows y to an fp32 buffer [T*k, H] of the
+ *            plan, and a finaliser per 32-token block forms
+ *            out[t] = sum_{j=0..k-1} w[t,j] * y[pos[t,j]] in j order (fp32 fused
+ *            multiply-adds): the result is the same bit for bit from run to
+ *            run and for every scheduler, at the cost of writing and reading
+ *            the rows once more.
+ */
+#define ETC_COMBINE_FUSED 0
+#define ETC_COMBINE_ORDERED 1
 
 /*
  * Creates a plan for one weight shape: validates the options, allocates the
@@ -113,7 +129,7 @@ int etc_moe_plan(etc_plan_t* plan, const etc_moe_opts* opts);
 
 /*
  * One MoE layer, out = sum_j w[t,j] * FFN_{ids[t,j]}(x[t]), in ONE kernel
- * launch on `stream`.
+ * launch on `stream`.  (See etc_moe_opts.combine for how the sum is formed.)
  *   x          bf16 [T, H]
  *   gate_w     bf16 [H, E]       router weight (logits = x gate_w + bias)
  *   w_gate_up  bf16 [E, 2I, H]   rows 0..I-1 gate, rows I..2I-1 up (K-major)

@@ -28,6 +28,8 @@ ETC_DEBUG_NO_PAIR = 0x8
 ETC_DEBUG_PAIR_MOE = 0x10
 ETC_OUT_F32 = 0
 ETC_OUT_BF16 = 1
+ETC_COMBINE_FUSED = 0
+ETC_COMBINE_ORDERED = 1
 
 EXPORTED = [
     "etc_moe_plan", "etc_moe_forward", "etc_moe_forward_unfused", "etc_moe_route_from_logits",
@@ -52,7 +54,7 @@ class etc_moe_opts(ctypes.Structure):
         ("n_blocks", ctypes.c_int), ("rms_eps", ctypes.c_float),
         ("router_bias", ctypes.c_void_p), ("wait_timeout_ns", ctypes.c_ulonglong),
         ("debug_flags", ctypes.c_uint), ("debug_arg", ctypes.c_int),
-        ("out_dtype", ctypes.c_int),
+        ("out_dtype", ctypes.c_int), ("combine", ctypes.c_int),
     ]
 
 
@@ -165,9 +167,9 @@ class Plan:
 
 def etc_moe_plan(hidden, n_experts, top_k, inter, t_max, sched=ETC_SCHED_STATIC, n_blocks=1,
                  rms_eps=1e-6, router_bias=None, wait_timeout_ns=0, debug_flags=0,
-                 debug_arg=0, out_dtype=ETC_OUT_F32) -> Plan:
+                 debug_arg=0, out_dtype=ETC_OUT_F32, combine=ETC_COMBINE_FUSED) -> Plan:
     o = etc_moe_opts(hidden, n_experts, top_k, inter, t_max, sched, n_blocks, rms_eps,
-                     _ptr(router_bias), wait_timeout_ns, debug_flags, debug_arg, out_dtype)
+                     _ptr(router_bias), wait_timeout_ns, debug_flags, debug_arg, out_dtype, combine)
     h = ctypes.c_void_p()
     _check(load().etc_moe_plan(ctypes.byref(h), ctypes.byref(o)))
     return Plan(h.value, o, keep=router_bias)
@@ -186,9 +188,9 @@ def etc_moe_forward_unfused(plan: Plan, x, gate_w, w_gate_up, w_down, T, out, st
 
 def etc_chain_plan(n_blocks, hidden, n_experts, top_k, inter, t_max, sched=ETC_SCHED_STATIC,
                    rms_eps=1e-6, wait_timeout_ns=0, debug_flags=0, debug_arg=0,
-                   out_dtype=ETC_OUT_F32) -> Plan:
+                   out_dtype=ETC_OUT_F32, combine=ETC_COMBINE_FUSED) -> Plan:
     o = etc_moe_opts(hidden, n_experts, top_k, inter, t_max, sched, 1, rms_eps, None,
-                     wait_timeout_ns, debug_flags, debug_arg, out_dtype)
+                     wait_timeout_ns, debug_flags, debug_arg, out_dtype, combine)
     h = ctypes.c_void_p()
     _check(load().etc_chain_plan(ctypes.byref(h), ctypes.byref(o), int(n_blocks)))
     o.n_blocks = int(n_blocks)

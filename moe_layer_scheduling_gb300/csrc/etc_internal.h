@@ -136,6 +136,7 @@ struct Workspace {
   __nv_bfloat16* x_perm;  // [R_max, H]
   __nv_bfloat16* act;     // [R_max, I]
   float* acc;             // [T_max, H] fp32 combine accumulator when `out` is bf16
+  float* yperm;           // [R_max, H] fp32 expert rows, expert-sorted (ordered combine)
   __nv_bfloat16* xn;      // [T_max, H] normalised input rounded to bf16 (chain)
   __nv_bfloat16* xn_lo;   // [T_max, H] bf16 of what that rounding dropped (router only)
   float* resid;           // [n_blocks-1, T_max, H] fp32 residual stream between blocks
@@ -166,6 +167,7 @@ struct MegaParams {
   const __nv_bfloat16* x;
   void* out;     // fp32 [T, H], or bf16 when out_bf16
   int out_bf16;
+  int ordered;   // combine: down tiles store y rows, a finaliser sums them in j order
   const __nv_bfloat16* gate_w[kMaxBlocks];
   const float* bias[kMaxBlocks];
   const __nv_bfloat16* norm_w[kMaxBlocks];

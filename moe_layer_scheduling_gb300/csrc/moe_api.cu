@@ -154,6 +154,8 @@ int validate_opts(const etc_moe_opts* o) {
     return set_error(ETC_ERR_INVALID, "router_bias must be 16-byte aligned");
   if (o->out_dtype != ETC_OUT_F32 && o->out_dtype != ETC_OUT_BF16)
     return set_error(ETC_ERR_INVALID, "out_dtype=%d unknown", o->out_dtype);
+  if (o->combine != ETC_COMBINE_FUSED && o->combine != ETC_COMBINE_ORDERED)
+    return set_error(ETC_ERR_INVALID, "combine=%d unknown", o->combine);
   return ETC_OK;
 }
 
@@ -278,6 +280,7 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   prm.x = static_cast<const __nv_bfloat16*>(a.x);
   prm.out = a.out;
   prm.out_bf16 = p->opts.out_dtype == ETC_OUT_BF16 ? 1 : 0;
+  prm.ordered = p->opts.combine == ETC_COMBINE_ORDERED ? 1 : 0;
   prm.logits_in = a.logits_in;
   prm.H = p->H;
   prm.E = p->E;
@@ -343,7 +346,7 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   } else {
     for (int stg = TK_ROUTER; stg <= TK_COMB; ++stg) {
       if (stg == TK_TOPK && prm.NC == 1) continue;  // top-k ran inside the router stage
-      if (stg == TK_COMB && !prm.out_bf16 && a.n_blocks == 1) continue;  // nothing to finalise
+      if (stg == TK_COMB && !prm.out_bf16 && !prm.ordered && a.n_blocks == 1) continue;  // nothing to finalise
       prm.stage_lo = prm.stage_hi = stg;
       ETC_CUDA_TRY(launch_megakernel(prm, grid, s));
       ++p->launches;
@@ -561,7 +564,10 @@ int plan_moe_buffers(etc_plan_t p) {
   if (encode_tensor_map_2d_bf16(&p->tm_xperm, p->ws.x_perm, p->H, R, kBK, 16) != CUDA_SUCCESS ||
       encode_tensor_map_2d_bf16(&p->tm_xperm64, p->ws.x_perm, p->H, R, kBK, 64) != CUDA_SUCCESS)
     return set_error(ETC_ERR_CUDA, "tensor map encoding of the workspace failed");
-  if (p->opts.out_dtype == ETC_OUT_BF16) {  // fp32 accumulator behind a bf16 output
+  if (p->opts.combine == ETC_COMBINE_ORDERED) {  // the expert rows the ordered combine sums
+    if ((r = alloc_dev(p, &m, R * p->H * 4)) != ETC_OK) return r;
+    p->ws.yperm = static_cast<float*>(m);
+  } else if (p->opts.out_dtype == ETC_OUT_BF16) {  // fp32 accumulator behind a bf16 output
     if ((r = alloc_dev(p, &m, static_cast<size_t>(p->T_max) * p->H * 4)) != ETC_OK) return r;
     p->ws.acc = static_cast<float*>(m);
   }

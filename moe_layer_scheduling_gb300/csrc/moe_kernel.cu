@@ -137,7 +137,7 @@ __device__ __forceinline__ bool tiles_queued(const MegaParams& p) { return p.mod
 // Otherwise the down tiles' fp32 additions are the result and no COMB runs.
 // The dense MLP's down tiles store their outputs themselves.
 __device__ __forceinline__ bool needs_comb(const MegaParams& p, int blk) {
-  return !p.dense && (blk < p.n_blocks - 1 || p.out_bf16 != 0);
+  return !p.dense && (blk < p.n_blocks - 1 || p.out_bf16 != 0 || p.ordered != 0);
 }
 
 // Dense MLP: the finished gate/up tiles chunk c's down tiles wait for (one more for the
@@ -584,7 +584,7 @@ __device__ __forceinline__ float* acc_rows(const MegaParams& p, int blk) {
 // has no output rows.)
 __device__ void init_acc_rows(const MegaParams& p, int blk, int tb, int wt) {
   float* accr = acc_rows(p, blk);
-  if (accr == nullptr) return;
+  if (accr == nullptr || p.ordered) return;  // (ordered combine: the finaliser writes whole rows)
   const int ww = wt >> 5, lane = wt & 31, n8 = p.H / 8, t0 = tb * kTB, ntok = min(kTB, p.T - t0);
   for (int r = ww; r < ntok; r += 8) {
     const int tok = t0 + r;
@@ -701,12 +701,55 @@ __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* 
 
 // Finaliser of token block tb once every down tile touching it has added its
 // weighted expert rows: rounds the rows to bf16 when the output is bf16, and
-// in the chain releases the next block's RMSNorm of tb.
-__device__ void task_comb(const MegaParams& p, const Task& t, int wt) {
+// in the chain releases the next block's RMSNorm of tb.  Ordered combine: the
+// down tiles stored their rows y; here out[t] = (residual +) sum over j in
+// order 0..k-1 of w[t,j] * y[pos[t,j]], one fused multiply-add per term.
+__device__ void task_comb(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
   const int blk = t.blk, tb = my_tb(p, t.a);
   const BlockWs& B = p.ws.blk[blk];
   const int ww = wt >> 5, lane = wt & 31, n8 = p.H / 8;
-  if (blk == p.n_blocks - 1 && p.out_bf16) {
+  const bool last = blk == p.n_blocks - 1;
+  if (p.ordered) {
+    float* resid = last ? nullptr : acc_rows(p, blk);
+    // the block's rows and weights (written by other CTAs) into shared memory
+    int* s_pos = reinterpret_cast<int*>(simt);                  // [kTB * kMaxK]
+    float* s_w = reinterpret_cast<float*>(simt + 4 * kTB * kMaxK);
+    const int t0 = tb * kTB, ntok = max(0, min(kTB, p.T - t0));
+    for (int i = wt; i < ntok * p.k; i += kNumWorkers) {
+      s_pos[i] = __ldcg(B.pos + t0 * p.k + i);
+      s_w[i] = __ldcg(B.wts + t0 * p.k + i);
+    }
+    named_bar(1, kNumWorkers);
+    for (int r = ww; r < ntok; r += 8) {
+      const int tok = t0 + r;
+      const int* rows = s_pos + r * p.k;
+      const float* wj = s_w + r * p.k;
+      for (int c = lane; c < n8; c += 32) {
+        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (p.use_norm) load_block_input8(p, blk, tok, c, f);
+        for (int j = 0; j < p.k; ++j) {
+          const float4* y = reinterpret_cast<const float4*>(p.ws.yperm + static_cast<size_t>(rows[j]) * p.H) + 2 * c;
+          const float4 a = __ldcg(y), b = __ldcg(y + 1);
+          f[0] = fmaf(wj[j], a.x, f[0]); f[1] = fmaf(wj[j], a.y, f[1]);
+          f[2] = fmaf(wj[j], a.z, f[2]); f[3] = fmaf(wj[j], a.w, f[3]);
+          f[4] = fmaf(wj[j], b.x, f[4]); f[5] = fmaf(wj[j], b.y, f[5]);
+          f[6] = fmaf(wj[j], b.z, f[6]); f[7] = fmaf(wj[j], b.w, f[7]);
+        }
+        if (!last) {
+          float4* d = reinterpret_cast<float4*>(resid + static_cast<size_t>(tok) * p.H) + 2 * c;
+          d[0] = make_float4(f[0], f[1], f[2], f[3]);
+          d[1] = make_float4(f[4], f[5], f[6], f[7]);
+        } else if (p.out_bf16) {
+          reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(tok) * p.H)[c] =
+              f32_to_bf16x8(f);
+        } else {
+          float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.out) + static_cast<size_t>(tok) * p.H) + 2 * c;
+          d[0] = make_float4(f[0], f[1], f[2], f[3]);
+          d[1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
+      }
+    }
+  } else if (last && p.out_bf16) {
     for (int r = ww; r < kTB; r += 8) {
       const int tok = tb * kTB + r;
       if (tok >= p.T) break;
@@ -720,7 +763,6 @@ __device__ void task_comb(const MegaParams& p, const Task& t, int wt) {
     }
   }
   named_bar(1, kNumWorkers);  // notify: comb_flag (by the notifier warp)
-  (void)B;
 }
 
 // TMEM epilogue of a GU or DN tile, then its notify.
@@ -851,6 +893,11 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
             } else {
               __stcs(reinterpret_cast<float4*>(static_cast<float*>(p.out) + o), val);
             }
+          } else if (r < t.rows && p.ordered) {
+            // ordered combine: the expert row y itself, in expert-sorted order
+            const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
+            *reinterpret_cast<float4*>(p.ws.yperm + static_cast<size_t>(t.row0 + r) * p.H + col0 +
+                                       chunk * 4) = val;
           } else if (r < t.rows) {
             const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
             const float wr = s_rw[r];
@@ -1160,7 +1207,7 @@ __device__ void run_workers(const MegaParams& p, Ctrl* c, uint8_t* simt, uint8_t
       case TK_PERM: task_perm(p, c, t, simt, wt, perm_li, clk); break;
       case TK_GU:
       case TK_DN: task_gemm_epilogue<PAIR>(p, c, epi, simt, t, gemm_i, clk, wt, ri); break;
-      case TK_COMB: task_comb(p, t, wt); break;
+      case TK_COMB: task_comb(p, t, simt, wt); break;
       default: break;
     }
     // Every task ends with a barrier of the 256 workers: its writes are done.
