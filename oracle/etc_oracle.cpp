@@ -103,8 +103,19 @@ void router_logits(const uint16_t* x, const uint16_t* wg, const float* bias,
   });
 }
 
+// Weights of a token's k selected experts ids[0..k-1]:
+// w_j = exp(L_j - L_0) / sum_j' exp(L_j' - L_0), the softmax over the selected
+// logits (L_0 the logit of the first selected expert).
+template <class Real>
+void selected_weights(const Real* L, int k, const int32_t* ids, double* w) {
+  const double l0 = static_cast<double>(L[ids[0]]);
+  double z = 0.0;
+  for (int j = 0; j < k; ++j) z += std::exp(static_cast<double>(L[ids[j]]) - l0);
+  for (int j = 0; j < k; ++j) w[j] = std::exp(static_cast<double>(L[ids[j]]) - l0) / z;
+}
+
 // Routing for one token: the k largest logits, ties to the lower expert id,
-// then w_j = exp(L_j - L_0) / sum_j' exp(L_j' - L_0) over the selected k.
+// then the softmax over the selected k.
 template <class Real>
 void route_token(const Real* L, int E, int k, int32_t* ids, double* w) {
   std::vector<char> taken(E, 0);
@@ -118,10 +129,7 @@ void route_token(const Real* L, int E, int k, int32_t* ids, double* w) {
     taken[best] = 1;
     ids[j] = best;
   }
-  const double l0 = static_cast<double>(L[ids[0]]);
-  double z = 0.0;
-  for (int j = 0; j < k; ++j) z += std::exp(static_cast<double>(L[ids[j]]) - l0);
-  for (int j = 0; j < k; ++j) w[j] = std::exp(static_cast<double>(L[ids[j]]) - l0) / z;
+  selected_weights(L, k, ids, w);
 }
 
 // Dispatch: per-expert counts, exp_indptr (exclusive prefix sum of the counts),
@@ -168,11 +176,14 @@ void expert_ffn(const double* xrow, const uint16_t* wgu_e, const uint16_t* wd_e,
   }
 }
 
-// One MoE layer on fp64 input rows xin[T, H] (already widened).
+// One MoE layer on fp64 input rows xin[T, H] (already widened).  ids_in
+// (nullable, [T, k]): the experts each token is routed to, given instead of
+// selected from the logits (the weights are still the softmax of this layer's
+// own logits over the given experts).
 void moe_layer_f64(const double* xin, const uint16_t* x_bf16_for_router, const uint16_t* wg,
                    const float* bias, const uint16_t* wgu, const uint16_t* wd, long T, int H,
                    int E, int k, int I, double* out, double* logits_out, int32_t* ids_out,
-                   double* w_out) {
+                   double* w_out, const int32_t* ids_in = nullptr) {
   std::vector<double> logits(static_cast<size_t>(T) * E);
   if (x_bf16_for_router) {
     router_logits(x_bf16_for_router, wg, bias, T, H, E, logits.data());
@@ -189,7 +200,14 @@ void moe_layer_f64(const double* xin, const uint16_t* x_bf16_for_router, const u
   }
   std::vector<int32_t> ids(static_cast<size_t>(T) * k);
   std::vector<double> w(static_cast<size_t>(T) * k);
-  parallel_for(T, [&](long t) { route_token(&logits[t * E], E, k, &ids[t * k], &w[t * k]); });
+  parallel_for(T, [&](long t) {
+    if (ids_in) {
+      std::copy(ids_in + t * k, ids_in + (t + 1) * k, &ids[t * k]);
+      selected_weights(&logits[t * E], k, &ids[t * k], &w[t * k]);
+    } else {
+      route_token(&logits[t * E], E, k, &ids[t * k], &w[t * k]);
+    }
+  });
 
   std::vector<int32_t> counts(E), exp_indptr(E + 1), pos(static_cast<size_t>(T) * k),
       row_token(static_cast<size_t>(T) * k);
@@ -324,12 +342,17 @@ int oracle_moe_layer(const uint16_t* x, const uint16_t* wg, const float* bias, c
 
 // Chain of n_blocks blocks x <- x + MoE_b(RMSNorm_b(x)); all pointers are
 // arrays of n_blocks per-block tensors.  ids_out: [n_blocks, T, k] (nullable),
-// logits_out: [n_blocks, T, E] (nullable).
-int oracle_chain(const uint16_t* x, int n_blocks, const uint16_t* const* norm_w,
-                 const uint16_t* const* wg, const float* const* bias, const uint16_t* const* wgu,
-                 const uint16_t* const* wd, long T, int H, int E, int k, int I, double eps,
-                 double* out, int32_t* ids_out, double* logits_out) {
+// logits_out: [n_blocks, T, E] (nullable), ids_in: [n_blocks, T, k] (nullable)
+// routing given for every block instead of selected (see moe_layer_f64).
+int oracle_chain_routed(const uint16_t* x, int n_blocks, const uint16_t* const* norm_w,
+                        const uint16_t* const* wg, const float* const* bias,
+                        const uint16_t* const* wgu, const uint16_t* const* wd, long T, int H,
+                        int E, int k, int I, double eps, double* out, int32_t* ids_out,
+                        double* logits_out, const int32_t* ids_in) {
   if (T < 0 || n_blocks <= 0) return -1;
+  if (ids_in)
+    for (long i = 0; i < static_cast<long>(n_blocks) * T * k; ++i)
+      if (ids_in[i] < 0 || ids_in[i] >= E) return -1;
   std::vector<double> cur(static_cast<size_t>(T) * H), normed(static_cast<size_t>(T) * H),
       delta(static_cast<size_t>(T) * H);
   for (long i = 0; i < T * H; ++i) cur[i] = bf16_to_double(x[i]);
@@ -343,11 +366,20 @@ int oracle_chain(const uint16_t* x, int n_blocks, const uint16_t* const* norm_w,
     });
     moe_layer_f64(normed.data(), nullptr, wg[b], bias ? bias[b] : nullptr, wgu[b], wd[b], T, H, E,
                   k, I, delta.data(), logits_out ? logits_out + static_cast<long>(b) * T * E : nullptr,
-                  ids_out ? ids_out + static_cast<long>(b) * T * k : nullptr, nullptr);
+                  ids_out ? ids_out + static_cast<long>(b) * T * k : nullptr, nullptr,
+                  ids_in ? ids_in + static_cast<long>(b) * T * k : nullptr);
     for (long i = 0; i < T * H; ++i) cur[i] += delta[i];
   }
   std::copy(cur.begin(), cur.end(), out);
   return 0;
+}
+
+int oracle_chain(const uint16_t* x, int n_blocks, const uint16_t* const* norm_w,
+                 const uint16_t* const* wg, const float* const* bias, const uint16_t* const* wgu,
+                 const uint16_t* const* wd, long T, int H, int E, int k, int I, double eps,
+                 double* out, int32_t* ids_out, double* logits_out) {
+  return oracle_chain_routed(x, n_blocks, norm_w, wg, bias, wgu, wd, T, H, E, k, I, eps, out,
+                             ids_out, logits_out, nullptr);
 }
 
 // Split-K row sum: B[i,j] = sum of row i over column tile j, C[i] = sum_j B[i,j].

@@ -79,13 +79,15 @@ def _declare(L):
     L.oracle_moe_layer.argtypes = [_P, _P, _P, _P, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P]
     L.oracle_chain.argtypes = [_P, _I, _P, _P, _P, _P, _P, _L, _I, _I, _I, _I, ctypes.c_double,
                                _P, _P, _P]
+    L.oracle_chain_routed.argtypes = [_P, _I, _P, _P, _P, _P, _P, _L, _I, _I, _I, _I,
+                                      ctypes.c_double, _P, _P, _P, _P]
     L.oracle_splitk.argtypes = [_P, _L, _L, _I, _P, _P]
     L.oracle_event_sim.argtypes = [_L, _I, _I, ctypes.c_char_p, ctypes.c_char_p,
                                    ctypes.c_ulonglong, _P, _P, _P, _P, _P]
     L.oracle_event_sim.restype = _L
     for name in ("oracle_router_logits", "oracle_route_f64", "oracle_route_f32",
                  "oracle_dispatch", "oracle_expert_ffn", "oracle_moe_layer", "oracle_chain",
-                 "oracle_splitk"):
+                 "oracle_chain_routed", "oracle_splitk"):
         getattr(L, name).restype = _I
 
 
@@ -209,8 +211,12 @@ def moe_layer(x, gate_w, w_gate_up, w_down, top_k: int, bias=None, want_routing=
     return (out, logits, ids, w) if want_routing else out
 
 
-def chain(x, blocks, eps: float = 1e-6, want_routing=False):
-    """fp64 chain x <- x + MoE_b(RMSNorm_b(x)) over the given blocks (MoEWeights-like)."""
+def chain(x, blocks, eps: float = 1e-6, want_routing=False, ids_in=None):
+    """fp64 chain x <- x + MoE_b(RMSNorm_b(x)) over the given blocks (MoEWeights-like).
+
+    ids_in (optional int [n_blocks, T, k]): the experts of every token in every
+    block, given instead of selected; each block still weights them by the
+    softmax of its own fp64 logits over the given experts."""
     xb = _u16(x)
     T, H = xb.shape
     nb = len(blocks)
@@ -236,8 +242,15 @@ def chain(x, blocks, eps: float = 1e-6, want_routing=False):
     out = np.empty((T, H), dtype=np.float64)
     ids = np.empty((nb, T, k), dtype=np.int32)
     logits = np.empty((nb, T, E), dtype=np.float64)
-    _check(lib().oracle_chain(_ptr(xb), nb, norm, wg, bias, wgu, wd, T, H, E, k, I, float(eps),
-                              _ptr(out), _ptr(ids), _ptr(logits)), "chain")
+    if ids_in is None:
+        _check(lib().oracle_chain(_ptr(xb), nb, norm, wg, bias, wgu, wd, T, H, E, k, I, float(eps),
+                                  _ptr(out), _ptr(ids), _ptr(logits)), "chain")
+    else:
+        given = np.ascontiguousarray(ids_in, dtype=np.int32)
+        assert given.shape == (nb, T, k), given.shape
+        _check(lib().oracle_chain_routed(_ptr(xb), nb, norm, wg, bias, wgu, wd, T, H, E, k, I,
+                                         float(eps), _ptr(out), _ptr(ids), _ptr(logits),
+                                         _ptr(given)), "chain")
     return (out, ids, logits) if want_routing else out
 
 

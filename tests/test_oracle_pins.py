@@ -323,6 +323,46 @@ def test_chain_matches_blockwise_brute_force(oracle_lib):
     assert _rel(out, cur) < 1e-12
 
 
+def test_chain_given_its_own_routing_is_the_plain_chain(oracle_lib):
+    # Routing given as exactly what the chain selects itself changes nothing.
+    blocks = _small_chain(3)
+    x = inputs.tokens(6, 64, 303)
+    out, ids, logits = oracle_lib.chain(x, blocks, want_routing=True)
+    out2, ids2, logits2 = oracle_lib.chain(x, blocks, want_routing=True, ids_in=ids)
+    assert np.array_equal(out, out2) and np.array_equal(ids, ids2) and np.array_equal(logits, logits2)
+
+
+def test_chain_given_routing_matches_brute_force(oracle_lib):
+    # Any given routing: each block uses the given experts, weighted by the
+    # softmax of its own logits over them (renormalised full softmax).
+    blocks = _small_chain(3)
+    T, E, k = 5, 8, 2
+    x = inputs.tokens(T, 64, 304)
+    given = np.zeros((3, T, k), dtype=np.int32)
+    for b in range(3):
+        for t in range(T):
+            given[b, t] = [(t + 3 * b) % E, (t + 3 * b + 5) % E]
+    out, ids, _ = oracle_lib.chain(x, blocks, want_routing=True, ids_in=given)
+    assert np.array_equal(ids, given)
+    cur = _f64(x)
+    for b, blk in enumerate(blocks):
+        rms = np.sqrt(np.mean(cur * cur, axis=1, keepdims=True) + 1e-6)
+        X = cur / rms * _f64(blk.norm_w)[None, :]
+        L = X @ _f64(blk.gate_w)
+        probs = softmax(L, axis=1)
+        I = blk.w_gate_up.shape[1] // 2
+        delta = np.zeros_like(X)
+        for t in range(T):
+            sel = list(given[b, t])
+            p = probs[t, sel] / probs[t, sel].sum()
+            for wj, e in zip(p, sel):
+                gu = _f64(blk.w_gate_up[e]) @ X[t]
+                g, u = gu[:I], gu[I:]
+                delta[t] += wj * (_f64(blk.w_down[e]) @ (g / (1.0 + np.exp(-g)) * u))
+        cur = cur + delta
+    assert _rel(out, cur) < 1e-12
+
+
 def test_chain_zero_experts_is_identity(oracle_lib):
     blocks = _small_chain(4)
     for b in blocks:
