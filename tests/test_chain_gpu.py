@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 import torch
 
-from _moe_check import LOGIT_RTOL, near_tie, read_routing, topk_is_valid
+from _moe_check import LOGIT_RTOL, dispatch_properties, near_tie, read_routing, topk_is_valid
 from moe_layer_scheduling_gb300 import binding as B
 from moe_layer_scheduling_gb300 import inputs
 
@@ -34,39 +34,50 @@ def _run_chain(plan, bd, x_cpu):
 
 
 def _check_chain(plan, blocks, x, out, oracle_lib):
-    """Output within 2e-2*RMS on every token whose routing agrees with the
-    oracle in all blocks; tokens whose routing differs must be near-ties in
-    the oracle's logits (the bf16 residual stream moves logits by ~1e-3)."""
+    """Every block and every token of a chain call against the oracle.
+
+    The oracle runs the chain on the GPU's own routing (its expert ids per block),
+    so every token's output is comparable, re-routed or not; it is held to
+    2e-2 * RMS.  Per block:
+      - the GPU's ids are the top-k of its own logits (lower-id ties);
+      - block 0 sees the same input as the oracle: its logits are held to the
+        stated 1e-4 relative bar; later blocks see the earlier blocks' bf16 GEMM
+        rounding in their input, and their logits to the layer bar 2e-2 * RMS;
+      - a token whose expert set differs from the oracle's own top-k of the same
+        block's oracle logits must be a near tie within what the measured logit
+        error can swap: two experts trade places only if their oracle logits are
+        within 2 * max_e |L_gpu - L_oracle| of that token.
+    Returns the re-routed token count of each block."""
     T = x.shape[0]
-    ref, ref_ids, ref_logits = oracle_lib.chain(x, blocks, eps=1e-6, want_routing=True)
-    flipped = np.zeros(T, dtype=bool)
-    for b in range(len(blocks)):
-        r = read_routing(plan, T, blocks[b], block=b)
-        assert topk_is_valid(r["logits"], r["ids"]) == []
-        for t in range(T):
-            if flipped[t]:
-                continue
-            if not np.array_equal(r["ids"][t], ref_ids[b, t]):
-                L = ref_logits[b, t]
-                # bf16 GEMM operands move later blocks' logits by ~1e-3
-                gap = 0.01 * np.sqrt(np.mean(L * L))
-                assert near_tie(L, blocks[b].top_k, r["ids"][t], ref_ids[b, t], gap), (b, t)
-                flipped[t] = True
+    nbk, k = len(blocks), blocks[0].top_k
+    gpu = [read_routing(plan, T, blocks[b], block=b) for b in range(nbk)]
+    gids = np.stack([g["ids"] for g in gpu])
+    ref, _, ref_logits = oracle_lib.chain(x, blocks, eps=1e-6, want_routing=True, ids_in=gids)
+    rerouted = []
+    for b in range(nbk):
+        L_gpu = gpu[b]["logits"].astype(np.float64)
+        L_ref = ref_logits[b]
+        rms_L = np.sqrt(np.mean(L_ref * L_ref))
+        dL = np.abs(L_gpu - L_ref)
         if b == 0:
-            # block 0 sees the same input as the oracle: logits within 1e-4 relative
-            # up to the bf16 rounding of the normalised input.
-            Lr = ref_logits[0]
-            rms = np.sqrt(np.mean(Lr * Lr))
-            assert np.max(np.abs(r["logits"] - Lr)) <= 2e-2 * rms
-    # Later blocks see the bf16-rounded expert outputs of earlier ones, so a
-    # few near-tied selections differ from the fp64 chain.
-    assert flipped.sum() <= max(3, int(0.15 * T)), f"{int(flipped.sum())} of {T} tokens re-routed"
-    keep = ~flipped
+            assert np.all(dL <= LOGIT_RTOL * (np.abs(L_ref) + rms_L)), f"block 0 logits: {dL.max():.3e}"
+        else:
+            assert dL.max() <= 2e-2 * rms_L, (b, dL.max(), rms_L)
+        assert topk_is_valid(gpu[b]["logits"], gids[b]) == []
+        dispatch_properties(gpu[b], blocks[b].n_experts)
+        own, _ = oracle_lib.route(L_ref, k)
+        n = 0
+        for t in range(T):
+            if not np.array_equal(np.sort(gids[b, t]), np.sort(own[t])):
+                n += 1
+                assert near_tie(L_ref[t], k, gids[b, t], own[t], 2 * dL[t].max()), (b, t)
+        rerouted.append(n)
     rms = float(np.sqrt(np.mean(ref * ref)))
     assert np.isfinite(out).all()
-    if keep.any():  # (a one-token call whose token is a near-tie leaves nothing to compare)
-        err = float(np.max(np.abs(out[keep] - ref[keep])))
-        assert err <= 2e-2 * rms, f"chain max err {err:.4e} > {2e-2 * rms:.4e}"
+    err = float(np.max(np.abs(out - ref)))
+    assert err <= 2e-2 * rms, f"chain max err {err:.4e} > {2e-2 * rms:.4e}"
+    print(f"chain T={T}: re-routed tokens per block {rerouted}, max err {err / rms:.2e} * RMS")
+    return rerouted
 
 
 @pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC])
@@ -96,16 +107,20 @@ def test_chain_parity(oracle_lib, blocks, blocks_dev, sched, T):
 @pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_DYNAMIC])
 def test_chain_dynamic_t_sequence(oracle_lib, blocks, blocks_dev, sched):
     # The seeded 200-value T sequence in [1, 512] on one plan: one launch per
-    # call, no recompilation; a subset of calls checked against the oracle.
+    # call, no recompilation; every 20th call (10 calls, whatever their T)
+    # checked token by token against the oracle.
     plan = B.etc_moe_plan(2048, 128, 8, 768, t_max=512, sched=sched, n_blocks=4)
     seq = inputs.chain_t_sequence(200, 1, 512, seed=7)
     launches0 = B.etc_plan_stats(plan)["launches"]
+    checked = []
     for i, T in enumerate(seq):
         x = inputs.tokens(T, 2048, 9000 + i)
         out = _run_chain(plan, blocks_dev, x)
         assert np.all(np.isfinite(out))
-        if i % 50 == 0 and T <= 256:
+        if i % 20 == 0:
             _check_chain(plan, blocks, x, out, oracle_lib)
+            checked.append(T)
+    assert len(checked) == 10 and max(checked) > 256
     assert B.etc_plan_stats(plan)["launches"] - launches0 == len(seq)
     plan.close()
 
