@@ -188,6 +188,7 @@ struct MegaParams {
   int nbp;       // token blocks as tasks see them: nb, or ceil(nb / 2) pair blocks
   int ev_mul;    // notifies per tile or routing task (2 with pair tiles: one per CTA)
   int thin;      // narrow tiles whose chunks hold at most kTB rows: 20 KB stages
+  int direct;    // one token block: gate/up tiles read all T token rows of x (no permute)
   unsigned epoch;
   int mode;  // 0 static, 1 dynamic, 2 mixed
   int dense;     // dense MLP: one weight set, chunks are 128-row slices of x, no routing

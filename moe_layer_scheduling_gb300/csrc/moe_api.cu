@@ -320,6 +320,9 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   // An expert holds at most one row per token: with T <= kTB no chunk is
   // above kTB rows, and the thin stages hold a whole token operand.
   prm.thin = (!prm.wide && !prm.pair && a.T <= kTB) ? 1 : 0;
+  // One token block: gate/up tiles read the T token rows straight from x (or
+  // the chain's normalised rows); no permute task, no x_perm rows.
+  prm.direct = (prm.thin && prm.nb == 1 && router_tiles) ? 1 : 0;
   if (++p->epoch == 0) p->epoch = 1;
   prm.epoch = p->epoch;
   prm.mode = mode;
@@ -346,6 +349,7 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   } else {
     for (int stg = TK_ROUTER; stg <= TK_COMB; ++stg) {
       if (stg == TK_TOPK && prm.NC == 1) continue;  // top-k ran inside the router stage
+      if (stg == TK_PERM && prm.direct) continue;   // no permute: tiles read x directly
       if (stg == TK_COMB && !prm.out_bf16 && !prm.ordered && a.n_blocks == 1) continue;  // nothing to finalise
       prm.stage_lo = prm.stage_hi = stg;
       ETC_CUDA_TRY(launch_megakernel(prm, grid, s));

@@ -207,18 +207,20 @@ __device__ __forceinline__ void load_block_input8(const MegaParams& p, int blk, 
   }
 }
 
-// Exclusive prefix sum over the 256 worker threads; `tmp` holds >= 8 ints.
-__device__ __forceinline__ int workers_excl_scan(int v, int* tmp, int wt) {
+// Exclusive prefix sum over the 256 worker threads; `tmp` holds >= 8 values.
+// (64-bit, so that two 32-bit sums can travel packed in one scan.)
+__device__ __forceinline__ unsigned long long workers_excl_scan(unsigned long long v,
+                                                                unsigned long long* tmp, int wt) {
   const int lane = wt & 31, w = wt >> 5;
-  int x = v;
+  unsigned long long x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) tmp[w] = x;
   named_bar(1, kNumWorkers);
-  int base = 0;
+  unsigned long long base = 0;
   for (int i = 0; i < w; ++i) base += tmp[i];
   named_bar(1, kNumWorkers);
   return base + x - v;
@@ -280,11 +282,11 @@ __device__ void task_norm(const MegaParams& p, const Task& t, int wt) {
 // of the block follows.
 // ---------------------------------------------------------------------------
 
-// Top-k of the tokens tok0.. of a block whose fp32 logits (bias included) are
-// in s_log [kTB][E]: one warp per token, ties to the lower expert id, weights
-// the softmax over the k selected logits.  Counts the experts in s_cnt.
-__device__ void topk_rows(const MegaParams& p, const BlockWs& B, const float* s_log, int tok0,
-                          int* s_cnt, int ww, int lane) {
+// Top-k by warps (blocks of more than kTopkRankMax tokens): one warp per
+// token, k rounds of a warp arg-max, ties to the lower expert id; weights the
+// softmax over the k selected logits.  Counts the experts in s_cnt.
+__device__ void topk_rows_warp(const MegaParams& p, const BlockWs& B, const float* s_log, int tok0,
+                               int* s_cnt, int ww, int lane) {
   const int E = p.E, k = p.k;
   for (int r = ww; r < kTB; r += 8) {
     const int tok = tok0 + r;
@@ -335,6 +337,61 @@ __device__ void topk_rows(const MegaParams& p, const BlockWs& B, const float* s_
   }
 }
 
+
+// Top-k of the tokens tok0.. of a block whose fp32 logits (bias included) are
+// in s_log [kTB][E].  Blocks of at most kTopkRankMax tokens (decode-sized
+// calls, where this task is on the critical path) use all 256 workers at
+// once: each (token, expert) pair counts the experts ahead of it in the order
+// (logit descending, expert id ascending); those of rank < k are the
+// selection, in rank order, so ties go to the lower expert id.  Larger blocks
+// take the warp arg-max above (the same selection).  Weights: the softmax over
+// the k selected logits.  Counts the selected experts in s_cnt.  `scr`: 4 KB
+// of scratch.
+constexpr int kTopkRankMax = 8;
+constexpr int kTopkScratchOff = 18 * 1024;  // offset of the top-k scratch in the SIMT region
+constexpr int kDirectOff = 24 * 1024;       // direct mode: the scan's row tables
+constexpr int kGatherOff = 16 * 1024;       // direct mode: gate/up activations of all T tokens
+__device__ void topk_rows(const MegaParams& p, const BlockWs& B, const float* s_log, int tok0,
+                          int* s_cnt, int wt, uint8_t* scr) {
+  const int E = p.E, k = p.k;
+  const int nt = max(0, min(kTB, p.T - tok0));
+  if (nt > kTopkRankMax) {
+    topk_rows_warp(p, B, s_log, tok0, s_cnt, wt >> 5, wt & 31);
+    return;
+  }
+  float* s_v = reinterpret_cast<float*>(scr);                 // [kTB][kMaxK] selected logits by rank
+  int* s_i = reinterpret_cast<int*>(scr + 4 * kTB * kMaxK);  // [kTB][kMaxK] selected experts by rank
+  for (int idx = wt; idx < nt * E; idx += kNumWorkers) {
+    const int r = idx / E, e = idx - r * E;
+    const float* row = s_log + r * E;
+    const float v = row[e];
+    int rank = 0;
+    for (int f = 0; f < E; f += 4) {
+      const float4 u = *reinterpret_cast<const float4*>(row + f);
+      rank += static_cast<int>(u.x > v) | (static_cast<int>(u.x == v) & static_cast<int>(f < e));
+      rank += static_cast<int>(u.y > v) | (static_cast<int>(u.y == v) & static_cast<int>(f + 1 < e));
+      rank += static_cast<int>(u.z > v) | (static_cast<int>(u.z == v) & static_cast<int>(f + 2 < e));
+      rank += static_cast<int>(u.w > v) | (static_cast<int>(u.w == v) & static_cast<int>(f + 3 < e));
+    }
+    if (rank < k) {
+      s_v[r * kMaxK + rank] = v;
+      s_i[r * kMaxK + rank] = e;
+    }
+  }
+  named_bar(1, kNumWorkers);
+  for (int idx = wt; idx < nt * k; idx += kNumWorkers) {
+    const int r = idx / k, j = idx - r * k;
+    const float* vr = s_v + r * kMaxK;
+    const float v0 = vr[0];
+    float z = 0.f;
+    for (int q = 0; q < k; ++q) z += expf(vr[q] - v0);
+    const int e = s_i[r * kMaxK + j], tok = tok0 + r;
+    B.ids[tok * k + j] = e;
+    B.wts[tok * k + j] = expf(vr[j] - v0) / z;
+    atomicAdd(&s_cnt[e], 1);
+  }
+}
+
 // The block's expert histogram: kept per block (the permute derives its row
 // offsets from it) and added into the call's counts (what the scan reads),
 // unless it is the call's only block and its task runs the scan itself.
@@ -377,7 +434,7 @@ __device__ void task_router_epilogue(const MegaParams& p, Ctrl* c, uint8_t* simt
   tc_fence_after();
   const BlockWs& B = p.ws.blk[t.blk];
   const int w = warp_id(), q = w & 3, h = (w - kWorkerWarp0) >> 2, lane = lane_id();
-  const int E = p.E, e = 32 * q + lane, ww = wt >> 5;
+  const int E = p.E, e = 32 * q + lane;
   const uint32_t col0 = p.pair ? 32u * pair_rank(p) : 0u;
   int* s_cnt = reinterpret_cast<int*>(simt);             // [E]
   float* s_log = reinterpret_cast<float*>(simt + 1024);  // [kTB][E]
@@ -414,7 +471,7 @@ __device__ void task_router_epilogue(const MegaParams& p, Ctrl* c, uint8_t* simt
       const int r = idx / E;
       if (tok0 + r < p.T) B.logits[static_cast<size_t>(tok0) * E + idx] = s_log[idx];
     }
-    topk_rows(p, B, s_log, tok0, s_cnt, ww, lane);
+    topk_rows(p, B, s_log, tok0, s_cnt, wt, simt + kTopkScratchOff);
     named_bar(1, kNumWorkers);
     publish_block_counts(p, B, tb, s_cnt, wt);
   }
@@ -426,16 +483,17 @@ __device__ void task_router_epilogue(const MegaParams& p, Ctrl* c, uint8_t* simt
 __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int wt) {
   const int blk = t.blk, tb = my_tb(p, t.a);
   const BlockWs& B = p.ws.blk[blk];
-  const int E = p.E, ww = wt >> 5, lane = wt & 31;
+  const int E = p.E;
   int* s_cnt = reinterpret_cast<int*>(simt);             // [E]
   float* s_log = reinterpret_cast<float*>(simt + 1024);  // [kTB][E]
   for (int i = wt; i < E; i += kNumWorkers) s_cnt[i] = 0;
   const float* bias = p.bias[blk];
   const int tok0 = tb * kTB;
   if (p.logits_in) init_acc_rows(p, blk, tb, wt);  // no router tile ran for this block
-  for (int idx = wt; idx < kTB * E; idx += kNumWorkers) {
+  const int ntok = max(0, min(kTB, p.T - tok0));
+  for (int idx = wt; idx < ntok * E; idx += kNumWorkers) {
     const int r = idx / E, e = idx - r * E, tok = tok0 + r;
-    if (tok < p.T) {
+    {
       const size_t o = static_cast<size_t>(tok) * E + e;
       float s;
       if (p.logits_in) {
@@ -452,7 +510,7 @@ __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int
     }
   }
   named_bar(1, kNumWorkers);
-  topk_rows(p, B, s_log, tok0, s_cnt, ww, lane);
+  topk_rows(p, B, s_log, tok0, s_cnt, wt, simt + kTopkScratchOff);
   named_bar(1, kNumWorkers);
   if (tb < p.nb) publish_block_counts(p, B, tb, s_cnt, wt, !p.fuse_scan);
   if (p.fuse_scan) {
@@ -485,8 +543,11 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
   int* tmp = reinterpret_cast<int*>(simt);  // scan scratch [32]
   const int cw = p.cw;
   const int nch = (cnt + cw - 1) / cw;
-  const int row0 = workers_excl_scan(cnt, tmp, wt);
-  const int ch0 = workers_excl_scan(nch, tmp + 16, wt);
+  // rows (low half) and chunks (high half) of the experts before this one, in one scan
+  const unsigned long long pre = workers_excl_scan(
+      (static_cast<unsigned long long>(nch) << 32) | static_cast<unsigned>(cnt),
+      reinterpret_cast<unsigned long long*>(simt + 256), wt);
+  const int row0 = static_cast<int>(pre & 0xffffffffu), ch0 = static_cast<int>(pre >> 32);
   if (wt < E) {
     B.counts[wt] = cnt;
     B.exp_indptr[wt] = row0;
@@ -507,9 +568,30 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
       B.ev_act[chn] = p.ev_mul * p.NT_gu;
       B.ev_down[chn] = p.ev_mul * p.NT_dn;
     }
-    // Data-dependent event update: expert e waits for its counts[e] rows.
+    // Data-dependent event update: expert e waits for its counts[e] rows
+    // (none in direct mode: its tiles read x itself).
     const int extra = ((p.debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT) && wt == p.debug_arg) ? 1 : 0;
-    B.ev_expert[wt] = cnt + extra;
+    B.ev_expert[wt] = (p.direct ? 0 : cnt) + extra;
+  }
+  int* s_row0 = reinterpret_cast<int*>(simt + kDirectOff);  // [kMaxE]
+  if (p.direct) {
+    // Direct mode (one token block, no permute task): the expert-sorted row of
+    // every slot (t, j) is exp_indptr[e] + the number of earlier slots routed
+    // to the same expert (ascending token within an expert).
+    int* s_ids = s_row0 + kMaxE;  // [kTB * kMaxK]
+    const int ns = p.T * p.k;
+    if (wt < E) s_row0[wt] = row0;
+    for (int i = wt; i < ns; i += kNumWorkers) s_ids[i] = __ldcg(B.ids + i);
+    named_bar(1, kNumWorkers);
+    for (int sl = wt; sl < ns; sl += kNumWorkers) {
+      const int e = s_ids[sl];
+      int rank = 0;
+      for (int s2 = 0; s2 < sl; ++s2) rank += s_ids[s2] == e;
+      const int row = s_row0[e] + rank;
+      B.pos[sl] = row;
+      B.row_token[row] = sl / p.k;
+      B.row_w[row] = __ldcg(B.wts + sl);
+    }
   }
   if (needs_comb(p, blk)) {
     // token rows the finaliser of (pair) token block tb waits for
@@ -528,40 +610,45 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
       const int n_chunks = B.meta[0];
       const int nbp = p.nbp;
       const int routing = dyn ? (p.use_norm ? nbp : 0) + p.n_router + (p.NC > 1 ? nbp : 0) +
-                                    (p.fuse_scan ? 0 : 1) + nbp * p.PP
+                                    (p.fuse_scan ? 0 : 1) + (p.direct ? 0 : nbp * p.PP)
                               : 0;
       const int blk_tasks = routing + n_chunks * (p.NT_gu + p.NT_dn) + (needs_comb(p, blk) ? nbp : 0);
       const int acc = (blk == 0 ? 0 : *p.ws.qacc) + blk_tasks;
       *p.ws.qacc = acc;
       if (blk == p.n_blocks - 1) *p.ws.qtotal = acc;
     }
-    // Re-arm the other parity's queue for the next call (whatever its mode).
-    const int other = (p.epoch + 1) & 1;
-    *p.ws.qhead[other] = 0;
-    *p.ws.qtail[other] = 0;
     __threadfence();
     st_release(B.plan_flag, p.epoch);
     if (tiles_queued(p) && blk == p.n_blocks - 1) st_release(p.ws.qtotal_flag, p.epoch);
-    if (dyn) {
+    // The tasks this plan makes ready at once: the block's permute tasks
+    // (DYNAMIC), or in direct mode every gate/up tile (DYNAMIC and MIXED).
+    const int n_push = p.direct ? (tiles_queued(p) ? B.meta[0] * p.NT_gu : 0) : dyn ? p.nbp * p.PP : 0;
+    if (n_push) {
       const QueueView q = queue_of(p);
-      tmp[0] = q.n_seed + atom_add_relaxed(q.tail, p.nbp * p.PP);  // the block's permute tasks
+      tmp[0] = q.n_seed + atom_add_relaxed(q.tail, n_push);
     }
+    tmp[1] = n_push;
   }
-  if (dynamic_mode(p)) {
+  if (p.direct ? tiles_queued(p) : dynamic_mode(p)) {
     // Every worker writes some of the reserved slots.
     named_bar(1, kNumWorkers);
-    const int base = tmp[0];
+    const int base = tmp[0], n_push = tmp[1];
     const QueueView q = queue_of(p);
     __threadfence();  // the plan above is published with the slots
-    for (int i = wt; i < p.nbp * p.PP; i += kNumWorkers) {
+    for (int i = wt; i < n_push; i += kNumWorkers) {
       if (base + i >= q.cap) {
         const Clock c0{~0ull, p.ws.status, p.ws.status_host};
         raise_error(c0, DERR_QUEUE_OVERFLOW, 3, base + i);
         break;
       }
-      st_relaxed_u64(&q.slots[base + i],
-                     (static_cast<unsigned long long>(q.epoch) << 32) |
-                         task_enc(TK_PERM, blk, i / p.PP, i % p.PP));
+      // (fault injection: the tiles of the expert that waits for one row more
+      // are never made ready, so a queue pop runs out of time)
+      if (p.direct && (p.debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT) &&
+          __ldcg(B.chunk_expert + i / p.NT_gu) == p.debug_arg)
+        continue;
+      const uint32_t d = p.direct ? task_enc(TK_GU, blk, i / p.NT_gu, i % p.NT_gu)
+                                  : task_enc(TK_PERM, blk, i / p.PP, i % p.PP);
+      st_relaxed_u64(&q.slots[base + i], (static_cast<unsigned long long>(q.epoch) << 32) | d);
     }
   }
 }
@@ -831,6 +918,38 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
         }
         named_bar(2 + h, 128);
       }
+    } else if (t.type == TK_GU && p.direct) {
+      // Direct mode: the accumulator's columns are the call's T tokens.  The
+      // activations of all of them go to shared memory, then each chunk row
+      // takes its own token's.
+      __nv_bfloat16* SA = reinterpret_cast<__nv_bfloat16*>(simt + kGatherOff);  // [kTB][64]
+      const int ncbt = (p.T + 15) >> 4;
+      for (int cb = h; cb < ncbt; cb += 2) {
+        float v[16];
+        tmem_ld16(tbase + cb * 16, v);
+        if (q >= 2) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) U[((q - 2) * 16 + i) * 32 + lane] = v[i];
+        }
+        named_bar(2 + h, 128);
+        if (q < 2) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float gte = v[i];
+            const float up = U[(q * 16 + i) * 32 + lane];
+            SA[(cb * 16 + i) * 64 + 32 * q + lane] = __float2bfloat16_rn(gte / (1.0f + __expf(-gte)) * up);
+          }
+        }
+        named_bar(2 + h, 128);
+      }
+      named_bar(1, kNumWorkers);
+      for (int idx = wt; idx < t.rows * 8; idx += kNumWorkers) {
+        const int i = idx >> 3, chunk = idx & 7;
+        const int tok = __ldcg(B.row_token + t.row0 + i);
+        const uint4 val = *reinterpret_cast<const uint4*>(SA + tok * 64 + chunk * 8);
+        store_act(p, reinterpret_cast<uint4*>(p.ws.act + static_cast<size_t>(t.row0 + i) * p.I +
+                                              t.b * kGuRows + chunk * 8), val);
+      }
     } else if (t.type == TK_GU) {
       for (int cb = h; cb < ncb; cb += 2) {
         float v[16];
@@ -876,33 +995,48 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
 #pragma unroll
         for (int i = 0; i < 16; ++i) S32[i * 128 + 32 * q + lane] = v[i];
         named_bar(2 + h, 128);
+        if (p.dense) {
 #pragma unroll
-        for (int rep = 0; rep < 4; ++rep) {
-          const int idx = i128 + 128 * rep;
-          const int r = cb * 16 + (idx >> 5), chunk = idx & 31;
-          if (r < t.rows && p.dense) {
-            const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
-            const size_t o = static_cast<size_t>(t.row0 + r) * p.H + col0 + chunk * 4;
-            if (p.out_bf16) {
-              const __nv_bfloat162 lo = __floats2bfloat162_rn(val.x, val.y);
-              const __nv_bfloat162 hi = __floats2bfloat162_rn(val.z, val.w);
-              uint2 pk;
-              pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-              pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-              __stcs(reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + o), pk);
-            } else {
-              __stcs(reinterpret_cast<float4*>(static_cast<float*>(p.out) + o), val);
+          for (int rep = 0; rep < 4; ++rep) {
+            const int idx = i128 + 128 * rep;
+            const int r = cb * 16 + (idx >> 5), chunk = idx & 31;
+            if (r < t.rows) {
+              const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
+              const size_t o = static_cast<size_t>(t.row0 + r) * p.H + col0 + chunk * 4;
+              if (p.out_bf16) {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(val.x, val.y);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(val.z, val.w);
+                uint2 pk;
+                pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+                pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+                __stcs(reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + o), pk);
+              } else {
+                __stcs(reinterpret_cast<float4*>(static_cast<float*>(p.out) + o), val);
+              }
             }
-          } else if (r < t.rows && p.ordered) {
-            // ordered combine: the expert row y itself, in expert-sorted order
-            const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
-            *reinterpret_cast<float4*>(p.ws.yperm + static_cast<size_t>(t.row0 + r) * p.H + col0 +
-                                       chunk * 4) = val;
-          } else if (r < t.rows) {
-            const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
-            const float wr = s_rw[r];
-            red_add_v4(accr + static_cast<size_t>(s_rtok[r]) * p.H + chunk * 4,
-                       make_float4(wr * val.x, wr * val.y, wr * val.z, wr * val.w));
+          }
+        } else if (p.ordered) {
+          // ordered combine: the expert row y itself, in expert-sorted order
+#pragma unroll
+          for (int rep = 0; rep < 4; ++rep) {
+            const int idx = i128 + 128 * rep;
+            const int r = cb * 16 + (idx >> 5), chunk = idx & 31;
+            if (r < t.rows)
+              *reinterpret_cast<float4*>(p.ws.yperm + static_cast<size_t>(t.row0 + r) * p.H + col0 +
+                                         chunk * 4) =
+                  *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
+          }
+        } else {
+#pragma unroll
+          for (int rep = 0; rep < 4; ++rep) {
+            const int idx = i128 + 128 * rep;
+            const int r = cb * 16 + (idx >> 5), chunk = idx & 31;
+            if (r < t.rows) {
+              const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
+              const float wr = s_rw[r];
+              red_add_v4(accr + static_cast<size_t>(s_rtok[r]) * p.H + chunk * 4,
+                         make_float4(wr * val.x, wr * val.y, wr * val.z, wr * val.w));
+            }
           }
         }
         named_bar(2 + h, 128);
@@ -1312,7 +1446,10 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
       const int r0 = t.e * p.H + (pair ? t.b * kDnRowsW + kDnRows * rank : t.b * (wide ? kDnRowsW : kDnRows));
       for (int i = 0; i < 4; ++i) rowA[i] = r0 + 64 * i;
     }
-    const uint32_t bytes = nA * (kOpABytes / 2) + nb16 * 16 * kBK * 2;
+    // Direct mode: a gate/up tile's token operand is all T (<= 32) rows of x,
+    // one 32-row box (rows past T read as zero).
+    const bool direct_x = gu && p.direct;
+    const uint32_t bytes = nA * (kOpABytes / 2) + (direct_x ? kTB : nb16 * 16) * kBK * 2;
     fence_proxy_async_global();
     for (int kb = 0; kb < KB; ++kb, st = st + 1 == g.n ? (ph ^= 1, 0) : st + 1) {
       const int s = st;
@@ -1321,6 +1458,10 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
       uint8_t* sb = sa + g.boff;
       if (announce) mbar_arrive_expect_tx(&c->full[s], bytes * tx_mul);
       for (int i = 0; i < nA; ++i) load(sa + i * (kOpABytes / 2), ta, s, kb * kBK, rowA[i]);
+      if (direct_x) {
+        load(sb, &p.tm_xr, s, kb * kBK, 0);
+        continue;
+      }
       for (int i = 0; i < n64; ++i) load(sb + i * 64 * kBK * 2, tb64, s, kb * kBK, brow0 + 64 * i);
       for (int i = 0; i < r16; ++i)
         load(sb + (n64 * 64 + i * 16) * kBK * 2, tb, s, kb * kBK, brow0 + n64 * 64 + 16 * i);
@@ -1351,7 +1492,9 @@ __device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock
     const uint32_t d = tmem + acc * kAccCols;
     // N = token columns: the 32-token router block (64 over a pair), the
     // chunk rounded to 16 (a pair's chunk rounded to 32).
-    const int npad = rt ? (pair ? 2 * kTB : kTB) : pair ? pair_npad(t.rows) : (t.rows + 15) & ~15;
+    // (direct mode: a gate/up tile's columns are all T tokens)
+    const int ncol = (t.type == TK_GU && p.direct) ? p.T : t.rows;
+    const int npad = rt ? (pair ? 2 * kTB : kTB) : pair ? pair_npad(ncol) : (ncol + 15) & ~15;
     const int M = pair ? 256 : 128;
     // Router tiles read A (the router weight) MN-major; expert tiles K-major.
     const uint32_t idesc = rt ? idesc_bf16_f32_amn(M, npad) : idesc_bf16_f32(M, npad);
@@ -1507,7 +1650,7 @@ __device__ bool sched_static(const MegaParams& p, Ctrl* c, const Clock& clk, Rin
     ok = wait_flag(B.plan_flag, p.epoch, clk, TK_PERM, 0);
     if (!ok) break;
     const int n_chunks = ld_acquire(&B.meta[0]);
-    if (in(TK_PERM))
+    if (in(TK_PERM) && !p.direct)
       for (int i = cta; i < p.nbp * p.PP && ok; i += G)
         ok = rw.emit(make_task(TK_PERM, blk, i / p.PP, i % p.PP), clk);
     if (routing_only) continue;
@@ -1704,9 +1847,9 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
   if (w == kWarpSched) {
     if (lane_id() == 0) {
       RingWriter rw{c, 0};
-      if (p.dense && blockIdx.x == 0) {
-        // Re-arm the other parity's queue for the next call (the routing
-        // scan does this in the MoE layer).
+      if (blockIdx.x == 0) {
+        // Re-arm the other parity's queue for the next call: the call before
+        // this one, which used it, has completed.
         const int other = (p.epoch + 1) & 1;
         *p.ws.qhead[other] = 0;
         *p.ws.qtail[other] = 0;
