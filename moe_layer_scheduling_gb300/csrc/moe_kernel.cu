@@ -286,7 +286,7 @@ __device__ void task_norm(const MegaParams& p, const Task& t, int wt) {
 // token, k rounds of a warp arg-max, ties to the lower expert id; weights the
 // softmax over the k selected logits.  Counts the experts in s_cnt.
 __device__ void topk_rows_warp(const MegaParams& p, const BlockWs& B, const float* s_log, int tok0,
-                               int* s_cnt, int ww, int lane) {
+                               int* s_cnt, int ww, int lane, int* s_sel_ids, float* s_sel_w) {
   const int E = p.E, k = p.k;
   for (int r = ww; r < kTB; r += 8) {
     const int tok = tok0 + r;
@@ -332,6 +332,8 @@ __device__ void topk_rows_warp(const MegaParams& p, const BlockWs& B, const floa
     if (lane < k) {
       B.ids[tok * k + lane] = my_id;
       B.wts[tok * k + lane] = ex / z;
+      s_sel_ids[r * k + lane] = my_id;
+      s_sel_w[r * k + lane] = ex / z;
       atomicAdd(&s_cnt[my_id], 1);
     }
   }
@@ -339,41 +341,53 @@ __device__ void topk_rows_warp(const MegaParams& p, const BlockWs& B, const floa
 
 
 // Top-k of the tokens tok0.. of a block whose fp32 logits (bias included) are
-// in s_log [kTB][E].  Blocks of at most kTopkRankMax tokens (decode-sized
-// calls, where this task is on the critical path) use all 256 workers at
-// once: each (token, expert) pair counts the experts ahead of it in the order
-// (logit descending, expert id ascending); those of rank < k are the
-// selection, in rank order, so ties go to the lower expert id.  Larger blocks
-// take the warp arg-max above (the same selection).  Weights: the softmax over
-// the k selected logits.  Counts the selected experts in s_cnt.  `scr`: 4 KB
-// of scratch.
-constexpr int kTopkRankMax = 8;
+// in s_log [kTB][E].  Blocks of at most kTopkRankMax tokens (where this task
+// is on the critical path of a one-token call) use all 256 workers at once:
+// each (token, expert) pair counts the experts ahead of it in the order
+// (logit descending, expert id ascending), two threads per pair for a single
+// token; those of rank < k are the selection, in rank order, so ties go to the
+// lower expert id.  Larger blocks take the warp arg-max above (the same
+// selection; its cost grows with k, not with E * T).  Weights: the softmax
+// over the k selected logits.  Counts the selected experts in s_cnt, and
+// leaves the selection in s_sel_ids / s_sel_w ([kTB][k]).  `scr`: 4 KB of
+// scratch.
+constexpr int kTopkRankMax = 2;
 constexpr int kTopkScratchOff = 18 * 1024;  // offset of the top-k scratch in the SIMT region
-constexpr int kDirectOff = 24 * 1024;       // direct mode: the scan's row tables
+constexpr int kDirectOff = 24 * 1024;       // direct mode: the scan's expert row offsets
+constexpr int kSelBytes = 4 * kTB * kMaxK;  // a block's selected experts (or weights)
+constexpr int kSelOff = kDirectOff + 4 * kMaxE;  // the top-k's selection, kept for the scan
 constexpr int kGatherOff = 16 * 1024;       // direct mode: gate/up activations of all T tokens
 __device__ void topk_rows(const MegaParams& p, const BlockWs& B, const float* s_log, int tok0,
-                          int* s_cnt, int wt, uint8_t* scr) {
+                          int* s_cnt, int wt, uint8_t* scr, int* s_sel_ids, float* s_sel_w) {
   const int E = p.E, k = p.k;
   const int nt = max(0, min(kTB, p.T - tok0));
   if (nt > kTopkRankMax) {
-    topk_rows_warp(p, B, s_log, tok0, s_cnt, wt >> 5, wt & 31);
+    topk_rows_warp(p, B, s_log, tok0, s_cnt, wt >> 5, wt & 31, s_sel_ids, s_sel_w);
     return;
   }
   float* s_v = reinterpret_cast<float*>(scr);                 // [kTB][kMaxK] selected logits by rank
   int* s_i = reinterpret_cast<int*>(scr + 4 * kTB * kMaxK);  // [kTB][kMaxK] selected experts by rank
-  for (int idx = wt; idx < nt * E; idx += kNumWorkers) {
+  const int tpi = nt * E * 2 <= kNumWorkers ? 2 : 1;          // threads per (token, expert) pair
+  const int n_items = nt * E * tpi;
+  // every worker runs every round (whole warps meet at the pair shuffle)
+  for (int base = 0; base < n_items; base += kNumWorkers) {
+    const int it = base + wt;
+    const bool act = it < n_items;
+    const int idx = act ? it / tpi : 0, part = it - (it / tpi) * tpi;
     const int r = idx / E, e = idx - r * E;
     const float* row = s_log + r * E;
     const float v = row[e];
     int rank = 0;
-    for (int f = 0; f < E; f += 4) {
+    const int f_end = act ? (part + 1) * E / tpi : 0;
+    for (int f = part * E / tpi; f < f_end; f += 4) {
       const float4 u = *reinterpret_cast<const float4*>(row + f);
       rank += static_cast<int>(u.x > v) | (static_cast<int>(u.x == v) & static_cast<int>(f < e));
       rank += static_cast<int>(u.y > v) | (static_cast<int>(u.y == v) & static_cast<int>(f + 1 < e));
       rank += static_cast<int>(u.z > v) | (static_cast<int>(u.z == v) & static_cast<int>(f + 2 < e));
       rank += static_cast<int>(u.w > v) | (static_cast<int>(u.w == v) & static_cast<int>(f + 3 < e));
     }
-    if (rank < k) {
+    if (tpi == 2) rank += __shfl_xor_sync(0xffffffffu, rank, 1);  // the pair's two halves
+    if (act && part == 0 && rank < k) {
       s_v[r * kMaxK + rank] = v;
       s_i[r * kMaxK + rank] = e;
     }
@@ -386,8 +400,11 @@ __device__ void topk_rows(const MegaParams& p, const BlockWs& B, const float* s_
     float z = 0.f;
     for (int q = 0; q < k; ++q) z += expf(vr[q] - v0);
     const int e = s_i[r * kMaxK + j], tok = tok0 + r;
+    const float wv = expf(vr[j] - v0) / z;
     B.ids[tok * k + j] = e;
-    B.wts[tok * k + j] = expf(vr[j] - v0) / z;
+    B.wts[tok * k + j] = wv;
+    s_sel_ids[r * k + j] = e;
+    s_sel_w[r * k + j] = wv;
     atomicAdd(&s_cnt[e], 1);
   }
 }
@@ -471,7 +488,8 @@ __device__ void task_router_epilogue(const MegaParams& p, Ctrl* c, uint8_t* simt
       const int r = idx / E;
       if (tok0 + r < p.T) B.logits[static_cast<size_t>(tok0) * E + idx] = s_log[idx];
     }
-    topk_rows(p, B, s_log, tok0, s_cnt, wt, simt + kTopkScratchOff);
+    topk_rows(p, B, s_log, tok0, s_cnt, wt, simt + kTopkScratchOff,
+              reinterpret_cast<int*>(simt + kSelOff), reinterpret_cast<float*>(simt + kSelOff + kSelBytes));
     named_bar(1, kNumWorkers);
     publish_block_counts(p, B, tb, s_cnt, wt);
   }
@@ -491,26 +509,46 @@ __device__ void task_topk(const MegaParams& p, const Task& t, uint8_t* simt, int
   const int tok0 = tb * kTB;
   if (p.logits_in) init_acc_rows(p, blk, tb, wt);  // no router tile ran for this block
   const int ntok = max(0, min(kTB, p.T - tok0));
-  for (int idx = wt; idx < ntok * E; idx += kNumWorkers) {
-    const int r = idx / E, e = idx - r * E, tok = tok0 + r;
-    {
-      const size_t o = static_cast<size_t>(tok) * E + e;
-      float s;
-      if (p.logits_in) {
-        s = __ldg(p.logits_in + o);
-      } else {
-        // written by other CTAs' router tiles: L2-only load
-        const long long v = static_cast<long long>(__ldcg(B.logit_fx + o));
-        B.logit_fx[o] = 0ull;  // consumed: re-armed for the next call
-        s = static_cast<float>(static_cast<double>(v) * 9.094947017729282379e-13);  // 2^-40
-        if (bias) s += __ldg(bias + e);
-      }
+  const size_t o0 = static_cast<size_t>(tok0) * E;
+  const int n = ntok * E;
+  if (p.logits_in) {
+    for (int idx = wt; idx < n; idx += kNumWorkers) {
+      const float s = __ldg(p.logits_in + o0 + idx);
       s_log[idx] = s;
-      B.logits[o] = s;
+      B.logits[o0 + idx] = s;
+    }
+  } else {
+    // Partial sums written by other CTAs' router tiles (L2-only loads), four
+    // per thread in flight before any store.
+    for (int base = wt; base < n; base += 4 * kNumWorkers) {
+      long long v[4];
+      float bi[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = base + u * kNumWorkers;
+        v[u] = 0;
+        bi[u] = 0.f;
+        if (idx < n) {
+          v[u] = static_cast<long long>(__ldcg(B.logit_fx + o0 + idx));
+          if (bias) bi[u] = __ldg(bias + (idx - (idx / E) * E));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = base + u * kNumWorkers;
+        if (idx < n) {
+          float s = static_cast<float>(static_cast<double>(v[u]) * 9.094947017729282379e-13);  // 2^-40
+          if (bias) s += bi[u];
+          B.logit_fx[o0 + idx] = 0ull;  // consumed: re-armed for the next call
+          s_log[idx] = s;
+          B.logits[o0 + idx] = s;
+        }
+      }
     }
   }
   named_bar(1, kNumWorkers);
-  topk_rows(p, B, s_log, tok0, s_cnt, wt, simt + kTopkScratchOff);
+  topk_rows(p, B, s_log, tok0, s_cnt, wt, simt + kTopkScratchOff,
+            reinterpret_cast<int*>(simt + kSelOff), reinterpret_cast<float*>(simt + kSelOff + kSelBytes));
   named_bar(1, kNumWorkers);
   if (tb < p.nb) publish_block_counts(p, B, tb, s_cnt, wt, !p.fuse_scan);
   if (p.fuse_scan) {
@@ -578,10 +616,17 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
     // Direct mode (one token block, no permute task): the expert-sorted row of
     // every slot (t, j) is exp_indptr[e] + the number of earlier slots routed
     // to the same expert (ascending token within an expert).
-    int* s_ids = s_row0 + kMaxE;  // [kTB * kMaxK]
+    // The selection of the call's single token block: still in shared memory
+    // when the top-k task runs the scan itself, else read back.
+    int* s_ids = reinterpret_cast<int*>(simt + kSelOff);                  // [kTB * k]
+    float* s_w = reinterpret_cast<float*>(simt + kSelOff + kSelBytes);   // [kTB * k]
     const int ns = p.T * p.k;
     if (wt < E) s_row0[wt] = row0;
-    for (int i = wt; i < ns; i += kNumWorkers) s_ids[i] = __ldcg(B.ids + i);
+    if (!s_counts)
+      for (int i = wt; i < ns; i += kNumWorkers) {
+        s_ids[i] = __ldcg(B.ids + i);
+        s_w[i] = __ldcg(B.wts + i);
+      }
     named_bar(1, kNumWorkers);
     for (int sl = wt; sl < ns; sl += kNumWorkers) {
       const int e = s_ids[sl];
@@ -590,7 +635,7 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
       const int row = s_row0[e] + rank;
       B.pos[sl] = row;
       B.row_token[row] = sl / p.k;
-      B.row_w[row] = __ldcg(B.wts + sl);
+      B.row_w[row] = s_w[sl];
     }
   }
   if (needs_comb(p, blk)) {
