@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Valid only for the kernel sources it was taken on: reported as null once any
 # of them changes.
 MEGAKERNEL_SOURCES = ("moe_kernel.cu", "moe_api.cu", "etc_internal.h", "etc_event.cuh", "etc_ptx.cuh")
-NCU_TRAFFIC = {"sources_sha256_16": "74c32e2740e875b8", "bytes_per_launch": 1222678528 + 296359936}
+NCU_TRAFFIC = {"sources_sha256_16": "5cf417b7b15a1ade", "bytes_per_launch": 1220105472 + 295447040}
 
 
 def megakernel_source_hash():
@@ -415,6 +415,14 @@ def run_extras(args, dev, weights, gw, wgu, wd, bias, x, out, T, plans, peaks, w
     abl["unfused_per_stage"] = {"us": sec * 1e6, "tflops": T * FLOPS_PER_TOKEN / sec / 1e12}
     for name in ("static", "dynamic", "mixed"):
         abl[name]["vs_unfused"] = abl["unfused_per_stage"]["us"] / abl[name]["us"]
+    # the same static call on CTA-pair tiles, and with the ordered (deterministic) combine
+    for name, kw in (("static_pair_tiles", dict(debug_flags=B.ETC_DEBUG_PAIR_MOE)),
+                     ("static_ordered_combine", dict(combine=B.ETC_COMBINE_ORDERED))):
+        pv = B.etc_moe_plan(H, E, K, I, t_max=T, sched=B.ETC_SCHED_STATIC, router_bias=bias, **kw)
+        sec = time_gpu(lambda: B.etc_moe_forward(pv, x, gw, wgu, wd, T, out), steps, 3, world)
+        assert B.etc_plan_check(pv) == B.ETC_OK, B.etc_last_error()
+        abl[name] = {"us": sec * 1e6, "tflops": T * FLOPS_PER_TOKEN / sec / 1e12}
+        pv.close()
     res["ablation_prefill_T4096"] = abl
 
     # --- decode sizes: 8 rotating weight copies defeat the 129 MB L2 ---
@@ -522,10 +530,12 @@ def run_mlp_rows(dev, tflops_peak, world, names=("MLP-1",)):
         out = torch.empty(S, Hm, device=dev)
         flops = 6.0 * S * Hm * Im
         row = {"S": S, "H": Hm, "I": Im, "gflop": flops / 1e9}
-        for mode, sched, unf in (("static", B.ETC_SCHED_STATIC, False),
-                                 ("dynamic", B.ETC_SCHED_DYNAMIC, False),
-                                 ("unfused_two_launches", B.ETC_SCHED_STATIC, True)):
-            pm = B.etc_mlp_plan(Hm, Im, S, sched=sched)
+        for mode, sched, unf, fl in (("static", B.ETC_SCHED_STATIC, False, 0),
+                                     ("dynamic", B.ETC_SCHED_DYNAMIC, False, 0),
+                                     ("unfused_two_launches", B.ETC_SCHED_STATIC, True, 0),
+                                     ("static_single_cta_tiles", B.ETC_SCHED_STATIC, False,
+                                      B.ETC_DEBUG_NO_PAIR)):
+            pm = B.etc_mlp_plan(Hm, Im, S, sched=sched, debug_flags=fl)
             fn = B.etc_mlp_forward_unfused if unf else B.etc_mlp_forward
             sec = time_gpu(lambda: fn(pm, xd, wgu, wd, S, out), 10, 3, world)
             assert B.etc_plan_check(pm) == B.ETC_OK, B.etc_last_error()
