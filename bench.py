@@ -617,12 +617,13 @@ def run_single(args):
         w, x = inputs.mlp_layer(args.mlp)
         wgu, wd, xd = w.w_gate_up.to(dev), w.w_down.to(dev), x.to(dev)
         out = torch.empty(S, Hm, device=dev)
-        plan = B.etc_mlp_plan(Hm, Im, S, sched=sched)
+        plan = B.etc_mlp_plan(Hm, Im, S, sched=sched,
+                              debug_flags=B.ETC_DEBUG_NO_PAIR if args.tiles == "single" else 0)
         sec = time_gpu(lambda: B.etc_mlp_forward(plan, xd, wgu, wd, S, out), args.steps,
                        args.warmup, 1)
         plan.close()
         return {"workload": f"dense_mlp_{args.mlp}_S{S}_H{Hm}_I{Im}", "sched": args.sched,
-                "us": sec * 1e6, "tflops": 6.0 * S * Hm * Im / sec / 1e12}
+                "tiles": args.tiles, "us": sec * 1e6, "tflops": 6.0 * S * Hm * Im / sec / 1e12}
     if args.workload == "splitk":
         if sched == B.ETC_SCHED_MIXED:
             raise SystemExit("split-K takes static or dynamic scheduling")
@@ -659,6 +660,10 @@ def main():
     ap.add_argument("--mlp", default="MLP-1", help="Table 4 shape for --workload mlp")
     ap.add_argument("--sched", default="static", choices=["static", "dynamic", "mixed"],
                     help="scheduler of the benchmark line (prefill) or of the single workload")
+    ap.add_argument("--tiles", default="default", choices=["default", "single"],
+                    help="--workload mlp: 'single' runs its wide tiles on single CTAs instead of CTA "
+                         "pairs (the form ncu can capture: it cannot launch the pair kernel's "
+                         "cooperative cluster launch)")
     ap.add_argument("--clock-window", type=float, default=1.5,
                     help="seconds of load kept up for the clock record (0 for profiler runs)")
     args = ap.parse_args()
