@@ -234,6 +234,50 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// The same load split in two, so that a load can be in flight while the
+// previous block is processed: issue, then wait.  The wait names the
+// registers as operands, so no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+
+// Transposes the 4 x 4 blocks held by each quad of lanes (lanes 4a..4a+3):
+// on entry lane 4a+j holds v[4g+i] = M[4a+j][4g+i]; on exit it holds
+// v[4g+i] = M[4a+i][4g+j].  Two exchange steps (partner lane ^1, then ^2),
+// each moving the half of the block that sits on the wrong side.
+__device__ __forceinline__ void quad_transpose16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int st = 0; st < 2; ++st) {
+    const int s = 1 << st;  // (a counter that counts by one: constant indices below)
+    const bool hi = (lane & s) != 0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (i & s) continue;
+        const int a = 4 * g + i, b = 4 * g + (i | s);
+        const float got = __shfl_xor_sync(0xffffffffu, hi ? v[a] : v[b], s);
+        if (hi) v[a] = got;
+        else v[b] = got;
+      }
+    }
+  }
+}
+
 // Shared-memory matrix descriptor for a K-major bf16 operand tile stored the
 // way a 128-byte-swizzled TMA box leaves it: rows of 64 elements (128 B),
 // 8-row swizzle atoms of 1024 B stacked along M/N.  The tile base must be

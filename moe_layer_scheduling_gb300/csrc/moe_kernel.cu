@@ -282,7 +282,7 @@ __device__ void task_norm(const MegaParams& p, const Task& t, int wt) {
 // of the block follows.
 // ---------------------------------------------------------------------------
 
-// Top-k by warps (blocks of more than kTopkRankMax tokens): one warp per
+// Top-k by warps (blocks of 3 to 8 tokens): one warp per
 // token, k rounds of a warp arg-max, ties to the lower expert id; weights the
 // softmax over the k selected logits.  Counts the experts in s_cnt.
 __device__ void topk_rows_warp(const MegaParams& p, const BlockWs& B, const float* s_log, int tok0,
@@ -340,27 +340,132 @@ __device__ void topk_rows_warp(const MegaParams& p, const BlockWs& B, const floa
 }
 
 
+// One level of a pairwise arg-max tree over 2W slots: slot i keeps the better
+// of slots i and i + W (logit descending, expert id ascending).
+template <int W>
+__device__ __forceinline__ void tree_level(float (&cv)[kMaxE / 8], int (&ci)[kMaxE / 8]) {
+#pragma unroll
+  for (int i = 0; i < W; ++i) {
+    if (cv[i + W] > cv[i] || (cv[i + W] == cv[i] && ci[i + W] < ci[i])) {
+      cv[i] = cv[i + W];
+      ci[i] = ci[i + W];
+    }
+  }
+}
+
+// Top-k by groups of eight threads (blocks of more than 8 tokens):
+// the 256 workers hold 32 tokens, thread `sub` of a token's group the logits
+// of experts sub, sub + 8, sub + 16, ... (E is a multiple of 8).  k rounds of
+// an arg-max over the group (ties to the lower expert id) give the selection
+// in rank order; weights: the softmax over the k selected logits.  Counts
+// the experts in s_cnt; `logits_out`: also stores the block's logits.
+__device__ void topk_rows_group(const MegaParams& p, const BlockWs& B, const float* s_log, int tok0,
+                                int nt, int* s_cnt, int wt, int* s_sel_ids, float* s_sel_w,
+                                bool logits_out) {
+  const int E = p.E, k = p.k, per = E >> 3;
+  const int r = wt >> 3, sub = wt & 7;
+  const bool live = r < nt;
+  float v[kMaxE / 8];
+#pragma unroll
+  for (int i = 0; i < kMaxE / 8; ++i) v[i] = live && i < per ? s_log[r * E + 8 * i + sub] : -INFINITY;
+  if (live && logits_out) {
+    float* lrow = B.logits + static_cast<size_t>(tok0 + r) * E;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 8; ++i)
+      if (i < per) lrow[8 * i + sub] = v[i];
+  }
+  unsigned taken = per >= 32 ? 0u : ~0u << per;  // slots past E count as taken
+  float v0 = 0.f, sv0 = 0.f, sv1 = 0.f;
+  int si0 = 0, si1 = 0;
+  for (int j = 0; j < k; ++j) {
+    // this thread's best untaken expert: a pairwise tree (depth 4), taken slots
+    // entering as (-inf, no id), which any real entry beats
+    float cv[kMaxE / 8];
+    int ci[kMaxE / 8];
+#pragma unroll
+    for (int i = 0; i < kMaxE / 8; ++i) {
+      const bool tk = (taken >> i) & 1u;
+      cv[i] = tk ? -INFINITY : v[i];
+      ci[i] = tk ? 0x7fffffff : 8 * i + sub;
+    }
+    tree_level<8>(cv, ci);
+    tree_level<4>(cv, ci);
+    tree_level<2>(cv, ci);
+    tree_level<1>(cv, ci);
+    float bv = cv[0];
+    int bi = ci[0];
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 7) == sub && bi < E) taken |= 1u << (bi >> 3);
+    if (j == 0) v0 = bv;
+    if (j == sub) { sv0 = bv; si0 = bi; }
+    if (j == sub + 8) { sv1 = bv; si1 = bi; }
+  }
+  const float ex0 = sub < k ? expf(sv0 - v0) : 0.f;
+  const float ex1 = sub + 8 < k ? expf(sv1 - v0) : 0.f;
+  float z = ex0 + ex1;
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  if (live) {
+    const int tok = tok0 + r;
+    if (sub < k) {
+      const float wv = ex0 / z;
+      B.ids[tok * k + sub] = si0;
+      B.wts[tok * k + sub] = wv;
+      s_sel_ids[r * k + sub] = si0;
+      s_sel_w[r * k + sub] = wv;
+      atomicAdd(&s_cnt[si0], 1);
+    }
+    if (sub + 8 < k) {
+      const float wv = ex1 / z;
+      B.ids[tok * k + sub + 8] = si1;
+      B.wts[tok * k + sub + 8] = wv;
+      s_sel_ids[r * k + sub + 8] = si1;
+      s_sel_w[r * k + sub + 8] = wv;
+      atomicAdd(&s_cnt[si1], 1);
+    }
+  }
+}
+
+
 // Top-k of the tokens tok0.. of a block whose fp32 logits (bias included) are
 // in s_log [kTB][E].  Blocks of at most kTopkRankMax tokens (where this task
 // is on the critical path of a one-token call) use all 256 workers at once:
 // each (token, expert) pair counts the experts ahead of it in the order
 // (logit descending, expert id ascending), two threads per pair for a single
 // token; those of rank < k are the selection, in rank order, so ties go to the
-// lower expert id.  Larger blocks take the warp arg-max above (the same
-// selection; its cost grows with k, not with E * T).  Weights: the softmax
+// lower expert id.  Blocks of up to kTopkWarpMax tokens take the warp arg-max,
+// larger ones the group arg-max above (the same selection; their cost grows
+// with k, not with E * T).  Weights: the softmax
 // over the k selected logits.  Counts the selected experts in s_cnt, and
 // leaves the selection in s_sel_ids / s_sel_w ([kTB][k]).  `scr`: 4 KB of
-// scratch.
+// scratch.  `logits_out`: also stores the block's logits (router tiles with
+// H whole).
 constexpr int kTopkRankMax = 2;
+constexpr int kTopkWarpMax = 8;
 constexpr int kTopkScratchOff = 18 * 1024;  // offset of the top-k scratch in the SIMT region
 constexpr int kDirectOff = 24 * 1024;       // direct mode: the scan's expert row offsets
 constexpr int kSelBytes = 4 * kTB * kMaxK;  // a block's selected experts (or weights)
 constexpr int kSelOff = kDirectOff + 4 * kMaxE;  // the top-k's selection, kept for the scan
 constexpr int kGatherOff = 16 * 1024;       // direct mode: gate/up activations of all T tokens
 __device__ void topk_rows(const MegaParams& p, const BlockWs& B, const float* s_log, int tok0,
-                          int* s_cnt, int wt, uint8_t* scr, int* s_sel_ids, float* s_sel_w) {
+                          int* s_cnt, int wt, uint8_t* scr, int* s_sel_ids, float* s_sel_w,
+                          bool logits_out = false) {
   const int E = p.E, k = p.k;
   const int nt = max(0, min(kTB, p.T - tok0));
+  if (nt > kTopkWarpMax) {
+    topk_rows_group(p, B, s_log, tok0, nt, s_cnt, wt, s_sel_ids, s_sel_w, logits_out);
+    return;
+  }
+  if (logits_out)
+    for (int idx = wt; idx < nt * E; idx += kNumWorkers) B.logits[static_cast<size_t>(tok0) * E + idx] = s_log[idx];
   if (nt > kTopkRankMax) {
     topk_rows_warp(p, B, s_log, tok0, s_cnt, wt >> 5, wt & 31, s_sel_ids, s_sel_w);
     return;
@@ -484,12 +589,9 @@ __device__ void task_router_epilogue(const MegaParams& p, Ctrl* c, uint8_t* simt
   if (wt == 0) release_acc<PAIR>(c, acc);  // accumulator free for the next tile
   if (ok && p.NC == 1 && tb < p.nb) {
     const int tok0 = tb * kTB;
-    for (int idx = wt; idx < kTB * E; idx += kNumWorkers) {
-      const int r = idx / E;
-      if (tok0 + r < p.T) B.logits[static_cast<size_t>(tok0) * E + idx] = s_log[idx];
-    }
     topk_rows(p, B, s_log, tok0, s_cnt, wt, simt + kTopkScratchOff,
-              reinterpret_cast<int*>(simt + kSelOff), reinterpret_cast<float*>(simt + kSelOff + kSelBytes));
+              reinterpret_cast<int*>(simt + kSelOff), reinterpret_cast<float*>(simt + kSelOff + kSelBytes),
+              /*logits_out=*/true);
     named_bar(1, kNumWorkers);
     publish_block_counts(p, B, tb, s_cnt, wt);
   }
@@ -741,12 +843,14 @@ __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* 
                           uint32_t& li, const Clock& clk) {
   const int blk = t.blk, tb = my_tb(p, t.a), part = t.b;
   const BlockWs& B = p.ws.blk[blk];
-  const int E = p.E, k = p.k, ww = wt >> 5, lane = wt & 31;
+  const int E = p.E, k = p.k;
   int* s_run = reinterpret_cast<int*>(simt);
   int* s_slot = s_run + kMaxE;
   int* s_ids = s_slot + kTB * kMaxK;
   int* s_part = s_ids + kTB * kMaxK;  // [kNumWorkers]
   int* s_pcnt = s_part + kNumWorkers; // [E]
+  unsigned* s_mask = reinterpret_cast<unsigned*>(s_pcnt + kMaxE);  // [E] tokens of the block per expert
+  static_assert(kTB <= 32, "a token block's tokens form one 32-bit mask");
   uint8_t* rows = simt + kPermRowOff;
   const int t0 = tb * kTB, ntok = max(0, min(kTB, p.T - t0));  // (odd CTA of the last pair block: none)
   const int TP = kTB / p.PP, r_lo = min(ntok, part * TP), r_hi = min(ntok, r_lo + TP);
@@ -764,40 +868,46 @@ __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* 
   // First row of each expert in this block: exp_indptr[e] plus the rows of e
   // in the blocks before tb, summed from the block histograms by `per`
   // threads per expert.
+  // (16 loads in flight per thread).
   const int per = kNumWorkers / E;
   {
     const int e = wt % E, q = wt / E;
     int sum = 0;
     if (q < per) {
-#pragma unroll 4
-      for (int b = q; b < tb; b += per) sum += __ldcg(B.blk_cnt + b * E + e);
+      for (int b0 = q; b0 < tb; b0 += 16 * per) {
+        int x[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int b = b0 + u * per;
+          x[u] = b < tb ? __ldcg(B.blk_cnt + b * E + e) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) sum += x[u];
+      }
     }
     s_part[wt] = sum;
   }
   for (int i = wt; i < r_hi * k; i += kNumWorkers) s_ids[i] = __ldcg(B.ids + t0 * k + i);
-  for (int i = wt; i < E; i += kNumWorkers) s_pcnt[i] = 0;
+  for (int i = wt; i < E; i += kNumWorkers) s_mask[i] = 0u;
   named_bar(1, kNumWorkers);
   for (int e = wt; e < E; e += kNumWorkers) {
     int run = __ldcg(B.exp_indptr + e);
     for (int j = 0; j < per; ++j) run += s_part[j * E + e];
     s_run[e] = run;
   }
+  // The block's tokens (up to this part's end) of each expert, as a bit mask
+  // (a token block has 32 tokens; one token's k experts are distinct).
+  for (int i = wt; i < r_hi * k; i += kNumWorkers) atomicOr(&s_mask[s_ids[i]], 1u << (i / k));
   named_bar(1, kNumWorkers);
-  if (ww == 0) {
-    // Ranks in ascending token order over the block's tokens up to this
-    // part's end; one token's k experts are distinct.
-    for (int r = 0; r < r_hi; ++r) {
-      if (lane < k) {
-        const int e = s_ids[r * k + lane];
-        const int row = s_run[e];
-        s_run[e] = row + 1;
-        if (r >= r_lo) {
-          s_slot[r * k + lane] = row;
-          s_pcnt[e] += 1;
-        }
-      }
-      __syncwarp();
-    }
+  // Rank of slot (r, j) among the block's rows of its expert: the block's
+  // tokens before r that chose the same expert (ascending token order).
+  for (int i = r_lo * k + wt; i < r_hi * k; i += kNumWorkers) {
+    const int e = s_ids[i], r = i / k;
+    s_slot[i] = s_run[e] + __popc(s_mask[e] & ((1u << r) - 1u));
+  }
+  {
+    const unsigned part_bits = (r_hi >= 32 ? ~0u : (1u << r_hi) - 1u) & ~((1u << r_lo) - 1u);
+    for (int e = wt; e < E; e += kNumWorkers) s_pcnt[e] = __popc(s_mask[e] & part_bits);
   }
   named_bar(1, kNumWorkers);
   for (int i = r_lo * k + wt; i < r_hi * k; i += kNumWorkers) {
@@ -915,6 +1025,17 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
   const uint32_t aph = (gemm_i >> 1) & 1;
   ++gemm_i;
   int* flag = &c->wflag[iter & 1];
+  const BlockWs& B = p.ws.blk[t.blk];
+  // Down tiles: each chunk row's token and routing weight, for the combine,
+  // read while the tile is still on the tensor cores.
+  int* s_rtok = reinterpret_cast<int*>(simt + 2 * kEpiHalfBytes);                 // [256]
+  float* s_rw = reinterpret_cast<float*>(simt + 2 * kEpiHalfBytes + 4 * kBT2);    // [256]
+  const bool fused_comb = t.type == TK_DN && !p.dense && !p.ordered;
+  if (fused_comb)
+    for (int r = wt; r < t.rows; r += kNumWorkers) {
+      s_rtok[r] = __ldcg(B.row_token + t.row0 + r);
+      s_rw[r] = __ldcg(B.row_w + t.row0 + r);
+    }
   if (wt == 0) *flag = mbar_wait(&c->tfull[acc], aph, clk, 230, PAIR) ? 1 : 0;
   named_bar(1, kNumWorkers);
   const bool ok = *flag != 0;
@@ -925,20 +1046,9 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
   __nv_bfloat16* S = reinterpret_cast<__nv_bfloat16*>(epi + h * kEpiHalfBytes + 4096);  // [16][128]
   const uint32_t tbase = c->tmem_base + acc * kAccCols + (static_cast<uint32_t>(32 * q) << 16);
   const int ncb = (t.rows + 15) >> 4;
-  const BlockWs& B = p.ws.blk[t.blk];
-  // Down tiles: each chunk row's token and routing weight, for the combine.
-  int* s_rtok = reinterpret_cast<int*>(simt + 2 * kEpiHalfBytes);                 // [256]
-  float* s_rw = reinterpret_cast<float*>(simt + 2 * kEpiHalfBytes + 4 * kBT2);    // [256]
   // Pair tiles: this CTA's 64 intermediate columns (gate/up) or 128 output
   // columns (down) of the pair's tile; the accumulator holds all chunk rows.
   const int rank = pair_rank(p);
-  if (t.type == TK_DN && !p.dense) {
-    for (int r = wt; r < t.rows; r += kNumWorkers) {
-      s_rtok[r] = __ldcg(B.row_token + t.row0 + r);
-      s_rw[r] = __ldcg(B.row_w + t.row0 + r);
-    }
-    named_bar(1, kNumWorkers);
-  }
   if (ok) {
     if (t.type == TK_GU && p.wide) {
       // Wide: gate rows in the buffer's first half, up rows in its second;
@@ -1024,30 +1134,45 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
         named_bar(2 + h, 128);
       }
     } else {
-      // Weighted combine fused here: out[token] += w * y, 4 columns per red op
-      // (wide tiles: two 128-column halves, one per accumulator half).  The
-      // dense MLP's tile owns its outputs and stores them.
-      float* S32 = reinterpret_cast<float*>(epi + h * kEpiHalfBytes);  // [16][128] fp32
+      // Down tile: TMEM lane = output column, TMEM column = chunk row.  Each
+      // quad of lanes transposes its 4 x 4 blocks in registers, so that a
+      // lane holds 4 consecutive output columns of one row and one warp
+      // instruction writes 4 rows x 128 bytes; no shared-memory staging.
+      // The two worker halves take alternate 16-row blocks (wide tiles: of
+      // both 128-column halves of the accumulator); the next block's TMEM
+      // load is in flight while one is written.  Weighted combine fused
+      // here: out[token] += w * y (fp32 reductions).  The ordered combine
+      // stores y; the dense MLP's tile owns its output rows and stores them.
       const int nhalf = p.wide ? 2 : 1;
-      for (int hc = 0; hc < nhalf * ncb; ++hc) {
-        const int half = hc / ncb, cb = hc - half * ncb;
-        if ((cb & 1) != h) continue;  // the two worker halves take alternate column blocks
-        const int col0 = p.pair ? t.b * kDnRowsW + kDnRows * rank
-                                : t.b * (p.wide ? kDnRowsW : kDnRows) + half * 128;
-        float* accr = p.dense ? nullptr : acc_rows(p, t.blk) + col0;
+      const int nmy = (ncb - h + 1) >> 1, nblk = nhalf * nmy;
+      const int cq = 32 * q + 4 * (lane >> 2), rq = lane & 3;
+      float* accr = fused_comb ? acc_rows(p, t.blk) : nullptr;
+      auto taddr = [&](int b) {
+        const int hf = b / nmy;
+        return tbase + hf * (kAccCols / 2) + (h + 2 * (b - hf * nmy)) * 16;
+      };
+      auto put = [&](uint32_t(&r)[16], int b) {
+        const int hf = b / nmy, cb = h + 2 * (b - hf * nmy);
+        const int col = (p.pair ? t.b * kDnRowsW + kDnRows * rank
+                                : t.b * (p.wide ? kDnRowsW : kDnRows) + hf * 128) + cq;
         float v[16];
-        tmem_ld16(tbase + half * (kAccCols / 2) + cb * 16, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) S32[i * 128 + 32 * q + lane] = v[i];
-        named_bar(2 + h, 128);
-        if (p.dense) {
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+        quad_transpose16(v, lane);
 #pragma unroll
-          for (int rep = 0; rep < 4; ++rep) {
-            const int idx = i128 + 128 * rep;
-            const int r = cb * 16 + (idx >> 5), chunk = idx & 31;
-            if (r < t.rows) {
-              const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
-              const size_t o = static_cast<size_t>(t.row0 + r) * p.H + col0 + chunk * 4;
+        for (int g = 0; g < 4; ++g) {
+          const int rr = cb * 16 + 4 * g + rq;
+          if (rr < t.rows) {
+            const float4 val = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+            if (fused_comb) {
+              const float wr = s_rw[rr];
+              red_add_v4(accr + static_cast<size_t>(s_rtok[rr]) * p.H + col,
+                         make_float4(wr * val.x, wr * val.y, wr * val.z, wr * val.w));
+            } else if (p.ordered) {
+              // ordered combine: the expert row y itself, in expert-sorted order
+              *reinterpret_cast<float4*>(p.ws.yperm + static_cast<size_t>(t.row0 + rr) * p.H + col) = val;
+            } else {
+              const size_t o = static_cast<size_t>(t.row0 + rr) * p.H + col;
               if (p.out_bf16) {
                 const __nv_bfloat162 lo = __floats2bfloat162_rn(val.x, val.y);
                 const __nv_bfloat162 hi = __floats2bfloat162_rn(val.z, val.w);
@@ -1060,31 +1185,19 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
               }
             }
           }
-        } else if (p.ordered) {
-          // ordered combine: the expert row y itself, in expert-sorted order
-#pragma unroll
-          for (int rep = 0; rep < 4; ++rep) {
-            const int idx = i128 + 128 * rep;
-            const int r = cb * 16 + (idx >> 5), chunk = idx & 31;
-            if (r < t.rows)
-              *reinterpret_cast<float4*>(p.ws.yperm + static_cast<size_t>(t.row0 + r) * p.H + col0 +
-                                         chunk * 4) =
-                  *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
-          }
-        } else {
-#pragma unroll
-          for (int rep = 0; rep < 4; ++rep) {
-            const int idx = i128 + 128 * rep;
-            const int r = cb * 16 + (idx >> 5), chunk = idx & 31;
-            if (r < t.rows) {
-              const float4 val = *reinterpret_cast<const float4*>(S32 + (idx >> 5) * 128 + chunk * 4);
-              const float wr = s_rw[r];
-              red_add_v4(accr + static_cast<size_t>(s_rtok[r]) * p.H + chunk * 4,
-                         make_float4(wr * val.x, wr * val.y, wr * val.z, wr * val.w));
-            }
-          }
         }
-        named_bar(2 + h, 128);
+      };
+      uint32_t ra[16], rb[16];
+      if (nblk > 0) tmem_ld16_issue(taddr(0), ra);
+      for (int b = 0; b < nblk; b += 2) {
+        tmem_ld_wait(ra);
+        if (b + 1 < nblk) tmem_ld16_issue(taddr(b + 1), rb);
+        put(ra, b);
+        if (b + 1 < nblk) {
+          tmem_ld_wait(rb);
+          if (b + 2 < nblk) tmem_ld16_issue(taddr(b + 2), ra);
+          put(rb, b + 1);
+        }
       }
     }
   }

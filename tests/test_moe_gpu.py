@@ -181,16 +181,22 @@ def test_run_to_run_difference_is_bounded(qwen, qwen_dev):
         assert np.max(np.abs(o.astype(np.float64) - outs[0])) <= scale
 
 
-def test_route_from_logits_bit_exact(oracle_lib):
+@pytest.mark.parametrize("T,E,k", [(300, 64, 6), (1, 128, 8), (2, 128, 8), (5, 128, 8), (8, 128, 8),
+                                   (34, 128, 8), (37, 8, 2), (70, 128, 16), (41, 8, 8)])
+def test_route_from_logits_bit_exact(oracle_lib, T, E, k):
     # Identical fp32 logits on both sides, with deliberate exact ties: ids,
     # counts, exp_indptr and the permutation must match bit for bit, and
-    # x_perm must hold the routed rows.
-    T, E, k, H = 300, 64, 6, 256
-    rng = np.random.default_rng(5)
+    # x_perm must hold the routed rows.  Token blocks of 1-2, 3-8 and more
+    # tokens take the three top-k methods (rank count, warp, thread groups).
+    H = 256
+    rng = np.random.default_rng(5 + T)
     L = rng.integers(-8, 8, size=(T, E)).astype(np.float32) * 0.25  # many ties
-    L[7] = 0.0  # a token whose logits are all equal
-    L[8, :] = -0.0
-    L[8, 3] = 0.0
+    if T > 8:
+        L[7] = 0.0  # a token whose logits are all equal
+        L[8, :] = -0.0
+        L[8, 3] = 0.0
+    else:
+        L[0] = 0.0
     x = inputs.tokens(T, H, 6)
     plan = B.etc_moe_plan(H, E, k, 128, t_max=T)
     B.etc_moe_route_from_logits(plan, torch.from_numpy(L).cuda(), x.cuda(), T)
@@ -203,7 +209,7 @@ def test_route_from_logits_bit_exact(oracle_lib):
     assert np.array_equal(r["logits"], L)
     check_dispatch_vs_oracle(r, oracle_lib, ids_ref, E)
     assert np.allclose(r["w"], w_ref, atol=1e-6, rtol=0)
-    assert r["ids"][7].tolist() == list(range(k))
+    assert r["ids"][7 if T > 8 else 0].tolist() == list(range(k))
     xp = torch.empty(T * k, H, dtype=torch.bfloat16, device="cuda")
     B.etc_moe_debug_buffer(plan, 0, xp)
     torch.cuda.synchronize()
