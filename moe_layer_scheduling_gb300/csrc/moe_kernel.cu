@@ -165,11 +165,17 @@ __device__ __forceinline__ StageGeom stage_geom(const MegaParams& p) {
                   : StageGeom{kStagesNarrow, kOpABytes + kStageBBytes, kOpABytes};
 }
 
+// K blocks of a router tile per operand stage: two when the stage holds two
+// (weights 16 KB + 32 token rows 4 KB per K block: the wide geometry).
+__device__ __forceinline__ int router_kpack(const StageGeom& g) {
+  return (g.boff >= 2 * kOpABytes && g.bytes - g.boff >= 2 * kTB * kBK * 2) ? 2 : 1;
+}
+
 // Eight consecutive values of block blk's input row `tok` (columns 8c..8c+7):
 // the caller's bf16 x for block 0, the fp32 residual stream after that.
 __device__ __forceinline__ void load_block_input8(const MegaParams& p, int blk, int tok, int c,
                                                   float (&f)[8]);
-__device__ void init_acc_rows(const MegaParams& p, int blk, int tb, int wt);
+__device__ void init_acc_rows(const MegaParams& p, int blk, int tb, int wt, uint8_t* zbuf = nullptr);
 __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
                            const int* s_counts = nullptr);
 
@@ -455,6 +461,10 @@ constexpr int kDirectOff = 24 * 1024;       // direct mode: the scan's expert ro
 constexpr int kSelBytes = 4 * kTB * kMaxK;  // a block's selected experts (or weights)
 constexpr int kSelOff = kDirectOff + 4 * kMaxE;  // the top-k's selection, kept for the scan
 constexpr int kGatherOff = 16 * 1024;       // direct mode: gate/up activations of all T tokens
+constexpr int kZeroOff = 30 * 1024;         // router tiles: zeros for the block's output rows
+constexpr int kZeroBytes = 2 * 1024;
+static_assert(kSelOff + 2 * kSelBytes <= kZeroOff && kZeroOff + kZeroBytes <= kSimtBytes,
+              "SIMT scratch layout");
 __device__ void topk_rows(const MegaParams& p, const BlockWs& B, const float* s_log, int tok0,
                           int* s_cnt, int wt, uint8_t* scr, int* s_sel_ids, float* s_sel_w,
                           bool logits_out = false) {
@@ -548,7 +558,8 @@ __device__ void task_router_epilogue(const MegaParams& p, Ctrl* c, uint8_t* simt
   ++gemm_i;
   const int tb = my_tb(p, t.a);
   // While the tile is still on the tensor cores: the block's combine rows.
-  if (t.b == 0) init_acc_rows(p, t.blk, tb, wt);
+  const bool zero_rows = t.b == 0;
+  if (zero_rows) init_acc_rows(p, t.blk, tb, wt, simt + kZeroOff);
   int* flag = &c->wflag[iter & 1];
   if (wt == 0) *flag = mbar_wait(&c->tfull[acc], aph, clk, 231, PAIR) ? 1 : 0;
   named_bar(1, kNumWorkers);
@@ -594,6 +605,10 @@ __device__ void task_router_epilogue(const MegaParams& p, Ctrl* c, uint8_t* simt
               /*logits_out=*/true);
     named_bar(1, kNumWorkers);
     publish_block_counts(p, B, tb, s_cnt, wt);
+  }
+  if (zero_rows && wt == 0) {
+    bulk_wait_all();             // the zeroed rows are written
+    fence_proxy_async_global();  // before any down tile adds into them
   }
   named_bar(1, kNumWorkers);  // notify: ev_route, or ev_rblk[tb] with H split (notifier warp)
 }
@@ -816,10 +831,27 @@ __device__ __forceinline__ float* acc_rows(const MegaParams& p, int blk) {
 // chain) before any down tile adds into them.  Run by the block's routing
 // task, which every down tile of the block follows.  (A routing-only call
 // has no output rows.)
-__device__ void init_acc_rows(const MegaParams& p, int blk, int tb, int wt) {
+__device__ void init_acc_rows(const MegaParams& p, int blk, int tb, int wt, uint8_t* zbuf) {
   float* accr = acc_rows(p, blk);
   if (accr == nullptr || p.ordered) return;  // (ordered combine: the finaliser writes whole rows)
   const int ww = wt >> 5, lane = wt & 31, n8 = p.H / 8, t0 = tb * kTB, ntok = min(kTB, p.T - t0);
+  if (zbuf != nullptr && !p.use_norm) {
+    // Zeros, written by the bulk-copy engine from kZeroBytes of zeroed shared
+    // memory (worker thread 0 issues the copies and waits for them before the
+    // task's notify): the workers go on to the tile's epilogue at once.
+    for (int i = wt; i < kZeroBytes / 16; i += kNumWorkers)
+      reinterpret_cast<uint4*>(zbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();  // visible to the bulk-copy engine
+    named_bar(1, kNumWorkers);
+    if (wt == 0 && ntok > 0) {
+      uint8_t* dst = reinterpret_cast<uint8_t*>(accr + static_cast<size_t>(t0) * p.H);
+      const uint32_t total = static_cast<uint32_t>(ntok) * static_cast<uint32_t>(p.H) * 4u;
+      for (uint32_t off = 0; off < total; off += kZeroBytes)
+        bulk_store(dst + off, zbuf, min(static_cast<uint32_t>(kZeroBytes), total - off));
+      bulk_commit();
+    }
+    return;
+  }
   for (int r = ww; r < ntok; r += 8) {
     const int tok = t0 + r;
     float4* d = reinterpret_cast<float4*>(accr + static_cast<size_t>(tok) * p.H);
@@ -1558,20 +1590,28 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
       // experts 0-63 and 64-127 (two MN-major boxes; experts >= E read as
       // zero) and the block's 32 input rows (the lo part second in the chain).
       // Pair tiles: both CTAs load the router weight, each its own 32 rows.
+      // Stages large enough for two K blocks (wide geometry) take two: twice
+      // the bytes in flight for a tile whose weight operand is the same
+      // 512 KB for every token block.
       const int KB = p.KBr * (p.use_norm ? 2 : 1);
       const uint32_t bytes = kOpABytes + kTB * kBK * 2;  // two 64-expert boxes + 32 token rows
+      const int per = router_kpack(g);
       const int tok0 = my_tb(p, t.a) * kTB;
       fence_proxy_async_global();
-      for (int kb = 0; kb < KB; ++kb, st = st + 1 == g.n ? (ph ^= 1, 0) : st + 1) {
+      for (int kb0 = 0; kb0 < KB; kb0 += per, st = st + 1 == g.n ? (ph ^= 1, 0) : st + 1) {
         const int s = st;
         if (!mbar_wait(&c->empty[s], ph ^ 1, clk, 222, pair)) return;
         uint8_t* sa = base + s * g.bytes;
-        const int part = kb >= p.KBr ? 1 : 0;
-        const int h = t.b * p.HC + (kb - part * p.KBr) * kBK;
-        if (announce) mbar_arrive_expect_tx(&c->full[s], bytes * tx_mul);
-        load(sa, &p.tm_wg[t.blk], s, 0, h);
-        load(sa + kOpABytes / 2, &p.tm_wg[t.blk], s, 64, h);
-        load(sa + g.boff, part ? &p.tm_xrlo : &p.tm_xr, s, h, tok0);
+        const int nk = min(per, KB - kb0);
+        if (announce) mbar_arrive_expect_tx(&c->full[s], nk * bytes * tx_mul);
+        for (int u = 0; u < nk; ++u) {
+          const int kb = kb0 + u;
+          const int part = kb >= p.KBr ? 1 : 0;
+          const int h = t.b * p.HC + (kb - part * p.KBr) * kBK;
+          load(sa + u * kOpABytes, &p.tm_wg[t.blk], s, 0, h);
+          load(sa + u * kOpABytes + kOpABytes / 2, &p.tm_wg[t.blk], s, 64, h);
+          load(sa + g.boff + u * (kTB * kBK * 2), part ? &p.tm_xrlo : &p.tm_xr, s, h, tok0);
+        }
       }
       continue;
     }
@@ -1657,7 +1697,8 @@ __device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock
     // Router tiles read A (the router weight) MN-major; expert tiles K-major.
     const uint32_t idesc = rt ? idesc_bf16_f32_amn(M, npad) : idesc_bf16_f32(M, npad);
     const int KB = rt ? p.KBr * (p.use_norm ? 2 : 1) : (t.type == TK_GU ? p.H : p.I) / kBK;
-    for (int kb = 0; kb < KB; ++kb, st = st + 1 == g.n ? (ph ^= 1, 0) : st + 1) {
+    const int per = rt ? router_kpack(g) : 1;  // K blocks per stage
+    for (int kb = 0; kb < KB; kb += per, st = st + 1 == g.n ? (ph ^= 1, 0) : st + 1) {
       const int s = st;
       if (!mbar_wait(&c->full[s], ph, clk, 242, pair)) return;
       tc_fence_after();
@@ -1673,11 +1714,16 @@ __device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock
         umma_commit_pair(&c->empty[s]);  // both CTAs' stages free once these MMAs have read them
         continue;
       } else if (rt) {
-        // 16 K rows per MMA: 2 KB further into each 64-expert box.
-        const uint64_t ad = desc_mnmajor_sw128(sa, kOpABytes / 2);
+        // 16 K rows per MMA: 2 KB further into each 64-expert box; the
+        // stage's second K block (if any) 16 KB (weight) and 4 KB (tokens) on.
+        const int nk = min(per, KB - kb);
+        for (int u = 0; u < nk; ++u) {
+          const uint64_t ad = desc_mnmajor_sw128(sa + u * kOpABytes, kOpABytes / 2);
+          const uint64_t bdu = desc_kmajor_sw128(sa + g.boff + u * (kTB * kBK * 2));
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          umma_bf16(d, ad + kk * (2048 >> 4), bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16(d, ad + kk * (2048 >> 4), bdu + 2 * kk, idesc, (kb | u | kk) != 0 ? 1u : 0u);
+        }
       } else {
         const uint64_t ad = desc_kmajor_sw128(sa);
 #pragma unroll
