@@ -77,6 +77,10 @@ typedef enum { ETC_SCHED_STATIC = 0, ETC_SCHED_DYNAMIC = 1, ETC_SCHED_MIXED = 2 
 #define ETC_DEBUG_PAIR_MOE 0x10u        /* run the wide expert tiles of MoE calls on CTA pairs too
                                            (by default only the dense MLP uses them: on the MoE
                                            layer's skewed chunks they measured no faster) */
+#define ETC_DEBUG_NO_HEAVY 0x20u        /* never run an expert over all T rows of x (by default, in
+                                           dynamic and mixed scheduling, an expert that >= 85 % of a
+                                           large call's tokens chose does, its tiles needing no
+                                           permuted rows; ablation) */
 
 typedef struct etc_plan_s* etc_plan_t;
 

@@ -26,6 +26,7 @@ ETC_DEBUG_FAULT_EXTRA_WAIT = 0x1
 ETC_DEBUG_POISON = 0x2
 ETC_DEBUG_NO_PAIR = 0x8
 ETC_DEBUG_PAIR_MOE = 0x10
+ETC_DEBUG_NO_HEAVY = 0x20
 ETC_OUT_F32 = 0
 ETC_OUT_BF16 = 1
 ETC_COMBINE_FUSED = 0

@@ -23,6 +23,7 @@ constexpr int kStagesNarrow = 6;
 constexpr int kRing = 8;            // smem task ring depth
 constexpr int kTB = 32;             // tokens per router/top-k/permute/combine task
 constexpr int kMaxPermParts = 4;    // permute tasks per token block when blocks are few
+constexpr int kHeavyMinT = 256;     // smallest call whose experts may run over all of x
 constexpr int kBT = 128;            // max rows (tokens) per expert chunk = max MMA N
 constexpr int kBT2 = 256;           // pair tiles: max rows per chunk (128 token rows per CTA)
 constexpr int kBK = 64;             // K elements per stage (one 128-byte swizzle row)
@@ -116,7 +117,10 @@ struct BlockWs {
   int* chunk_expert;   // [C_max]
   int* chunk_row0;     // [C_max]
   int* chunk_rows;     // [C_max]
-  int* meta;           // [8] 0: n_chunks 1: n_gu 2: n_dn
+  int* chunk_src;      // [C_max] token rows of the chunk: x_perm rows from chunk_src[c], or
+                       // (heavy expert) x rows from -1 - chunk_src[c]
+  int* heavy;          // [E] 1: this call runs the expert over all T rows of x (no permute)
+  int* meta;           // [8] 0: n_chunks 1: n_gu 2: n_dn 3: heavy experts' chunks (first)
   // Event tensor counters
   int* ev_rblk;        // [nb_max] router partials landed per token block (count up to NC)
   int* ev_route;       // [1] top-k tasks done (count up to nb)
@@ -134,7 +138,7 @@ struct BlockWs {
 struct Workspace {
   BlockWs blk[kMaxBlocks];
   __nv_bfloat16* x_perm;  // [R_max, H]
-  __nv_bfloat16* act;     // [R_max, I]
+  __nv_bfloat16* act;     // [R_act, I] (R_act: R_max plus the heavy experts' extra rows)
   float* acc;             // [T_max, H] fp32 combine accumulator when `out` is bf16
   float* yperm;           // [R_max, H] fp32 expert rows, expert-sorted (ordered combine)
   __nv_bfloat16* xn;      // [T_max, H] normalised input rounded to bf16 (chain)
@@ -163,6 +167,8 @@ struct MegaParams {
   CUtensorMap tm_wg[kMaxBlocks];   // router weight [H, E], box 64 experts x 64 rows (MN-major A)
   CUtensorMap tm_xr;               // router input rows [T, H] (x, or xn in the chain), box 32x64
   CUtensorMap tm_xrlo;             // xn_lo [T_max, H] (chain), box 32x64
+  CUtensorMap tm_xh;               // x [T, H] box 16x64: heavy experts' token rows
+  CUtensorMap tm_xh64;             // x [T, H] box 64x64
   Workspace ws;
   const __nv_bfloat16* x;
   void* out;     // fp32 [T, H], or bf16 when out_bf16
@@ -189,6 +195,8 @@ struct MegaParams {
   int ev_mul;    // notifies per tile or routing task (2 with pair tiles: one per CTA)
   int thin;      // narrow tiles whose chunks hold at most kTB rows: 20 KB stages
   int direct;    // one token block: gate/up tiles read all T token rows of x (no permute)
+  int heavy_min; // > 0: experts with at least this many rows run over all T rows of x,
+                 // their tiles reading x itself (ready as soon as the scan has run); 0: off
   unsigned epoch;
   int mode;  // 0 static, 1 dynamic, 2 mixed
   int dense;     // dense MLP: one weight set, chunks are 128-row slices of x, no routing

@@ -29,6 +29,7 @@ struct etc_plan_s {
   int grid = 0;
   int pair_grid = 0;          // CTAs of a launch in CTA pairs (0: cluster launches unavailable)
   int nb_max = 0, C_max = 0, R_max = 0;
+  int R_act = 0;              // act rows: R_max plus what heavy experts add (up to 20 %)
   long long partial_max = 0;  // max NC * T_pad over T
   std::vector<void*> allocs;
   void* ctrl = nullptr;       // counters, flags, queue heads: cleared by reset
@@ -43,6 +44,9 @@ struct etc_plan_s {
   const void* cached_x = nullptr;  // router input map of the caller's x, per (pointer, T)
   int cached_xT = 0;
   CUtensorMap tm_x{};
+  const void* cached_xh = nullptr;  // heavy experts' token-operand maps of x, per (pointer, T)
+  int cached_xhT = 0;
+  CUtensorMap tm_xh16{}, tm_xh64{};
   CUtensorMap tm_xn{}, tm_xnlo{};  // router input maps of the chain's normalised rows
   unsigned epoch = 0;
   long long launches = 0;
@@ -107,6 +111,8 @@ void carve_block(Bump& data, Bump& ctrl, BlockWs& b, const etc_plan_s& p) {
   b.chunk_expert = data.take<int>(C);
   b.chunk_row0 = data.take<int>(C);
   b.chunk_rows = data.take<int>(C);
+  b.chunk_src = data.take<int>(C);
+  b.heavy = data.take<int>(E);
   b.meta = data.take<int>(8);
   b.ev_rblk = ctrl.take<int>(nb);
   b.ev_route = ctrl.take<int>(1);
@@ -323,6 +329,30 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   // One token block: gate/up tiles read the T token rows straight from x (or
   // the chain's normalised rows); no permute task, no x_perm rows.
   prm.direct = (prm.thin && prm.nb == 1 && router_tiles) ? 1 : 0;
+  // Heavy experts: an expert that at least 85 % of the call's tokens chose
+  // runs over all T rows of x, its gate/up tiles reading x itself (weight 0
+  // for the tokens that did not choose it), so that its tiles need no
+  // permuted rows and start as soon as the scan has run, while the permute of
+  // the other experts is still in flight.  Calls whose output is the plain
+  // fp32 sum of the fused combine, with the expert tiles taken from the
+  // queue (dynamic and mixed scheduling: 21 us faster on the skewed T = 4096
+  // prefill; the static walk measured no gain).
+  prm.heavy_min = (prm.wide && !prm.pair && !prm.direct && a.n_blocks == 1 && !a.use_norm &&
+                   router_tiles && !prm.out_bf16 && !prm.ordered && a.T >= kHeavyMinT &&
+                   mode != ETC_SCHED_STATIC && !(p->opts.debug_flags & ETC_DEBUG_NO_HEAVY))
+                      ? (17 * a.T + 19) / 20
+                      : 0;
+  if (prm.heavy_min > 0) {
+    if (p->cached_xh != a.x || p->cached_xhT != a.T) {
+      if (encode_tensor_map_2d_bf16(&p->tm_xh16, a.x, p->H, a.T, kBK, 16) != CUDA_SUCCESS ||
+          encode_tensor_map_2d_bf16(&p->tm_xh64, a.x, p->H, a.T, kBK, 64) != CUDA_SUCCESS)
+        return set_error(ETC_ERR_CUDA, "tensor map (x, heavy experts) failed");
+      p->cached_xh = a.x;
+      p->cached_xhT = a.T;
+    }
+    prm.tm_xh = p->tm_xh16;
+    prm.tm_xh64 = p->tm_xh64;
+  }
   if (++p->epoch == 0) p->epoch = 1;
   prm.epoch = p->epoch;
   prm.mode = mode;
@@ -335,7 +365,7 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   if (p->opts.debug_flags & ETC_DEBUG_POISON) {
     const size_t rows = static_cast<size_t>(p->R_max);
     ETC_CUDA_TRY(cudaMemsetAsync(p->ws.x_perm, 0xFF, rows * p->H * 2, s));
-    ETC_CUDA_TRY(cudaMemsetAsync(p->ws.act, 0xFF, rows * p->I * 2, s));
+    ETC_CUDA_TRY(cudaMemsetAsync(p->ws.act, 0xFF, static_cast<size_t>(p->R_act) * p->I * 2, s));
     if (p->ws.acc)
       ETC_CUDA_TRY(cudaMemsetAsync(p->ws.acc, 0xFF, static_cast<size_t>(p->T_max) * p->H * 4, s));
   }
@@ -493,7 +523,11 @@ int make_plan(etc_plan_t* out, const etc_moe_opts* opts, bool dense) {
 
   p->nb_max = (p->T_max + kTB - 1) / kTB;
   p->R_max = p->T_max * p->k;
-  p->C_max = (p->R_max + kBT - 1) / kBT + p->E;
+  // Heavy experts (at least ceil(0.85 T) rows each, so at most k / 0.85 of
+  // them) take T act rows instead of their row count: at most
+  // 0.15 / 0.85 < 0.2 of R_max more.
+  p->R_act = dense ? p->R_max : p->R_max + p->R_max / 5 + kBT;
+  p->C_max = (p->R_act + kBT - 1) / kBT + p->E;
   // Rows of fixed-point router sums: the token rows of the largest call whose
   // H is split (the split depends on T only through nb).
   p->partial_max = kTB;
@@ -529,7 +563,7 @@ int make_plan(etc_plan_t* out, const etc_moe_opts* opts, bool dense) {
     return fail(set_error(ETC_ERR_CUDA, "cudaMemset failed"));
 
   void* m = nullptr;
-  const size_t R = static_cast<size_t>(p->R_max);
+  const size_t R = static_cast<size_t>(p->R_act);
   if ((r = alloc_dev(p, &m, R * p->I * 2)) != ETC_OK) return fail(r);
   p->ws.act = static_cast<__nv_bfloat16*>(m);
   if (encode_tensor_map_2d_bf16(&p->tm_act, p->ws.act, p->I, R, kBK, 16) != CUDA_SUCCESS ||
@@ -744,7 +778,7 @@ int etc_moe_debug_buffer(etc_plan_t p, void* stream, int which, void* dst,
     cap = R * p->H * 2;
   } else if (which == 1) {
     src = p->ws.act;
-    cap = R * p->I * 2;
+    cap = static_cast<unsigned long long>(p->R_act) * p->I * 2;
   } else {
     return set_error(ETC_ERR_INVALID, "unknown buffer %d", which);
   }

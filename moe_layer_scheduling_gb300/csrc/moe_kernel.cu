@@ -55,7 +55,8 @@ namespace etc {
 
 struct Task {
   int type, blk, a, b;
-  int e, row0, rows, pad;
+  int e, row0, rows, pad;  // expert chunks: act rows [row0, row0 + rows); token rows from
+                           // x_perm row pad, or (pad < 0, heavy expert) x row -1 - pad
   unsigned long long t_disp;  // when the scheduler handed the task over (trace only)
 };
 
@@ -229,6 +230,29 @@ __device__ __forceinline__ unsigned long long workers_excl_scan(unsigned long lo
   unsigned long long base = 0;
   for (int i = 0; i < w; ++i) base += tmp[i];
   named_bar(1, kNumWorkers);
+  return base + x - v;
+}
+// The same, also giving every thread the sum over all 256 values.
+__device__ __forceinline__ unsigned long long workers_excl_scan_total(unsigned long long v,
+                                                                      unsigned long long* tmp, int wt,
+                                                                      unsigned long long& total) {
+  const int lane = wt & 31, w = wt >> 5;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[w] = x;
+  named_bar(1, kNumWorkers);
+  unsigned long long base = 0, all = 0;
+#pragma unroll
+  for (int i = 0; i < kNumWorkers / 32; ++i) {
+    if (i < w) base += tmp[i];
+    all += tmp[i];
+  }
+  named_bar(1, kNumWorkers);
+  total = all;
   return base + x - v;
 }
 
@@ -696,37 +720,66 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
   }
   named_bar(1, kNumWorkers);  // the counts are read before the scan scratch is reused
   int* tmp = reinterpret_cast<int*>(simt);  // scan scratch [32]
+  unsigned long long* scr = reinterpret_cast<unsigned long long*>(simt + 256);
   const int cw = p.cw;
-  const int nch = (cnt + cw - 1) / cw;
-  // rows (low half) and chunks (high half) of the experts before this one, in one scan
-  const unsigned long long pre = workers_excl_scan(
-      (static_cast<unsigned long long>(nch) << 32) | static_cast<unsigned>(cnt),
-      reinterpret_cast<unsigned long long*>(simt + 256), wt);
-  const int row0 = static_cast<int>(pre & 0xffffffffu), ch0 = static_cast<int>(pre >> 32);
+  // A heavy expert runs over all T rows of x: T act rows, ceil(T / cw)
+  // chunks, numbered before every other expert's (the static walk and the
+  // queue take them first: they need no permuted rows).
+  const bool heavy = p.heavy_min > 0 && wt < E && cnt >= p.heavy_min;
+  const int arows = heavy ? p.T : cnt;
+  const int nch = (arows + cw - 1) / cw;
+  int row0, arow0, ch0, n_rows, n_chunks, n_heavy_ch = 0;
+  unsigned long long tot = 0;
+  if (p.heavy_min == 0) {
+    // rows (low half) and chunks (high half) of the experts before this one, in one scan
+    const unsigned long long pre = workers_excl_scan_total(
+        (static_cast<unsigned long long>(nch) << 32) | static_cast<unsigned>(cnt), scr, wt, tot);
+    row0 = arow0 = static_cast<int>(pre & 0xffffffffu);
+    ch0 = static_cast<int>(pre >> 32);
+    n_rows = static_cast<int>(tot & 0xffffffffu);
+    n_chunks = static_cast<int>(tot >> 32);
+  } else {
+    // x_perm rows (low) and act rows (high); then heavy experts' chunks (low)
+    // and the other experts' chunks (high)
+    const unsigned long long pre = workers_excl_scan_total(
+        (static_cast<unsigned long long>(arows) << 32) | static_cast<unsigned>(cnt), scr, wt, tot);
+    row0 = static_cast<int>(pre & 0xffffffffu);
+    arow0 = static_cast<int>(pre >> 32);
+    n_rows = static_cast<int>(tot & 0xffffffffu);
+    const unsigned long long pc = workers_excl_scan_total(
+        (static_cast<unsigned long long>(heavy ? 0 : nch) << 32) | static_cast<unsigned>(heavy ? nch : 0),
+        scr, wt, tot);
+    n_heavy_ch = static_cast<int>(tot & 0xffffffffu);
+    n_chunks = n_heavy_ch + static_cast<int>(tot >> 32);
+    ch0 = heavy ? static_cast<int>(pc & 0xffffffffu) : n_heavy_ch + static_cast<int>(pc >> 32);
+  }
   if (wt < E) {
     B.counts[wt] = cnt;
     B.exp_indptr[wt] = row0;
-    B.chunk_indptr[wt] = ch0;
-    if (wt == E - 1) {
-      B.exp_indptr[E] = row0 + cnt;
-      B.chunk_indptr[E] = ch0 + nch;
-      B.meta[0] = ch0 + nch;
-      B.meta[1] = (ch0 + nch) * p.NT_gu;
-      B.meta[2] = (ch0 + nch) * p.NT_dn;
+    B.chunk_indptr[wt] = ch0;  // (first chunk of the expert; its chunks are consecutive)
+    B.heavy[wt] = heavy ? 1 : 0;
+    if (wt == 0) {
+      B.exp_indptr[E] = n_rows;
+      B.chunk_indptr[E] = n_chunks;
+      B.meta[0] = n_chunks;
+      B.meta[1] = n_chunks * p.NT_gu;
+      B.meta[2] = n_chunks * p.NT_dn;
+      B.meta[3] = n_heavy_ch;
     }
     for (int c = 0; c < nch; ++c) {
       const int chn = ch0 + c;
       B.chunk_expert[chn] = wt;
-      B.chunk_row0[chn] = row0 + c * cw;
-      B.chunk_rows[chn] = min(cw, cnt - c * cw);
+      B.chunk_row0[chn] = arow0 + c * cw;
+      B.chunk_rows[chn] = min(cw, arows - c * cw);
+      B.chunk_src[chn] = heavy ? -1 - c * cw : row0 + c * cw;
       // one notify per tile, or per CTA of a pair tile
       B.ev_act[chn] = p.ev_mul * p.NT_gu;
       B.ev_down[chn] = p.ev_mul * p.NT_dn;
     }
     // Data-dependent event update: expert e waits for its counts[e] rows
-    // (none in direct mode: its tiles read x itself).
+    // (none in direct mode or for a heavy expert: their tiles read x itself).
     const int extra = ((p.debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT) && wt == p.debug_arg) ? 1 : 0;
-    B.ev_expert[wt] = (p.direct ? 0 : cnt) + extra;
+    B.ev_expert[wt] = (p.direct || heavy ? 0 : cnt) + extra;
   }
   int* s_row0 = reinterpret_cast<int*>(simt + kDirectOff);  // [kMaxE]
   if (p.direct) {
@@ -769,7 +822,6 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
     if (tiles_queued(p)) {
       // Tasks of the block that pass through the queue: all of them in
       // DYNAMIC, the expert tiles and the finaliser in MIXED.
-      const int n_chunks = B.meta[0];
       const int nbp = p.nbp;
       const int routing = dyn ? (p.use_norm ? nbp : 0) + p.n_router + (p.NC > 1 ? nbp : 0) +
                                     (p.fuse_scan ? 0 : 1) + (p.direct ? 0 : nbp * p.PP)
@@ -783,18 +835,22 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
     st_release(B.plan_flag, p.epoch);
     if (tiles_queued(p) && blk == p.n_blocks - 1) st_release(p.ws.qtotal_flag, p.epoch);
     // The tasks this plan makes ready at once: the block's permute tasks
-    // (DYNAMIC), or in direct mode every gate/up tile (DYNAMIC and MIXED).
-    const int n_push = p.direct ? (tiles_queued(p) ? B.meta[0] * p.NT_gu : 0) : dyn ? p.nbp * p.PP : 0;
+    // (DYNAMIC), then the gate/up tiles that need no permuted rows (DYNAMIC
+    // and MIXED): every one in direct mode, the heavy experts' otherwise.
+    const int n_perm = (!p.direct && dyn) ? p.nbp * p.PP : 0;
+    const int n_gu = tiles_queued(p) ? (p.direct ? n_chunks : n_heavy_ch) * p.NT_gu : 0;
+    const int n_push = n_perm + n_gu;
     if (n_push) {
       const QueueView q = queue_of(p);
       tmp[0] = q.n_seed + atom_add_relaxed(q.tail, n_push);
     }
     tmp[1] = n_push;
+    tmp[2] = n_perm;
   }
-  if (p.direct ? tiles_queued(p) : dynamic_mode(p)) {
+  if (tiles_queued(p)) {
     // Every worker writes some of the reserved slots.
     named_bar(1, kNumWorkers);
-    const int base = tmp[0], n_push = tmp[1];
+    const int base = tmp[0], n_push = tmp[1], n_perm = tmp[2];
     const QueueView q = queue_of(p);
     __threadfence();  // the plan above is published with the slots
     for (int i = wt; i < n_push; i += kNumWorkers) {
@@ -803,13 +859,14 @@ __device__ void scan_block(const MegaParams& p, int blk, uint8_t* simt, int wt,
         raise_error(c0, DERR_QUEUE_OVERFLOW, 3, base + i);
         break;
       }
+      const int g = i - n_perm;  // gate/up tile g of the chunks pushed here
       // (fault injection: the tiles of the expert that waits for one row more
       // are never made ready, so a queue pop runs out of time)
-      if (p.direct && (p.debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT) &&
-          __ldcg(B.chunk_expert + i / p.NT_gu) == p.debug_arg)
+      if (g >= 0 && (p.debug_flags & ETC_DEBUG_FAULT_EXTRA_WAIT) &&
+          __ldcg(B.chunk_expert + g / p.NT_gu) == p.debug_arg)
         continue;
-      const uint32_t d = p.direct ? task_enc(TK_GU, blk, i / p.NT_gu, i % p.NT_gu)
-                                  : task_enc(TK_PERM, blk, i / p.PP, i % p.PP);
+      const uint32_t d = g >= 0 ? task_enc(TK_GU, blk, g / p.NT_gu, g % p.NT_gu)
+                                : task_enc(TK_PERM, blk, i / p.PP, i % p.PP);
       st_relaxed_u64(&q.slots[base + i], (static_cast<unsigned long long>(q.epoch) << 32) | d);
     }
   }
@@ -882,6 +939,8 @@ __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* 
   int* s_part = s_ids + kTB * kMaxK;  // [kNumWorkers]
   int* s_pcnt = s_part + kNumWorkers; // [E]
   unsigned* s_mask = reinterpret_cast<unsigned*>(s_pcnt + kMaxE);  // [E] tokens of the block per expert
+  int* s_heavy = reinterpret_cast<int*>(s_mask + kMaxE);             // [E] experts that read x itself
+  static_assert(4 * (5 * kMaxE + 2 * kTB * kMaxK + kNumWorkers) <= kPermRowOff, "permute tables");
   static_assert(kTB <= 32, "a token block's tokens form one 32-bit mask");
   uint8_t* rows = simt + kPermRowOff;
   const int t0 = tb * kTB, ntok = max(0, min(kTB, p.T - t0));  // (odd CTA of the last pair block: none)
@@ -920,7 +979,10 @@ __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* 
     s_part[wt] = sum;
   }
   for (int i = wt; i < r_hi * k; i += kNumWorkers) s_ids[i] = __ldcg(B.ids + t0 * k + i);
-  for (int i = wt; i < E; i += kNumWorkers) s_mask[i] = 0u;
+  for (int i = wt; i < E; i += kNumWorkers) {
+    s_mask[i] = 0u;
+    s_heavy[i] = p.heavy_min > 0 ? __ldcg(B.heavy + i) : 0;
+  }
   named_bar(1, kNumWorkers);
   for (int e = wt; e < E; e += kNumWorkers) {
     int run = __ldcg(B.exp_indptr + e);
@@ -949,7 +1011,8 @@ __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* 
     B.row_w[row] = __ldcg(B.wts + t0 * k + i);
   }
   if (tb < p.nb)
-    for (int e = wt; e < E; e += kNumWorkers) B.part_cnt[(tb * p.PP + part) * E + e] = s_pcnt[e];
+    for (int e = wt; e < E; e += kNumWorkers)  // (a heavy expert waits for no rows)
+      B.part_cnt[(tb * p.PP + part) * E + e] = s_heavy[e] ? 0 : s_pcnt[e];
   if (wt == 0) {
     for (int r = 0; r < nmine; ++r) {
       const uint32_t L = li + r;
@@ -957,7 +1020,8 @@ __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* 
       if (!mbar_wait(&c->pbar[sl], (L / nslot) & 1, clk, 270)) break;
       const uint8_t* srow = rows + sl * RB;
       for (int j = 0; j < k; ++j)
-        bulk_store(p.ws.x_perm + static_cast<size_t>(s_slot[(r_lo + r) * k + j]) * p.H, srow, RB);
+        if (!s_heavy[s_ids[(r_lo + r) * k + j]])  // (a heavy expert's tiles read x itself)
+          bulk_store(p.ws.x_perm + static_cast<size_t>(s_slot[(r_lo + r) * k + j]) * p.H, srow, RB);
       bulk_commit();
       const int nx = r + nslot;
       if (nx < nmine) {
@@ -1063,11 +1127,31 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
   int* s_rtok = reinterpret_cast<int*>(simt + 2 * kEpiHalfBytes);                 // [256]
   float* s_rw = reinterpret_cast<float*>(simt + 2 * kEpiHalfBytes + 4 * kBT2);    // [256]
   const bool fused_comb = t.type == TK_DN && !p.dense && !p.ordered;
-  if (fused_comb)
-    for (int r = wt; r < t.rows; r += kNumWorkers) {
-      s_rtok[r] = __ldcg(B.row_token + t.row0 + r);
-      s_rw[r] = __ldcg(B.row_w + t.row0 + r);
+  if (fused_comb) {
+    if (t.pad >= 0) {
+      for (int r = wt; r < t.rows; r += kNumWorkers) {
+        s_rtok[r] = __ldcg(B.row_token + t.pad + r);
+        s_rw[r] = __ldcg(B.row_w + t.pad + r);
+      }
+    } else {
+      // Heavy expert: chunk row r is token -1 - pad + r; its weight for this
+      // expert from the token's selection (no row: a token that did not
+      // choose the expert, which adds nothing).
+      const int tok0 = -1 - t.pad;
+      for (int r = wt; r < t.rows; r += kNumWorkers) {
+        const int tok = tok0 + r;
+        int hit = -1;
+        float w = 0.f;
+        for (int j = 0; j < p.k; ++j)
+          if (__ldcg(B.ids + static_cast<size_t>(tok) * p.k + j) == t.e) {
+            hit = tok;
+            w = __ldcg(B.wts + static_cast<size_t>(tok) * p.k + j);
+          }
+        s_rtok[r] = hit;
+        s_rw[r] = w;
+      }
     }
+  }
   if (wt == 0) *flag = mbar_wait(&c->tfull[acc], aph, clk, 230, PAIR) ? 1 : 0;
   named_bar(1, kNumWorkers);
   const bool ok = *flag != 0;
@@ -1132,7 +1216,7 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
       named_bar(1, kNumWorkers);
       for (int idx = wt; idx < t.rows * 8; idx += kNumWorkers) {
         const int i = idx >> 3, chunk = idx & 7;
-        const int tok = __ldcg(B.row_token + t.row0 + i);
+        const int tok = __ldcg(B.row_token + t.pad + i);
         const uint4 val = *reinterpret_cast<const uint4*>(SA + tok * 64 + chunk * 8);
         store_act(p, reinterpret_cast<uint4*>(p.ws.act + static_cast<size_t>(t.row0 + i) * p.I +
                                               t.b * kGuRows + chunk * 8), val);
@@ -1198,11 +1282,13 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
             const float4 val = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
             if (fused_comb) {
               const float wr = s_rw[rr];
-              red_add_v4(accr + static_cast<size_t>(s_rtok[rr]) * p.H + col,
-                         make_float4(wr * val.x, wr * val.y, wr * val.z, wr * val.w));
+              const int tok = s_rtok[rr];
+              if (tok >= 0)
+                red_add_v4(accr + static_cast<size_t>(tok) * p.H + col,
+                           make_float4(wr * val.x, wr * val.y, wr * val.z, wr * val.w));
             } else if (p.ordered) {
               // ordered combine: the expert row y itself, in expert-sorted order
-              *reinterpret_cast<float4*>(p.ws.yperm + static_cast<size_t>(t.row0 + rr) * p.H + col) = val;
+              *reinterpret_cast<float4*>(p.ws.yperm + static_cast<size_t>(t.pad + rr) * p.H + col) = val;
             } else {
               const size_t o = static_cast<size_t>(t.row0 + rr) * p.H + col;
               if (p.out_bf16) {
@@ -1373,7 +1459,7 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
             red_add_relaxed(&B.ev_expert[e], -n[i]);
           } else if (notify(&B.ev_expert[e], n[i]) == 0) {
             c0[i] = __ldcg(B.chunk_indptr + e);
-            tiles[i] = (__ldcg(B.chunk_indptr + e + 1) - c0[i]) * p.NT_gu;
+            tiles[i] = ((__ldcg(B.counts + e) + p.cw - 1) / p.cw) * p.NT_gu;
             mine += tiles[i];
           }
         }
@@ -1435,7 +1521,7 @@ __device__ void notify_follow(const MegaParams& p, Ctrl* c, const Task& t, int f
         };
         const int tbw = p.pair ? 2 * kTB : kTB;  // rows of a (pair) token block
         for (int r = r0; r < r1; ++r) {
-          const int tb = __ldcg(B.row_token + t.row0 + r) / tbw;
+          const int tb = __ldcg(B.row_token + t.pad + r) / tbw;
           if (tb != run_tb) {
             flush_run();
             run_tb = tb;
@@ -1618,13 +1704,16 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
     if (t.type != TK_GU && t.type != TK_DN) continue;
     const bool gu = t.type == TK_GU;
     const CUtensorMap* ta = gu ? &p.tm_wgu[t.blk] : &p.tm_wd[t.blk];
-    const CUtensorMap* tb = gu ? &p.tm_xperm : &p.tm_act;
-    const CUtensorMap* tb64 = gu ? &p.tm_xperm64 : &p.tm_act64;
+    // token operand: x_perm rows (a heavy expert's: x rows) for gate/up, act rows for down
+    const bool heavy_x = gu && t.pad < 0;
+    const CUtensorMap* tb = !gu ? &p.tm_act : heavy_x ? &p.tm_xh : &p.tm_xperm;
+    const CUtensorMap* tb64 = !gu ? &p.tm_act64 : heavy_x ? &p.tm_xh64 : &p.tm_xperm64;
+    const int src0 = !gu ? t.row0 : heavy_x ? -1 - t.pad : t.pad;
     const int KB = (gu ? p.H : p.I) / kBK;
     // Token rows of this CTA: the whole chunk, or its half of a pair tile
     // (the MMA takes rows [0, npad/2) from the even CTA, the rest from the odd).
     const int half = pair ? pair_npad(t.rows) / 2 : 0;
-    const int brow0 = pair ? t.row0 + rank * half : t.row0;
+    const int brow0 = pair ? src0 + rank * half : src0;
     const int nb16 = pair ? half >> 4 : (t.rows + 15) >> 4;
     const int n64 = nb16 >> 2, r16 = nb16 & 3;  // token rows as 64-row boxes, then 16-row boxes
     // Weight rows as 64-row boxes, 8 KB apart.  Narrow gate/up: 64 gate + 64
@@ -1776,12 +1865,14 @@ __device__ __forceinline__ void resolve_chunk(const MegaParams& p, Task& t) {
     t.e = 0;
     t.row0 = t.a * p.cw;
     t.rows = min(p.cw, p.T - t.row0);
+    t.pad = t.row0;
     return;
   }
   const BlockWs& B = p.ws.blk[t.blk];
   t.e = __ldcg(B.chunk_expert + t.a);
   t.row0 = __ldcg(B.chunk_row0 + t.a);
   t.rows = __ldcg(B.chunk_rows + t.a);
+  t.pad = __ldcg(B.chunk_src + t.a);
 }
 
 // Dense MLP gate/up tile g of a call: groups of kGc chunks, each group taken

@@ -245,6 +245,35 @@ def test_all_tokens_on_one_expert(oracle_lib):
         _full_check(oracle_lib, w, x, sched, False)
 
 
+@pytest.mark.parametrize("sched", [B.ETC_SCHED_DYNAMIC, B.ETC_SCHED_MIXED], ids=["dynamic", "mixed"])
+def test_heavy_experts(oracle_lib, sched):
+    # Experts 5 (all 600 tokens) and 2 (552 of them) reach the heavy threshold
+    # (ceil(0.85 T) = 510 rows; queued schedules only): they run over all of
+    # x, with weight 0 for the 48 tokens that did not choose expert 2; the
+    # other six experts keep their permuted rows.  The result must match the
+    # oracle, and the same call with heavy experts switched off up to the
+    # rounding of the tiles' fp32 accumulation.
+    unfused = False
+    w = inputs.moe_weights(256, 8, 2, 256, seed=31)
+    bias = torch.zeros(8)
+    bias[5], bias[2] = 50.0, 1.0
+    w.router_bias = bias
+    x = inputs.tokens(600, 256, 32)
+    _, _, ref_ids, _ = oracle_lib.moe_layer(x, w.gate_w, w.w_gate_up, w.w_down, 2, bias=bias,
+                                            want_routing=True)
+    cnt = np.bincount(np.asarray(ref_ids).reshape(-1), minlength=8)
+    assert cnt[5] == 600 and 510 <= cnt[2] < 600 and (cnt[[0, 1, 3, 4, 6, 7]] > 0).all()
+    _full_check(oracle_lib, w, x, sched, unfused)
+    out_h, _, plan = run_layer(w, x, sched, unfused)
+    plan.close()
+    out_p, _, plan = run_layer(w, x, sched, unfused, debug_flags=B.ETC_DEBUG_NO_HEAVY)
+    plan.close()
+    # (a tile's MMAs see the token rows in other positions: fp32 accumulation
+    # may round differently, far below the bf16 operands' own rounding)
+    diff = np.max(np.abs(out_h.astype(np.float64) - out_p))
+    assert diff <= 1e-5 * np.max(np.abs(out_p)), diff
+
+
 def test_identical_experts_closed_form(oracle_lib):
     # Routing-independent closed form: with every expert equal the layer is one FFN.
     w = inputs.moe_weights(256, 16, 4, 128, seed=23)
