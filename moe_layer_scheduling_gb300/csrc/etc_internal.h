@@ -158,17 +158,17 @@ struct Workspace {
 };
 
 struct MegaParams {
-  CUtensorMap tm_wgu[kMaxBlocks];  // [E*2I, H] box 64x64, 128B swizzle
-  CUtensorMap tm_wd[kMaxBlocks];   // [E*H, I]  box 64x64
+  CUtensorMap tm_wgu[kMaxBlocks];  // [E*2I, H] box 64 rows x 64 (wide tiles: 128 rows), 128B swizzle
+  CUtensorMap tm_wd[kMaxBlocks];   // [E*H, I]  box 128 rows x 64
   CUtensorMap tm_xperm;            // [R_max, H] box 16x64 (dense MLP: the caller's x [T, H])
   CUtensorMap tm_act;              // [R_max, I] box 16x64
-  CUtensorMap tm_xperm64;          // [R_max, H] box 64x64 (dense MLP: x)
-  CUtensorMap tm_act64;            // [R_max, I] box 64x64
+  CUtensorMap tm_xperm128;         // [R_max, H] box 128 rows x 64 (dense MLP: x)
+  CUtensorMap tm_act128;           // [R_act, I] box 128 rows x 64
   CUtensorMap tm_wg[kMaxBlocks];   // router weight [H, E], box 64 experts x 64 rows (MN-major A)
   CUtensorMap tm_xr;               // router input rows [T, H] (x, or xn in the chain), box 32x64
   CUtensorMap tm_xrlo;             // xn_lo [T_max, H] (chain), box 32x64
   CUtensorMap tm_xh;               // x [T, H] box 16x64: heavy experts' token rows
-  CUtensorMap tm_xh64;             // x [T, H] box 64x64
+  CUtensorMap tm_xh128;            // x [T, H] box 128 rows x 64
   Workspace ws;
   const __nv_bfloat16* x;
   void* out;     // fp32 [T, H], or bf16 when out_bf16

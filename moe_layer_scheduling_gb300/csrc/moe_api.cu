@@ -35,10 +35,13 @@ struct etc_plan_s {
   void* ctrl = nullptr;       // counters, flags, queue heads: cleared by reset
   size_t ctrl_bytes = 0;
   Workspace ws{};
-  CUtensorMap tm_xperm{}, tm_act{}, tm_xperm64{}, tm_act64{};
+  CUtensorMap tm_xperm{}, tm_act{}, tm_xperm128{}, tm_act128{};
   const void* cached_wgu[kMaxBlocks] = {};
   const void* cached_wd[kMaxBlocks] = {};
-  CUtensorMap tm_wgu[kMaxBlocks]{}, tm_wd[kMaxBlocks]{};
+  // w_gate_up with 64-row boxes (narrow and pair tiles: 64 gate rows, then 64 up
+  // rows) and with 128-row boxes (wide tiles); w_down with 128-row boxes
+  const void* cached_wgu128[kMaxBlocks] = {};
+  CUtensorMap tm_wgu[kMaxBlocks]{}, tm_wgu128[kMaxBlocks]{}, tm_wd[kMaxBlocks]{};
   const void* cached_wg[kMaxBlocks] = {};
   CUtensorMap tm_wg[kMaxBlocks]{};
   const void* cached_x = nullptr;  // router input map of the caller's x, per (pointer, T)
@@ -46,7 +49,7 @@ struct etc_plan_s {
   CUtensorMap tm_x{};
   const void* cached_xh = nullptr;  // heavy experts' token-operand maps of x, per (pointer, T)
   int cached_xhT = 0;
-  CUtensorMap tm_xh16{}, tm_xh64{};
+  CUtensorMap tm_xh16{}, tm_xh128{};
   CUtensorMap tm_xn{}, tm_xnlo{};  // router input maps of the chain's normalised rows
   unsigned epoch = 0;
   long long launches = 0;
@@ -54,7 +57,7 @@ struct etc_plan_s {
   int dense = 0;                    // dense MLP plan (etc_mlp_plan)
   const void* cached_xd = nullptr;  // dense MLP: token-operand maps of the caller's x, per (pointer, T)
   int cached_xdT = 0;
-  CUtensorMap tm_xd16{}, tm_xd64{};
+  CUtensorMap tm_xd16{}, tm_xd128{};
 };
 
 namespace {
@@ -174,16 +177,24 @@ int status_of(etc_plan_t p) {
                    h->code, h->where, h->aux, h->cta);
 }
 
-int weight_maps(etc_plan_t p, int b, const void* wgu, const void* wd) {
-  if (p->cached_wgu[b] != wgu) {
-    CUresult r = encode_tensor_map_2d_bf16(&p->tm_wgu[b], wgu, p->H,
-                                           static_cast<unsigned long long>(p->E) * 2 * p->I, kBK, 64);
+// Weight maps of block b; `wide`: the gate/up map with 128-row boxes.
+int weight_maps(etc_plan_t p, int b, const void* wgu, const void* wd, bool wide,
+                CUtensorMap* wgu_map) {
+  const unsigned long long rows_gu = static_cast<unsigned long long>(p->E) * 2 * p->I;
+  if (!wide && p->cached_wgu[b] != wgu) {
+    CUresult r = encode_tensor_map_2d_bf16(&p->tm_wgu[b], wgu, p->H, rows_gu, kBK, 64);
     if (r != CUDA_SUCCESS) return set_error(ETC_ERR_CUDA, "tensor map (w_gate_up) failed: %d", r);
     p->cached_wgu[b] = wgu;
   }
+  if (wide && p->cached_wgu128[b] != wgu) {
+    CUresult r = encode_tensor_map_2d_bf16(&p->tm_wgu128[b], wgu, p->H, rows_gu, kBK, 128);
+    if (r != CUDA_SUCCESS) return set_error(ETC_ERR_CUDA, "tensor map (w_gate_up) failed: %d", r);
+    p->cached_wgu128[b] = wgu;
+  }
+  *wgu_map = wide ? p->tm_wgu128[b] : p->tm_wgu[b];
   if (p->cached_wd[b] != wd) {
     CUresult r = encode_tensor_map_2d_bf16(&p->tm_wd[b], wd, p->I,
-                                           static_cast<unsigned long long>(p->E) * p->H, kBK, 64);
+                                           static_cast<unsigned long long>(p->E) * p->H, kBK, 128);
     if (r != CUDA_SUCCESS) return set_error(ETC_ERR_CUDA, "tensor map (w_down) failed: %d", r);
     p->cached_wd[b] = wd;
   }
@@ -248,25 +259,19 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   std::memset(&prm, 0, sizeof prm);
   const bool router_tiles = a.logits_in == nullptr;
   for (int b = 0; b < a.n_blocks; ++b) {
-    if (stage_hi >= TK_GU) {
-      int r = weight_maps(p, b, a.wgu[b], a.wd[b]);
-      if (r != ETC_OK) return r;
-    }
     if (router_tiles) {
       int r = router_weight_map(p, b, a.gate_w[b]);
       if (r != ETC_OK) return r;
       prm.tm_wg[b] = p->tm_wg[b];
     }
-    prm.tm_wgu[b] = p->tm_wgu[b];
-    prm.tm_wd[b] = p->tm_wd[b];
     prm.gate_w[b] = static_cast<const __nv_bfloat16*>(a.gate_w[b]);
     prm.bias[b] = a.bias[b];
     prm.norm_w[b] = static_cast<const __nv_bfloat16*>(a.norm_w[b]);
   }
   prm.tm_xperm = p->tm_xperm;
   prm.tm_act = p->tm_act;
-  prm.tm_xperm64 = p->tm_xperm64;
-  prm.tm_act64 = p->tm_act64;
+  prm.tm_xperm128 = p->tm_xperm128;
+  prm.tm_act128 = p->tm_act128;
   if (router_tiles) {
     if (a.use_norm) {
       prm.tm_xr = p->tm_xn;
@@ -329,6 +334,12 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   // One token block: gate/up tiles read the T token rows straight from x (or
   // the chain's normalised rows); no permute task, no x_perm rows.
   prm.direct = (prm.thin && prm.nb == 1 && router_tiles) ? 1 : 0;
+  if (stage_hi >= TK_GU)
+    for (int b = 0; b < a.n_blocks; ++b) {
+      int r = weight_maps(p, b, a.wgu[b], a.wd[b], prm.wide != 0, &prm.tm_wgu[b]);
+      if (r != ETC_OK) return r;
+      prm.tm_wd[b] = p->tm_wd[b];
+    }
   // Heavy experts: an expert that at least 85 % of the call's tokens chose
   // runs over all T rows of x, its gate/up tiles reading x itself (weight 0
   // for the tokens that did not choose it), so that its tiles need no
@@ -345,13 +356,13 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   if (prm.heavy_min > 0) {
     if (p->cached_xh != a.x || p->cached_xhT != a.T) {
       if (encode_tensor_map_2d_bf16(&p->tm_xh16, a.x, p->H, a.T, kBK, 16) != CUDA_SUCCESS ||
-          encode_tensor_map_2d_bf16(&p->tm_xh64, a.x, p->H, a.T, kBK, 64) != CUDA_SUCCESS)
+          encode_tensor_map_2d_bf16(&p->tm_xh128, a.x, p->H, a.T, kBK, 128) != CUDA_SUCCESS)
         return set_error(ETC_ERR_CUDA, "tensor map (x, heavy experts) failed");
       p->cached_xh = a.x;
       p->cached_xhT = a.T;
     }
     prm.tm_xh = p->tm_xh16;
-    prm.tm_xh64 = p->tm_xh64;
+    prm.tm_xh128 = p->tm_xh128;
   }
   if (++p->epoch == 0) p->epoch = 1;
   prm.epoch = p->epoch;
@@ -425,24 +436,20 @@ int run_dense_call(etc_plan_t p, void* stream, const void* x, const void* wgu, c
   ETC_CUDA_TRY(cudaGetDevice(&dev));
   if (dev != p->device)
     return set_error(ETC_ERR_INVALID, "plan belongs to device %d, current device is %d", p->device, dev);
-  int r = weight_maps(p, 0, wgu, wd);
-  if (r != ETC_OK) return r;
   if (p->cached_xd != x || p->cached_xdT != T) {
     // Rows past T read as zero: the maps' extent is the call's T.
     if (encode_tensor_map_2d_bf16(&p->tm_xd16, x, p->H, T, kBK, 16) != CUDA_SUCCESS ||
-        encode_tensor_map_2d_bf16(&p->tm_xd64, x, p->H, T, kBK, 64) != CUDA_SUCCESS)
+        encode_tensor_map_2d_bf16(&p->tm_xd128, x, p->H, T, kBK, 128) != CUDA_SUCCESS)
       return set_error(ETC_ERR_CUDA, "tensor map (x) failed");
     p->cached_xd = x;
     p->cached_xdT = T;
   }
   MegaParams prm;
   std::memset(&prm, 0, sizeof prm);
-  prm.tm_wgu[0] = p->tm_wgu[0];
-  prm.tm_wd[0] = p->tm_wd[0];
   prm.tm_xperm = p->tm_xd16;
-  prm.tm_xperm64 = p->tm_xd64;
+  prm.tm_xperm128 = p->tm_xd128;
   prm.tm_act = p->tm_act;
-  prm.tm_act64 = p->tm_act64;
+  prm.tm_act128 = p->tm_act128;
   prm.ws = p->ws;
   prm.x = static_cast<const __nv_bfloat16*>(x);
   prm.out = out;
@@ -468,6 +475,9 @@ int run_dense_call(etc_plan_t p, void* stream, const void* x, const void* wgu, c
   prm.NT_gu = p->I / (prm.wide || prm.pair ? kGuRowsW : kGuRows);
   prm.NT_dn = p->H / (prm.wide || prm.pair ? kDnRowsW : kDnRows);
   prm.thin = (!prm.wide && !prm.pair && T <= kTB) ? 1 : 0;  // chunks of at most kTB rows
+  int r = weight_maps(p, 0, wgu, wd, prm.wide != 0, &prm.tm_wgu[0]);
+  if (r != ETC_OK) return r;
+  prm.tm_wd[0] = p->tm_wd[0];
   prm.dense = 1;
   prm.n_chunks = (T + prm.cw - 1) / prm.cw;
   prm.q_total = prm.n_chunks * (prm.NT_gu + prm.NT_dn);
@@ -567,7 +577,7 @@ int make_plan(etc_plan_t* out, const etc_moe_opts* opts, bool dense) {
   if ((r = alloc_dev(p, &m, R * p->I * 2)) != ETC_OK) return fail(r);
   p->ws.act = static_cast<__nv_bfloat16*>(m);
   if (encode_tensor_map_2d_bf16(&p->tm_act, p->ws.act, p->I, R, kBK, 16) != CUDA_SUCCESS ||
-      encode_tensor_map_2d_bf16(&p->tm_act64, p->ws.act, p->I, R, kBK, 64) != CUDA_SUCCESS)
+      encode_tensor_map_2d_bf16(&p->tm_act128, p->ws.act, p->I, R, kBK, 128) != CUDA_SUCCESS)
     return fail(set_error(ETC_ERR_CUDA, "tensor map encoding of the workspace failed"));
   if (!dense && (r = plan_moe_buffers(p)) != ETC_OK) return fail(r);
   for (int i = 0; i < 2; ++i) {
@@ -600,7 +610,7 @@ int plan_moe_buffers(etc_plan_t p) {
   if ((r = alloc_dev(p, &m, R * p->H * 2)) != ETC_OK) return r;
   p->ws.x_perm = static_cast<__nv_bfloat16*>(m);
   if (encode_tensor_map_2d_bf16(&p->tm_xperm, p->ws.x_perm, p->H, R, kBK, 16) != CUDA_SUCCESS ||
-      encode_tensor_map_2d_bf16(&p->tm_xperm64, p->ws.x_perm, p->H, R, kBK, 64) != CUDA_SUCCESS)
+      encode_tensor_map_2d_bf16(&p->tm_xperm128, p->ws.x_perm, p->H, R, kBK, 128) != CUDA_SUCCESS)
     return set_error(ETC_ERR_CUDA, "tensor map encoding of the workspace failed");
   if (p->opts.combine == ETC_COMBINE_ORDERED) {  // the expert rows the ordered combine sums
     if ((r = alloc_dev(p, &m, R * p->H * 4)) != ETC_OK) return r;

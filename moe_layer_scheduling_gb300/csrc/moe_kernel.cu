@@ -1707,7 +1707,7 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
     // token operand: x_perm rows (a heavy expert's: x rows) for gate/up, act rows for down
     const bool heavy_x = gu && t.pad < 0;
     const CUtensorMap* tb = !gu ? &p.tm_act : heavy_x ? &p.tm_xh : &p.tm_xperm;
-    const CUtensorMap* tb64 = !gu ? &p.tm_act64 : heavy_x ? &p.tm_xh64 : &p.tm_xperm64;
+    const CUtensorMap* tb128 = !gu ? &p.tm_act128 : heavy_x ? &p.tm_xh128 : &p.tm_xperm128;
     const int src0 = !gu ? t.row0 : heavy_x ? -1 - t.pad : t.pad;
     const int KB = (gu ? p.H : p.I) / kBK;
     // Token rows of this CTA: the whole chunk, or its half of a pair tile
@@ -1715,11 +1715,12 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
     const int half = pair ? pair_npad(t.rows) / 2 : 0;
     const int brow0 = pair ? src0 + rank * half : src0;
     const int nb16 = pair ? half >> 4 : (t.rows + 15) >> 4;
-    const int n64 = nb16 >> 2, r16 = nb16 & 3;  // token rows as 64-row boxes, then 16-row boxes
-    // Weight rows as 64-row boxes, 8 KB apart.  Narrow gate/up: 64 gate + 64
-    // up rows (one M=128 operand); wide: 128 gate rows, then 128 up rows (two
-    // operands); pair: 64 gate + 64 up rows of this CTA's half of the 128
-    // intermediate columns; down tiles: consecutive output rows of w_down.
+    const int n128 = nb16 >> 3, r16 = nb16 & 7;  // token rows as 128-row boxes, then 16-row boxes
+    // Weight rows.  Narrow gate/up: 64 gate + 64 up rows (one M=128 operand,
+    // two 64-row boxes); wide: 128 gate rows, then 128 up rows (two operands,
+    // two 128-row boxes); pair: 64 gate + 64 up rows of this CTA's half of the
+    // 128 intermediate columns (two 64-row boxes); down tiles: 128 (wide: 256)
+    // consecutive output rows of w_down (128-row boxes).
     const bool wide = p.wide != 0;
     const int nA = wide ? 4 : 2;
     int rowA[4];
@@ -1744,14 +1745,20 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
       uint8_t* sa = base + s * g.bytes;
       uint8_t* sb = sa + g.boff;
       if (announce) mbar_arrive_expect_tx(&c->full[s], bytes * tx_mul);
-      for (int i = 0; i < nA; ++i) load(sa + i * (kOpABytes / 2), ta, s, kb * kBK, rowA[i]);
+      if (gu && !wide) {
+        load(sa, ta, s, kb * kBK, rowA[0]);
+        load(sa + kOpABytes / 2, ta, s, kb * kBK, rowA[1]);
+      } else {
+        load(sa, ta, s, kb * kBK, rowA[0]);
+        if (wide) load(sa + kOpABytes, ta, s, kb * kBK, rowA[2]);
+      }
       if (direct_x) {
         load(sb, &p.tm_xr, s, kb * kBK, 0);
         continue;
       }
-      for (int i = 0; i < n64; ++i) load(sb + i * 64 * kBK * 2, tb64, s, kb * kBK, brow0 + 64 * i);
+      for (int i = 0; i < n128; ++i) load(sb + i * 128 * kBK * 2, tb128, s, kb * kBK, brow0 + 128 * i);
       for (int i = 0; i < r16; ++i)
-        load(sb + (n64 * 64 + i * 16) * kBK * 2, tb, s, kb * kBK, brow0 + n64 * 64 + 16 * i);
+        load(sb + (n128 * 128 + i * 16) * kBK * 2, tb, s, kb * kBK, brow0 + n128 * 128 + 16 * i);
     }
   }
 }
@@ -2122,8 +2129,8 @@ __global__ void __launch_bounds__(kThreads, 1) etc_moe_megakernel(const __grid_c
     }
     tma_prefetch_desc(&p.tm_xperm);
     tma_prefetch_desc(&p.tm_act);
-    tma_prefetch_desc(&p.tm_xperm64);
-    tma_prefetch_desc(&p.tm_act64);
+    tma_prefetch_desc(&p.tm_xperm128);
+    tma_prefetch_desc(&p.tm_act128);
   }
   if (w == kWarpMma) {
     if constexpr (PAIR) {  // the same columns in both CTAs of the pair
