@@ -63,6 +63,23 @@ CUresult encode_tensor_map_2d_bf16(CUtensorMap* m, const void* base, unsigned lo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// 3-D map of a bf16 tensor [outer][middle][inner] (inner contiguous), same
+// swizzle and fill as above; the box lands as box_outer blocks of box_mid
+// rows of 128-byte swizzled rows.
+CUresult encode_tensor_map_3d_bf16(CUtensorMap* m, const void* base, unsigned long long inner,
+                                   unsigned long long mid, unsigned long long outer,
+                                   unsigned box_inner, unsigned box_mid, unsigned box_outer) {
+  PFN_encodeTiled fn = get_encode();
+  if (!fn) return CUDA_ERROR_NOT_SUPPORTED;
+  cuuint64_t dims[3] = {inner, mid, outer};
+  cuuint64_t strides[2] = {inner * 2, inner * 2 * mid};
+  cuuint32_t box[3] = {box_inner, box_mid, box_outer};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 int sm_count(int device) {
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;

@@ -22,6 +22,9 @@ extern std::atomic<long long> g_launches;
 CUresult encode_tensor_map_2d_bf16(CUtensorMap* m, const void* base, unsigned long long inner,
                                    unsigned long long rows, unsigned box_inner,
                                    unsigned box_rows);
+CUresult encode_tensor_map_3d_bf16(CUtensorMap* m, const void* base, unsigned long long inner,
+                                   unsigned long long mid, unsigned long long outer,
+                                   unsigned box_inner, unsigned box_mid, unsigned box_outer);
 
 int sm_count(int device);
 

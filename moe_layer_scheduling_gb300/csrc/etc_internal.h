@@ -158,8 +158,9 @@ struct Workspace {
 };
 
 struct MegaParams {
-  CUtensorMap tm_wgu[kMaxBlocks];  // [E*2I, H] box 64 rows x 64 (wide tiles: 128 rows), 128B swizzle
-  CUtensorMap tm_wd[kMaxBlocks];   // [E*H, I]  box 128 rows x 64
+  CUtensorMap tm_wgu[kMaxBlocks];  // [E*2][I][H] box 2 x 64 rows x 64 (wide tiles: 2 x 128 rows),
+                                   // 128B swizzle: R gate rows, then the R up rows beside them
+  CUtensorMap tm_wd[kMaxBlocks];   // [E*H, I]  box 128 rows x 64 (wide tiles: 256 rows)
   CUtensorMap tm_xperm;            // [R_max, H] box 16x64 (dense MLP: the caller's x [T, H])
   CUtensorMap tm_act;              // [R_max, I] box 16x64
   CUtensorMap tm_xperm128;         // [R_max, H] box 128 rows x 64 (dense MLP: x)

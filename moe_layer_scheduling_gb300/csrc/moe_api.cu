@@ -38,10 +38,13 @@ struct etc_plan_s {
   CUtensorMap tm_xperm{}, tm_act{}, tm_xperm128{}, tm_act128{};
   const void* cached_wgu[kMaxBlocks] = {};
   const void* cached_wd[kMaxBlocks] = {};
-  // w_gate_up with 64-row boxes (narrow and pair tiles: 64 gate rows, then 64 up
-  // rows) and with 128-row boxes (wide tiles); w_down with 128-row boxes
+  // w_gate_up as [E * 2][I][H] (gate half, then up half of each expert): one
+  // box = R gate rows and the R up rows beside them, R = 64 (narrow and pair
+  // tiles) or 128 (wide); w_down [E * H][I] with 128-row (wide: 256-row) boxes
   const void* cached_wgu128[kMaxBlocks] = {};
-  CUtensorMap tm_wgu[kMaxBlocks]{}, tm_wgu128[kMaxBlocks]{}, tm_wd[kMaxBlocks]{};
+  const void* cached_wd256[kMaxBlocks] = {};
+  CUtensorMap tm_wgu[kMaxBlocks]{}, tm_wgu128[kMaxBlocks]{}, tm_wd[kMaxBlocks]{},
+      tm_wd256[kMaxBlocks]{};
   const void* cached_wg[kMaxBlocks] = {};
   CUtensorMap tm_wg[kMaxBlocks]{};
   const void* cached_x = nullptr;  // router input map of the caller's x, per (pointer, T)
@@ -177,27 +180,27 @@ int status_of(etc_plan_t p) {
                    h->code, h->where, h->aux, h->cta);
 }
 
-// Weight maps of block b; `wide`: the gate/up map with 128-row boxes.
+// Weight maps of block b for a call with wide (or narrow / pair) tiles.
 int weight_maps(etc_plan_t p, int b, const void* wgu, const void* wd, bool wide,
-                CUtensorMap* wgu_map) {
-  const unsigned long long rows_gu = static_cast<unsigned long long>(p->E) * 2 * p->I;
-  if (!wide && p->cached_wgu[b] != wgu) {
-    CUresult r = encode_tensor_map_2d_bf16(&p->tm_wgu[b], wgu, p->H, rows_gu, kBK, 64);
+                CUtensorMap* wgu_map, CUtensorMap* wd_map) {
+  const unsigned long long halves = static_cast<unsigned long long>(p->E) * 2;
+  const unsigned long long rows_dn = static_cast<unsigned long long>(p->E) * p->H;
+  const void** cgu = wide ? p->cached_wgu128 : p->cached_wgu;
+  CUtensorMap* mgu = wide ? p->tm_wgu128 : p->tm_wgu;
+  if (cgu[b] != wgu) {
+    CUresult r = encode_tensor_map_3d_bf16(&mgu[b], wgu, p->H, p->I, halves, kBK, wide ? 128 : 64, 2);
     if (r != CUDA_SUCCESS) return set_error(ETC_ERR_CUDA, "tensor map (w_gate_up) failed: %d", r);
-    p->cached_wgu[b] = wgu;
+    cgu[b] = wgu;
   }
-  if (wide && p->cached_wgu128[b] != wgu) {
-    CUresult r = encode_tensor_map_2d_bf16(&p->tm_wgu128[b], wgu, p->H, rows_gu, kBK, 128);
-    if (r != CUDA_SUCCESS) return set_error(ETC_ERR_CUDA, "tensor map (w_gate_up) failed: %d", r);
-    p->cached_wgu128[b] = wgu;
-  }
-  *wgu_map = wide ? p->tm_wgu128[b] : p->tm_wgu[b];
-  if (p->cached_wd[b] != wd) {
-    CUresult r = encode_tensor_map_2d_bf16(&p->tm_wd[b], wd, p->I,
-                                           static_cast<unsigned long long>(p->E) * p->H, kBK, 128);
+  const void** cdn = wide ? p->cached_wd256 : p->cached_wd;
+  CUtensorMap* mdn = wide ? p->tm_wd256 : p->tm_wd;
+  if (cdn[b] != wd) {
+    CUresult r = encode_tensor_map_2d_bf16(&mdn[b], wd, p->I, rows_dn, kBK, wide ? 256 : 128);
     if (r != CUDA_SUCCESS) return set_error(ETC_ERR_CUDA, "tensor map (w_down) failed: %d", r);
-    p->cached_wd[b] = wd;
+    cdn[b] = wd;
   }
+  *wgu_map = mgu[b];
+  *wd_map = mdn[b];
   return ETC_OK;
 }
 
@@ -336,9 +339,8 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
   prm.direct = (prm.thin && prm.nb == 1 && router_tiles) ? 1 : 0;
   if (stage_hi >= TK_GU)
     for (int b = 0; b < a.n_blocks; ++b) {
-      int r = weight_maps(p, b, a.wgu[b], a.wd[b], prm.wide != 0, &prm.tm_wgu[b]);
+      int r = weight_maps(p, b, a.wgu[b], a.wd[b], prm.wide != 0, &prm.tm_wgu[b], &prm.tm_wd[b]);
       if (r != ETC_OK) return r;
-      prm.tm_wd[b] = p->tm_wd[b];
     }
   // Heavy experts: an expert that at least 85 % of the call's tokens chose
   // runs over all T rows of x, its gate/up tiles reading x itself (weight 0
@@ -475,9 +477,8 @@ int run_dense_call(etc_plan_t p, void* stream, const void* x, const void* wgu, c
   prm.NT_gu = p->I / (prm.wide || prm.pair ? kGuRowsW : kGuRows);
   prm.NT_dn = p->H / (prm.wide || prm.pair ? kDnRowsW : kDnRows);
   prm.thin = (!prm.wide && !prm.pair && T <= kTB) ? 1 : 0;  // chunks of at most kTB rows
-  int r = weight_maps(p, 0, wgu, wd, prm.wide != 0, &prm.tm_wgu[0]);
+  int r = weight_maps(p, 0, wgu, wd, prm.wide != 0, &prm.tm_wgu[0], &prm.tm_wd[0]);
   if (r != ETC_OK) return r;
-  prm.tm_wd[0] = p->tm_wd[0];
   prm.dense = 1;
   prm.n_chunks = (T + prm.cw - 1) / prm.cw;
   prm.q_total = prm.n_chunks * (prm.NT_gu + prm.NT_dn);

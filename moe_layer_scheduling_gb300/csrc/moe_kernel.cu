@@ -1668,6 +1668,10 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
     if constexpr (PAIR) tma_load_2d_pair(dst, m, mapa_shared(&c->full[s], 0), x, y);
     else tma_load_2d(dst, m, &c->full[s], x, y);
   };
+  auto load3 = [&](void* dst, const CUtensorMap* m, int s, int x, int y, int z) {
+    if constexpr (PAIR) tma_load_3d_pair(dst, m, mapa_shared(&c->full[s], 0), x, y, z);
+    else tma_load_3d(dst, m, &c->full[s], x, y, z);
+  };
   for (;;) {
     Task t;
     if (!ring_take(c, ri, t, clk, 220) || t.type == TK_TERM) break;
@@ -1716,24 +1720,15 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
     const int brow0 = pair ? src0 + rank * half : src0;
     const int nb16 = pair ? half >> 4 : (t.rows + 15) >> 4;
     const int n128 = nb16 >> 3, r16 = nb16 & 7;  // token rows as 128-row boxes, then 16-row boxes
-    // Weight rows.  Narrow gate/up: 64 gate + 64 up rows (one M=128 operand,
-    // two 64-row boxes); wide: 128 gate rows, then 128 up rows (two operands,
-    // two 128-row boxes); pair: 64 gate + 64 up rows of this CTA's half of the
-    // 128 intermediate columns (two 64-row boxes); down tiles: 128 (wide: 256)
-    // consecutive output rows of w_down (128-row boxes).
+    // Weight rows, one box per K step.  Gate/up: R gate rows and the R up
+    // rows beside them (3-D box, gate block then up block): R = 64 narrow (one
+    // M=128 operand) and pair (this CTA's half of the 128 intermediate
+    // columns), 128 wide (two operands).  Down tiles: 128 (wide: 256)
+    // consecutive output rows of w_down.
     const bool wide = p.wide != 0;
-    const int nA = wide ? 4 : 2;
-    int rowA[4];
-    if (gu) {
-      const int g0 = t.e * 2 * p.I + (pair ? t.b * 2 * kGuRows + kGuRows * rank : t.b * (wide ? kGuRowsW : kGuRows));
-      rowA[0] = g0;
-      rowA[1] = wide ? g0 + 64 : g0 + p.I;
-      rowA[2] = g0 + p.I;
-      rowA[3] = g0 + p.I + 64;
-    } else {
-      const int r0 = t.e * p.H + (pair ? t.b * kDnRowsW + kDnRows * rank : t.b * (wide ? kDnRowsW : kDnRows));
-      for (int i = 0; i < 4; ++i) rowA[i] = r0 + 64 * i;
-    }
+    const int nA = wide ? 4 : 2;  // 64-row weight blocks per K step
+    const int i0 = gu ? (pair ? t.b * 2 * kGuRows + kGuRows * rank : t.b * (wide ? kGuRowsW : kGuRows)) : 0;
+    const int r0 = gu ? 0 : t.e * p.H + (pair ? t.b * kDnRowsW + kDnRows * rank : t.b * (wide ? kDnRowsW : kDnRows));
     // Direct mode: a gate/up tile's token operand is all T (<= 32) rows of x,
     // one 32-row box (rows past T read as zero).
     const bool direct_x = gu && p.direct;
@@ -1745,13 +1740,8 @@ __device__ void run_producer(const MegaParams& p, Ctrl* c, uint8_t* base, const 
       uint8_t* sa = base + s * g.bytes;
       uint8_t* sb = sa + g.boff;
       if (announce) mbar_arrive_expect_tx(&c->full[s], bytes * tx_mul);
-      if (gu && !wide) {
-        load(sa, ta, s, kb * kBK, rowA[0]);
-        load(sa + kOpABytes / 2, ta, s, kb * kBK, rowA[1]);
-      } else {
-        load(sa, ta, s, kb * kBK, rowA[0]);
-        if (wide) load(sa + kOpABytes, ta, s, kb * kBK, rowA[2]);
-      }
+      if (gu) load3(sa, ta, s, kb * kBK, i0, 2 * t.e);
+      else load(sa, ta, s, kb * kBK, r0);
       if (direct_x) {
         load(sb, &p.tm_xr, s, kb * kBK, 0);
         continue;
