@@ -27,6 +27,7 @@ ETC_DEBUG_POISON = 0x2
 ETC_DEBUG_NO_PAIR = 0x8
 ETC_DEBUG_PAIR_MOE = 0x10
 ETC_DEBUG_NO_HEAVY = 0x20
+ETC_DEBUG_WIDE_SWAP_AB = 0x40
 ETC_OUT_F32 = 0
 ETC_OUT_BF16 = 1
 ETC_COMBINE_FUSED = 0

@@ -325,6 +325,7 @@ int run_call(etc_plan_t p, void* stream, const CallArgs& a, bool unfused, int st
               (p->opts.debug_flags & ETC_DEBUG_PAIR_MOE) && !(p->opts.debug_flags & ETC_DEBUG_NO_PAIR))
                  ? 1 : 0;
   if (prm.pair) prm.wide = 0;
+  prm.tokmaj = (prm.wide && !(p->opts.debug_flags & ETC_DEBUG_WIDE_SWAP_AB)) ? 1 : 0;
   prm.cw = prm.pair ? kBT2 : kBT;
   prm.nbp = prm.pair ? (prm.nb + 1) / 2 : prm.nb;
   prm.ev_mul = prm.pair ? 2 : 1;
@@ -471,6 +472,7 @@ int run_dense_call(etc_plan_t p, void* stream, const void* x, const void* wgu, c
   prm.wide = (T >= 64 && p->I % kGuRowsW == 0 && p->H % kDnRowsW == 0) ? 1 : 0;
   prm.pair = (prm.wide && p->pair_grid > 0 && !(p->opts.debug_flags & ETC_DEBUG_NO_PAIR)) ? 1 : 0;
   if (prm.pair) prm.wide = 0;
+  prm.tokmaj = (prm.wide && !(p->opts.debug_flags & ETC_DEBUG_WIDE_SWAP_AB)) ? 1 : 0;
   prm.cw = prm.pair ? kBT2 : kBT;
   prm.nbp = prm.nb;
   prm.ev_mul = prm.pair ? 2 : 1;

@@ -1166,7 +1166,32 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
   // columns (down) of the pair's tile; the accumulator holds all chunk rows.
   const int rank = pair_rank(p);
   if (ok) {
-    if (t.type == TK_GU && p.wide) {
+    if (t.type == TK_GU && p.tokmaj) {
+      // Token-major: TMEM lane = chunk row, columns 0-127 gate and 128-255 up
+      // of the tile's 128 intermediate columns; each worker half takes 64 of
+      // them, so a thread writes one 128-byte piece of its row's act.
+      const int r = 32 * q + lane;
+      __nv_bfloat16* arow = p.ws.act + static_cast<size_t>(t.row0 + r) * p.I + t.b * kGuRowsW + 64 * h;
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        float g[16], u[16];
+        tmem_ld16(tbase + 64 * h + 16 * cb, g);
+        tmem_ld16(tbase + kGuRowsW + 64 * h + 16 * cb, u);
+        if (r < t.rows) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float a0 = g[2 * i] / (1.0f + __expf(-g[2 * i])) * u[2 * i];
+            const float a1 = g[2 * i + 1] / (1.0f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
+            pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(arow + 16 * cb);
+          store_act(p, dst, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+          store_act(p, dst + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]));
+        }
+      }
+    } else if (t.type == TK_GU && p.wide) {
       // Wide: gate rows in the buffer's first half, up rows in its second;
       // lane = intermediate column, so SwiGLU pairs them in registers.
       for (int cb = h; cb < ncb; cb += 2) {
@@ -1248,6 +1273,55 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
                                                 gcol + chunk * 8), val);
         }
         named_bar(2 + h, 128);
+      }
+    } else if (p.tokmaj) {
+      // Token-major down tile: TMEM lane = chunk row, columns = the tile's 256
+      // output columns; each worker half takes 128 of them.  A thread holds
+      // 16 consecutive output columns of its row per load: the weighted
+      // combine adds them with four 16-byte reductions (the ordered combine
+      // and the dense MLP store them).
+      const int r = 32 * q + lane;
+      const int col0 = t.b * kDnRowsW + 128 * h;
+      const bool live = r < t.rows;
+      const int tok = fused_comb && live ? s_rtok[r] : -1;
+      const float wr = fused_comb && live ? s_rw[r] : 0.f;
+      float* accr = fused_comb ? acc_rows(p, t.blk) : nullptr;
+#pragma unroll 1
+      for (int cb = 0; cb < 8; ++cb) {
+        float v[16];
+        tmem_ld16(tbase + 128 * h + 16 * cb, v);
+        const int col = col0 + 16 * cb;
+        if (fused_comb) {
+          if (tok >= 0) {
+            float* dst = accr + static_cast<size_t>(tok) * p.H + col;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              red_add_v4(dst + 4 * i, make_float4(wr * v[4 * i], wr * v[4 * i + 1], wr * v[4 * i + 2],
+                                                  wr * v[4 * i + 3]));
+          }
+        } else if (live && p.ordered) {
+          float4* dst = reinterpret_cast<float4*>(p.ws.yperm + static_cast<size_t>(t.pad + r) * p.H + col);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        } else if (live) {
+          const size_t o = static_cast<size_t>(t.row0 + r) * p.H + col;
+          if (p.out_bf16) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+              pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + o);
+            __stcs(dst, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+            __stcs(dst + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]));
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              __stcs(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+          }
+        }
       }
     } else {
       // Down tile: TMEM lane = output column, TMEM column = chunk row.  Each
@@ -1780,8 +1854,13 @@ __device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock
     const int ncol = (t.type == TK_GU && p.direct) ? p.T : t.rows;
     const int npad = rt ? (pair ? 2 * kTB : kTB) : pair ? pair_npad(ncol) : (ncol + 15) & ~15;
     const int M = pair ? 256 : 128;
+    // Token-major wide tiles: M = 128 token rows (rows past the chunk are
+    // don't-care lanes), N = the 256 weight rows.
+    const bool tmaj = !rt && p.tokmaj;
     // Router tiles read A (the router weight) MN-major; expert tiles K-major.
-    const uint32_t idesc = rt ? idesc_bf16_f32_amn(M, npad) : idesc_bf16_f32(M, npad);
+    const uint32_t idesc = rt     ? idesc_bf16_f32_amn(M, npad)
+                           : tmaj ? idesc_bf16_f32(128, 2 * kGuRowsW)
+                                  : idesc_bf16_f32(M, npad);
     const int KB = rt ? p.KBr * (p.use_norm ? 2 : 1) : (t.type == TK_GU ? p.H : p.I) / kBK;
     const int per = rt ? router_kpack(g) : 1;  // K blocks per stage
     for (int kb = 0; kb < KB; kb += per, st = st + 1 == g.n ? (ph ^= 1, 0) : st + 1) {
@@ -1810,6 +1889,12 @@ __device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock
           for (int kk = 0; kk < kBK / 16; ++kk)
             umma_bf16(d, ad + kk * (2048 >> 4), bdu + 2 * kk, idesc, (kb | u | kk) != 0 ? 1u : 0u);
         }
+      } else if (tmaj) {
+        // A = the token rows (the stage's token part), B = all 256 weight rows
+        const uint64_t ta = desc_kmajor_sw128(sa + g.boff), wb = desc_kmajor_sw128(sa);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          umma_bf16(d, ta + 2 * kk, wb + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
       } else {
         const uint64_t ad = desc_kmajor_sw128(sa);
 #pragma unroll
