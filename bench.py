@@ -5,9 +5,10 @@ MoE layer (hidden 2048, 128 experts, top-8, intermediate 768, SwiGLU),
 prefill T=4096 with Zipf(1.2)-skewed routing, bf16 weights, fp32 accumulation,
 synthetic seeded inputs.  A step is one MoE layer forward (router, top-k,
 counts/exp_indptr scan, permute, GroupGEMM gate/up+SwiGLU, GroupGEMM down,
-combine) = ONE kernel launch of the megakernel, static-scheduled by default
-(--sched dynamic or mixed for the other schedulers; every one of them is also
-timed in the ablation).
+combine) = ONE kernel launch of the megakernel; the benchmark line takes the
+mixed scheduler (routing walked statically, expert tiles from the queue), the
+fastest of the three on this workload (--sched static or dynamic for the
+others; every one of them is also timed in the ablation).
 
 One JSON line on stdout (rank 0).  Extra keys report the decode sizes,
 the static/dynamic/unfused ablation, the split-K task graph and the chain.
@@ -41,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of ONE launch of the
-# benchmark line's kernel (static scheduler, prefill T=4096), from one ncu capture.
+# benchmark line's kernel (mixed scheduler, prefill T=4096), from one ncu capture.
 # Valid only for the kernel sources it was taken on: reported as null once any
 # of them changes.
 MEGAKERNEL_SOURCES = ("moe_kernel.cu", "moe_api.cu", "etc_internal.h", "etc_event.cuh", "etc_ptx.cuh")
@@ -415,10 +416,14 @@ def run_extras(args, dev, weights, gw, wgu, wd, bias, x, out, T, plans, peaks, w
     abl["unfused_per_stage"] = {"us": sec * 1e6, "tflops": T * FLOPS_PER_TOKEN / sec / 1e12}
     for name in ("static", "dynamic", "mixed"):
         abl[name]["vs_unfused"] = abl["unfused_per_stage"]["us"] / abl[name]["us"]
-    # the same static call on CTA-pair tiles, and with the ordered (deterministic) combine
-    for name, kw in (("static_pair_tiles", dict(debug_flags=B.ETC_DEBUG_PAIR_MOE)),
-                     ("static_ordered_combine", dict(combine=B.ETC_COMBINE_ORDERED))):
-        pv = B.etc_moe_plan(H, E, K, I, t_max=T, sched=B.ETC_SCHED_STATIC, router_bias=bias, **kw)
+    # the same call on CTA-pair tiles, with the ordered (deterministic) combine,
+    # with swap-AB wide tiles, and (mixed) without heavy experts
+    for name, sched, kw in (
+            ("static_pair_tiles", B.ETC_SCHED_STATIC, dict(debug_flags=B.ETC_DEBUG_PAIR_MOE)),
+            ("static_ordered_combine", B.ETC_SCHED_STATIC, dict(combine=B.ETC_COMBINE_ORDERED)),
+            ("static_swap_ab_wide_tiles", B.ETC_SCHED_STATIC, dict(debug_flags=B.ETC_DEBUG_WIDE_SWAP_AB)),
+            ("mixed_no_heavy_experts", B.ETC_SCHED_MIXED, dict(debug_flags=B.ETC_DEBUG_NO_HEAVY))):
+        pv = B.etc_moe_plan(H, E, K, I, t_max=T, sched=sched, router_bias=bias, **kw)
         sec = time_gpu(lambda: B.etc_moe_forward(pv, x, gw, wgu, wd, T, out), steps, 3, world)
         assert B.etc_plan_check(pv) == B.ETC_OK, B.etc_last_error()
         abl[name] = {"us": sec * 1e6, "tflops": T * FLOPS_PER_TOKEN / sec / 1e12}
@@ -658,8 +663,9 @@ def main():
     ap.add_argument("--workload", default="prefill", choices=["prefill", "decode", "splitk", "mlp"],
                     help="prefill = the benchmark line; decode/splitk/mlp = one workload (profiling)")
     ap.add_argument("--mlp", default="MLP-1", help="Table 4 shape for --workload mlp")
-    ap.add_argument("--sched", default="static", choices=["static", "dynamic", "mixed"],
-                    help="scheduler of the benchmark line (prefill) or of the single workload")
+    ap.add_argument("--sched", default=None, choices=["static", "dynamic", "mixed"],
+                    help="scheduler of the benchmark line (prefill; default mixed) or of the single "
+                         "workload (default static)")
     ap.add_argument("--tiles", default="default", choices=["default", "single"],
                     help="--workload mlp: 'single' runs its wide tiles on single CTAs instead of CTA "
                          "pairs (the form ncu can capture: it cannot launch the pair kernel's "
@@ -667,6 +673,8 @@ def main():
     ap.add_argument("--clock-window", type=float, default=1.5,
                     help="seconds of load kept up for the clock record (0 for profiler runs)")
     args = ap.parse_args()
+    if args.sched is None:
+        args.sched = "mixed" if args.workload == "prefill" and args.impl == "ours" else "static"
     rank, world, _ = dist_init()
     if args.impl == "reference":
         line = run_reference(args, rank, world)
