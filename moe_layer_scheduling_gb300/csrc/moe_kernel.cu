@@ -925,9 +925,9 @@ __device__ void init_acc_rows(const MegaParams& p, int blk, int tb, int wt, uint
 // spreads the copies of few blocks over more CTAs) into x_perm at
 // exp_indptr[e] + rank, records each row's token and routing weight, and the
 // part's expert histogram (what its notify takes off ev_expert).  The rows
-// move through shared memory with the bulk-copy engine: worker thread 0 reads
-// each token row once (kPermSlots rows in flight) and stores it to its k
-// expert-sorted rows.
+// move through shared memory with the bulk-copy engine: each token row is
+// read once (kPermSlots rows in flight) and stored to its k expert-sorted
+// rows by k lanes of worker warp 0.
 __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* simt, int wt,
                           uint32_t& li, const Clock& clk) {
   const int blk = t.blk, tb = my_tb(p, t.a), part = t.b;
@@ -1013,21 +1013,38 @@ __device__ void task_perm(const MegaParams& p, Ctrl* c, const Task& t, uint8_t* 
   if (tb < p.nb)
     for (int e = wt; e < E; e += kNumWorkers)  // (a heavy expert waits for no rows)
       B.part_cnt[(tb * p.PP + part) * E + e] = s_heavy[e] ? 0 : s_pcnt[e];
-  if (wt == 0) {
-    for (int r = 0; r < nmine; ++r) {
-      const uint32_t L = li + r;
-      const int sl = L % nslot;
-      if (!mbar_wait(&c->pbar[sl], (L / nslot) & 1, clk, 270)) break;
-      const uint8_t* srow = rows + sl * RB;
-      for (int j = 0; j < k; ++j)
-        if (!s_heavy[s_ids[(r_lo + r) * k + j]])  // (a heavy expert's tiles read x itself)
-          bulk_store(p.ws.x_perm + static_cast<size_t>(s_slot[(r_lo + r) * k + j]) * p.H, srow, RB);
-      bulk_commit();
-      const int nx = r + nslot;
-      if (nx < nmine) {
-        bulk_wait_read_all();  // the slot's row has been read out before it is refilled
-        mbar_arrive_expect_tx(&c->pbar[sl], RB);
-        bulk_load(rows + sl * RB, src + static_cast<size_t>(t0 + r_lo + nx) * p.H, RB, &c->pbar[sl]);
+  if (wt < 32) {
+    // Warp 0 issues the copies: G groups of k lanes take every G-th row, lane
+    // j of a group storing the row's slot j (one thread issuing all of them
+    // measured 20 % slower); the group's first lane refills the row's shared
+    // memory slot once the group's stores have read it.  G divides nslot, so
+    // the rows that share a slot (nslot apart) fall to one group, which waits
+    // for each of the slot's loads in turn (a parity wait could not tell a
+    // load two phases ahead from the one before it).
+    int G = 32 / k;
+    while (nslot % G) --G;
+    const int lane = wt, g = lane / k, j = lane - g * k;
+    if (g < G) {
+      const unsigned gm = (k >= 32 ? 0xffffffffu : ((1u << k) - 1u)) << (g * k);
+      for (int r = g; r < nmine; r += G) {
+        const uint32_t L = li + r;
+        const int sl = L % nslot;
+        const bool got = mbar_wait(&c->pbar[sl], (L / nslot) & 1, clk, 270);
+        if (!__all_sync(gm, got)) break;
+        const uint8_t* srow = rows + sl * RB;
+        const int i = (r_lo + r) * k + j;
+        if (!s_heavy[s_ids[i]])  // (a heavy expert's tiles read x itself)
+          bulk_store(p.ws.x_perm + static_cast<size_t>(s_slot[i]) * p.H, srow, RB);
+        bulk_commit();
+        const int nx = r + nslot;
+        if (nx < nmine) {
+          bulk_wait_read_all();  // the slot's row has been read out before it is refilled
+          __syncwarp(gm);
+          if (j == 0) {
+            mbar_arrive_expect_tx(&c->pbar[sl], RB);
+            bulk_load(rows + sl * RB, src + static_cast<size_t>(t0 + r_lo + nx) * p.H, RB, &c->pbar[sl]);
+          }
+        }
       }
     }
     bulk_wait_all();  // x_perm rows written before the notify
