@@ -630,7 +630,7 @@ __device__ void task_router_epilogue(const MegaParams& p, Ctrl* c, uint8_t* simt
     named_bar(1, kNumWorkers);
     publish_block_counts(p, B, tb, s_cnt, wt);
   }
-  if (zero_rows && wt == 0) {
+  if (zero_rows && wt < 32) {
     bulk_wait_all();             // the zeroed rows are written
     fence_proxy_async_global();  // before any down tile adds into them
   }
@@ -894,16 +894,16 @@ __device__ void init_acc_rows(const MegaParams& p, int blk, int tb, int wt, uint
   const int ww = wt >> 5, lane = wt & 31, n8 = p.H / 8, t0 = tb * kTB, ntok = min(kTB, p.T - t0);
   if (zbuf != nullptr && !p.use_norm) {
     // Zeros, written by the bulk-copy engine from kZeroBytes of zeroed shared
-    // memory (worker thread 0 issues the copies and waits for them before the
-    // task's notify): the workers go on to the tile's epilogue at once.
+    // memory (the lanes of worker warp 0 issue the copies and wait for them
+    // before the task's notify): the workers go on to the tile's epilogue.
     for (int i = wt; i < kZeroBytes / 16; i += kNumWorkers)
       reinterpret_cast<uint4*>(zbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();  // visible to the bulk-copy engine
     named_bar(1, kNumWorkers);
-    if (wt == 0 && ntok > 0) {
+    if (wt < 32 && ntok > 0) {
       uint8_t* dst = reinterpret_cast<uint8_t*>(accr + static_cast<size_t>(t0) * p.H);
       const uint32_t total = static_cast<uint32_t>(ntok) * static_cast<uint32_t>(p.H) * 4u;
-      for (uint32_t off = 0; off < total; off += kZeroBytes)
+      for (uint32_t off = wt * kZeroBytes; off < total; off += 32 * kZeroBytes)
         bulk_store(dst + off, zbuf, min(static_cast<uint32_t>(kZeroBytes), total - off));
       bulk_commit();
     }
