@@ -77,9 +77,9 @@ typedef enum { ETC_SCHED_STATIC = 0, ETC_SCHED_DYNAMIC = 1, ETC_SCHED_MIXED = 2 
 #define ETC_DEBUG_PAIR_MOE 0x10u        /* run the wide expert tiles of MoE calls on CTA pairs too
                                            (by default only the dense MLP uses them: on the MoE
                                            layer's skewed chunks they measured no faster) */
-#define ETC_DEBUG_WIDE_SWAP_AB 0x40u    /* wide expert tiles with the weight rows as the MMA's M
-                                           (two M=128 x N=128 MMAs per K step) instead of the
-                                           token rows (one M=128 x N=256 MMA); ablation */
+#define ETC_DEBUG_WIDE_SWAP_AB 0x40u    /* wide gate/up tiles of full chunks with the weight rows as
+                                           the MMA's M (two M=128 x N=128 MMAs per K step) instead of
+                                           the token rows (one M=128 x N=256 MMA); ablation */
 #define ETC_DEBUG_NO_HEAVY 0x20u        /* never run an expert over all T rows of x (by default, in
                                            dynamic and mixed scheduling, an expert that >= 85 % of a
                                            large call's tokens chose does, its tiles needing no

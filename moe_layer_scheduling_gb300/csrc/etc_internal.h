@@ -196,8 +196,9 @@ struct MegaParams {
   int ev_mul;    // notifies per tile or routing task (2 with pair tiles: one per CTA)
   int thin;      // narrow tiles whose chunks hold at most kTB rows: 20 KB stages
   int direct;    // one token block: gate/up tiles read all T token rows of x (no permute)
-  int tokmaj;    // wide tiles token-major: M = the chunk's 128 token rows, N = 256 weight
-                 // rows (one N=256 MMA per K step); else swap-AB (M = weight rows)
+  int tokmaj;    // wide gate/up tiles of full chunks token-major: M = the chunk's 128 token
+                 // rows, N = 256 weight rows (one N=256 MMA per K step); other expert tiles
+                 // swap-AB (M = weight rows, N = chunk rows)
   int heavy_min; // > 0: experts with at least this many rows run over all T rows of x,
                  // their tiles reading x itself (ready as soon as the scan has run); 0: off
   unsigned epoch;

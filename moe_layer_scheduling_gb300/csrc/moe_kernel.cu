@@ -166,6 +166,14 @@ __device__ __forceinline__ StageGeom stage_geom(const MegaParams& p) {
                   : StageGeom{kStagesNarrow, kOpABytes + kStageBBytes, kOpABytes};
 }
 
+// Token-major MMA for this expert tile: wide gate/up tiles of full chunks
+// (one M=128 x N=256 MMA per K step).  Partial chunks and down tiles measured
+// faster swap-AB (M = weight rows, N = the chunk's rows rounded to 16; down
+// tiles: the epilogue's coalesced reductions).
+__device__ __forceinline__ bool tile_tokmaj(const MegaParams& p, const Task& t) {
+  return p.tokmaj && t.type == TK_GU && t.rows == p.cw;
+}
+
 // K blocks of a router tile per operand stage: two when the stage holds two
 // (weights 16 KB + 32 token rows 4 KB per K block: the wide geometry).
 __device__ __forceinline__ int router_kpack(const StageGeom& g) {
@@ -1183,7 +1191,7 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
   // columns (down) of the pair's tile; the accumulator holds all chunk rows.
   const int rank = pair_rank(p);
   if (ok) {
-    if (t.type == TK_GU && p.tokmaj) {
+    if (t.type == TK_GU && tile_tokmaj(p, t)) {
       // Token-major: TMEM lane = chunk row, columns 0-127 gate and 128-255 up
       // of the tile's 128 intermediate columns; each worker half takes 64 of
       // them, so a thread writes one 128-byte piece of its row's act.
@@ -1290,55 +1298,6 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
                                                 gcol + chunk * 8), val);
         }
         named_bar(2 + h, 128);
-      }
-    } else if (p.tokmaj) {
-      // Token-major down tile: TMEM lane = chunk row, columns = the tile's 256
-      // output columns; each worker half takes 128 of them.  A thread holds
-      // 16 consecutive output columns of its row per load: the weighted
-      // combine adds them with four 16-byte reductions (the ordered combine
-      // and the dense MLP store them).
-      const int r = 32 * q + lane;
-      const int col0 = t.b * kDnRowsW + 128 * h;
-      const bool live = r < t.rows;
-      const int tok = fused_comb && live ? s_rtok[r] : -1;
-      const float wr = fused_comb && live ? s_rw[r] : 0.f;
-      float* accr = fused_comb ? acc_rows(p, t.blk) : nullptr;
-#pragma unroll 1
-      for (int cb = 0; cb < 8; ++cb) {
-        float v[16];
-        tmem_ld16(tbase + 128 * h + 16 * cb, v);
-        const int col = col0 + 16 * cb;
-        if (fused_comb) {
-          if (tok >= 0) {
-            float* dst = accr + static_cast<size_t>(tok) * p.H + col;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              red_add_v4(dst + 4 * i, make_float4(wr * v[4 * i], wr * v[4 * i + 1], wr * v[4 * i + 2],
-                                                  wr * v[4 * i + 3]));
-          }
-        } else if (live && p.ordered) {
-          float4* dst = reinterpret_cast<float4*>(p.ws.yperm + static_cast<size_t>(t.pad + r) * p.H + col);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        } else if (live) {
-          const size_t o = static_cast<size_t>(t.row0 + r) * p.H + col;
-          if (p.out_bf16) {
-            uint32_t pk[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-              pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + o);
-            __stcs(dst, make_uint4(pk[0], pk[1], pk[2], pk[3]));
-            __stcs(dst + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]));
-          } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              __stcs(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
-          }
-        }
       }
     } else {
       // Down tile: TMEM lane = output column, TMEM column = chunk row.  Each
@@ -1873,7 +1832,7 @@ __device__ void run_mma(const MegaParams& p, Ctrl* c, uint8_t* base, const Clock
     const int M = pair ? 256 : 128;
     // Token-major wide tiles: M = 128 token rows (rows past the chunk are
     // don't-care lanes), N = the 256 weight rows.
-    const bool tmaj = !rt && p.tokmaj;
+    const bool tmaj = !rt && tile_tokmaj(p, t);
     // Router tiles read A (the router weight) MN-major; expert tiles K-major.
     const uint32_t idesc = rt     ? idesc_bf16_f32_amn(M, npad)
                            : tmaj ? idesc_bf16_f32(128, 2 * kGuRowsW)
