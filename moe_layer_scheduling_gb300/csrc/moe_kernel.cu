@@ -494,6 +494,7 @@ constexpr int kSelBytes = 4 * kTB * kMaxK;  // a block's selected experts (or we
 constexpr int kSelOff = kDirectOff + 4 * kMaxE;  // the top-k's selection, kept for the scan
 constexpr int kGatherOff = 16 * 1024;       // direct mode: gate/up activations of all T tokens
 constexpr int kZeroOff = 30 * 1024;         // router tiles: zeros for the block's output rows
+constexpr int kDirectTokOff = 20 * 1024;    // direct-mode gate/up tiles: the chunk rows' tokens
 constexpr int kZeroBytes = 2 * 1024;
 static_assert(kSelOff + 2 * kSelBytes <= kZeroOff && kZeroOff + kZeroBytes <= kSimtBytes,
               "SIMT scratch layout");
@@ -1152,6 +1153,11 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
   int* s_rtok = reinterpret_cast<int*>(simt + 2 * kEpiHalfBytes);                 // [256]
   float* s_rw = reinterpret_cast<float*>(simt + 2 * kEpiHalfBytes + 4 * kBT2);    // [256]
   const bool fused_comb = t.type == TK_DN && !p.dense && !p.ordered;
+  // Direct-mode gate/up tiles: each chunk row's token, read while the tile
+  // is still on the tensor cores (the scan wrote them before the tile ran).
+  int* s_dtok = reinterpret_cast<int*>(simt + kDirectTokOff);  // [kTB]
+  if (t.type == TK_GU && p.direct)
+    for (int i = wt; i < t.rows; i += kNumWorkers) s_dtok[i] = __ldcg(B.row_token + t.pad + i);
   if (fused_comb) {
     if (t.pad >= 0) {
       for (int r = wt; r < t.rows; r += kNumWorkers) {
@@ -1266,7 +1272,7 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
       named_bar(1, kNumWorkers);
       for (int idx = wt; idx < t.rows * 8; idx += kNumWorkers) {
         const int i = idx >> 3, chunk = idx & 7;
-        const int tok = __ldcg(B.row_token + t.pad + i);
+        const int tok = s_dtok[i];
         const uint4 val = *reinterpret_cast<const uint4*>(SA + tok * 64 + chunk * 8);
         store_act(p, reinterpret_cast<uint4*>(p.ws.act + static_cast<size_t>(t.row0 + i) * p.I +
                                               t.b * kGuRows + chunk * 8), val);
