@@ -222,25 +222,9 @@ __device__ __forceinline__ void load_block_input8(const MegaParams& p, int blk, 
   }
 }
 
-// Exclusive prefix sum over the 256 worker threads; `tmp` holds >= 8 values.
-// (64-bit, so that two 32-bit sums can travel packed in one scan.)
-__device__ __forceinline__ unsigned long long workers_excl_scan(unsigned long long v,
-                                                                unsigned long long* tmp, int wt) {
-  const int lane = wt & 31, w = wt >> 5;
-  unsigned long long x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) tmp[w] = x;
-  named_bar(1, kNumWorkers);
-  unsigned long long base = 0;
-  for (int i = 0; i < w; ++i) base += tmp[i];
-  named_bar(1, kNumWorkers);
-  return base + x - v;
-}
-// The same, also giving every thread the sum over all 256 values.
+// Exclusive prefix sum over the 256 worker threads (64-bit, so that two 32-bit
+// sums can travel packed in one scan), also giving every thread the sum over
+// all 256 values; `tmp` holds >= 8 values.
 __device__ __forceinline__ unsigned long long workers_excl_scan_total(unsigned long long v,
                                                                       unsigned long long* tmp, int wt,
                                                                       unsigned long long& total) {
