@@ -274,6 +274,22 @@ def test_heavy_experts(oracle_lib, sched):
     assert diff <= 1e-5 * np.max(np.abs(out_p)), diff
 
 
+@pytest.mark.parametrize("flags", [0, B.ETC_DEBUG_WIDE_SWAP_AB, B.ETC_DEBUG_NO_HEAVY,
+                                   B.ETC_DEBUG_WIDE_SWAP_AB | B.ETC_DEBUG_NO_HEAVY],
+                         ids=["default", "swap_ab", "no_heavy", "swap_ab_no_heavy"])
+@pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_MIXED], ids=["static", "mixed"])
+def test_wide_tile_forms(oracle_lib, sched, flags):
+    # Wide tiles in every form the flags select: full chunks token-major or
+    # swap-AB, with and without a heavy expert (expert 3 takes every token),
+    # several full 128-row chunks and ragged ones; all against the oracle.
+    w = inputs.moe_weights(512, 16, 4, 256, seed=41)
+    bias = inputs.zipf_bias(16, 1.2, 41)
+    bias[3] = 40.0
+    w.router_bias = bias
+    x = inputs.tokens(700, 512, 42)
+    _full_check(oracle_lib, w, x, sched, False, debug_flags=flags)
+
+
 def test_identical_experts_closed_form(oracle_lib):
     # Routing-independent closed form: with every expert equal the layer is one FFN.
     w = inputs.moe_weights(256, 16, 4, 128, seed=23)
