@@ -3,7 +3,8 @@
 Runs one MoE layer with the library's ETC_DEBUG_TRACE flag and prints, per
 task type, how many tasks ran, their summed and mean busy time on the worker
 warps, and when the stage started and ended relative to the first task;
-also the time from the first to the last task and how busy the SMs were.
+also the time from the first to the last task and how busy the SMs' workers
+were, over the whole call and per 20 us window.
 
     python -m moe_layer_scheduling_gb300.trace --tokens 4096 --skew --sched dynamic
     python -m moe_layer_scheduling_gb300.trace --mlp MLP-1 --sched static   # dense MLP
@@ -15,7 +16,7 @@ import json
 from collections import defaultdict
 
 
-def summarize(recs: list[dict]) -> dict:
+def summarize(recs: list[dict], window_ns: int = 20000) -> dict:
     if not recs:
         return {}
     t0 = min(r["t_dispatch"] or r["t_start"] for r in recs)
@@ -38,8 +39,20 @@ def summarize(recs: list[dict]) -> dict:
     sms = {r["sm"] for r in recs}
     busy_total = sum(r["t_end"] - r["t_start"] for r in recs)
     span = t_end - t0
+    # fraction of the SMs' workers inside a task, per window of the call
+    win = window_ns if span > window_ns else max(span, 1)
+    n_win = max(1, -(-span // win))
+    busy_win = [0.0] * n_win
+    for r in recs:
+        a, b = r["t_start"] - t0, r["t_end"] - t0
+        for i in range(max(0, a // win), min(n_win, b // win + 1)):
+            lo, hi = i * win, (i + 1) * win
+            busy_win[i] += max(0, min(b, hi) - max(a, lo))
+    n_sm = max(len(sms), 1)
     return {"span_us": span / 1e3, "sms": len(sms),
-            "worker_busy_frac": busy_total / (span * max(len(sms), 1)) if span else None,
+            "worker_busy_frac": busy_total / (span * n_sm) if span else None,
+            "busy_frac_per_window": {"window_us": win / 1e3,
+                                     "values": [round(v / (win * n_sm), 2) for v in busy_win]},
             "stages": stages}
 
 

@@ -45,3 +45,16 @@ def test_summarize_spans_and_busy_fractions():
     assert d["queue_us_mean"] is None  # no dispatch time recorded
     assert d["last_end_us"] == pytest.approx(4.0)
     assert summarize([]) == {}
+
+
+def test_summarize_busy_fraction_per_window():
+    # two SMs, 20 us windows: [0, 20) holds 20 + 10 us of task time, [20, 40)
+    # 10 + 20 us, [40, 60) 10 us (of 2 x 20 us each)
+    recs = [dict(type="router", block=0, sm=0, a=0, b=0, t_dispatch=0, t_start=0, t_end=30000),
+            dict(type="gate_up", block=0, sm=1, a=0, b=0, t_dispatch=0, t_start=10000, t_end=50000)]
+    w = summarize(recs)["busy_frac_per_window"]
+    assert w["window_us"] == pytest.approx(20.0)
+    assert w["values"] == [0.75, 0.75, 0.25]
+    # a call shorter than one window: one window of its own length
+    w = summarize(recs[:1], window_ns=100000)["busy_frac_per_window"]
+    assert w["window_us"] == pytest.approx(30.0) and w["values"] == [1.0]
