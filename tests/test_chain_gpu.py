@@ -133,3 +133,37 @@ def test_chain_plan_entry_point(oracle_lib, blocks, blocks_dev):
     out = _run_chain(plan, bd, x)
     _check_chain(plan, blocks[:2], x, out, oracle_lib)
     plan.close()
+
+
+def _draw_chain(seed):
+    """A seeded chain shape within the library's limits: 1-4 blocks, H, E, k, I, T."""
+    rng = np.random.default_rng(3000 + seed)
+    H = int(rng.choice([128, 256, 512, 1024]))
+    E = int(rng.choice([8, 16, 64, 128]))
+    k = int(rng.integers(1, min(E, 8) + 1))
+    I = int(rng.choice([64, 128, 256, 384]))
+    nb = int(rng.integers(1, 5))
+    T = int(rng.choice([int(rng.integers(1, 33)), int(rng.integers(33, 400))]))
+    # keep the fp64 oracle and the weight draws within a few seconds
+    while T > 1 and T * k * H * I * 3 * nb > 3e9:
+        T //= 2
+    while E > 8 and E * I * H * nb > 2e8:
+        E //= 2
+    k = min(k, E)
+    sched = B.ETC_SCHED_DYNAMIC if rng.integers(0, 2) else B.ETC_SCHED_STATIC
+    return H, E, k, I, nb, T, sched
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_chain_random_shape(oracle_lib, seed):
+    """Seeded chain shapes (blocks, H, E, k, I, T, schedule) against the oracle,
+    every block and every token, through the same check as the fixed shape."""
+    H, E, k, I, nb, T, sched = _draw_chain(seed)
+    blocks = inputs.chain_blocks(nb, hidden=H, n_experts=E, top_k=k, inter=I)
+    bd = dict(norm=[b.norm_w.cuda() for b in blocks], gate=[b.gate_w.cuda() for b in blocks],
+              gu=[b.w_gate_up.cuda() for b in blocks], dn=[b.w_down.cuda() for b in blocks])
+    plan = B.etc_moe_plan(H, E, k, I, t_max=T, sched=sched, n_blocks=nb)
+    x = inputs.tokens(T, H, 7300 + seed)
+    out = _run_chain(plan, bd, x)
+    _check_chain(plan, blocks, x, out, oracle_lib)
+    plan.close()
