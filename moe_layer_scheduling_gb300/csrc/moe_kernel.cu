@@ -1118,6 +1118,12 @@ __device__ void task_comb(const MegaParams& p, const Task& t, uint8_t* simt, int
 // phase) are stored evict-first, so that they do not push x and the weight
 // slices in use out of L2; the MoE layer's act (re-read soon, from L2) is
 // stored normally.
+// SiLU, x * sigmoid(x), with the fast division (2 ulp): its result is rounded
+// to bf16 right after, far coarser, and the IEEE division's refinement cost
+// about 2 us of a one-token gate/up epilogue.  For x < -87 the denominator is
+// past 2^126 and the result is 0, the function's limit.
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
 __device__ __forceinline__ void store_act(const MegaParams& p, uint4* dst, const uint4& v) {
   if (p.dense) __stcs(dst, v);
   else *dst = v;
@@ -1196,8 +1202,8 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
           uint32_t pk[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float a0 = g[2 * i] / (1.0f + __expf(-g[2 * i])) * u[2 * i];
-            const float a1 = g[2 * i + 1] / (1.0f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
+            const float a0 = silu(g[2 * i]) * u[2 * i];
+            const float a1 = silu(g[2 * i + 1]) * u[2 * i + 1];
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
             pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
           }
@@ -1215,7 +1221,7 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
         tmem_ld16(tbase + kAccCols / 2 + cb * 16, u);
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          S[i * 128 + i128] = __float2bfloat16_rn(g[i] / (1.0f + __expf(-g[i])) * u[i]);
+          S[i * 128 + i128] = __float2bfloat16_rn(silu(g[i]) * u[i]);
         named_bar(2 + h, 128);
         // 16 token rows x 128 columns = 256 chunks of 16 bytes
 #pragma unroll
@@ -1248,7 +1254,7 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
           for (int i = 0; i < 16; ++i) {
             const float gte = v[i];
             const float up = U[(q * 16 + i) * 32 + lane];
-            SA[(cb * 16 + i) * 64 + 32 * q + lane] = __float2bfloat16_rn(gte / (1.0f + __expf(-gte)) * up);
+            SA[(cb * 16 + i) * 64 + 32 * q + lane] = __float2bfloat16_rn(silu(gte) * up);
           }
         }
         named_bar(2 + h, 128);
@@ -1275,7 +1281,7 @@ __device__ void task_gemm_epilogue(const MegaParams& p, Ctrl* c, uint8_t* epi, u
           for (int i = 0; i < 16; ++i) {
             const float gte = v[i];
             const float up = U[(q * 16 + i) * 32 + lane];
-            const float a = gte / (1.0f + __expf(-gte)) * up;
+            const float a = silu(gte) * up;
             S[i * 64 + 32 * q + lane] = __float2bfloat16_rn(a);
           }
         }
