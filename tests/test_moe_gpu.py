@@ -290,6 +290,23 @@ def test_wide_tile_forms(oracle_lib, sched, flags):
     _full_check(oracle_lib, w, x, sched, False, debug_flags=flags)
 
 
+@pytest.mark.parametrize("T", [20, 600])
+@pytest.mark.parametrize("sched", [B.ETC_SCHED_STATIC, B.ETC_SCHED_MIXED], ids=["static", "mixed"])
+def test_saturated_gate_activations(oracle_lib, sched, T):
+    # Gate rows scaled by 100: pre-activations reach past -88 and +88, where
+    # SiLU sits on its asymptotes (0 and the identity) and the epilogue's
+    # denominator 1 + exp(-g) leaves the normal range of the fast division.
+    # T=20 runs the one-block direct tiles, T=600 the wide ones.
+    w = inputs.moe_weights(256, 8, 2, 128, seed=51)
+    wgu = w.w_gate_up.float()
+    wgu[:, :128, :] *= 100.0
+    w.w_gate_up = wgu.to(torch.bfloat16)
+    x = inputs.tokens(T, 256, 52)
+    g = np.einsum("th,eih->tei", x.float().numpy(), w.w_gate_up[:, :128, :].float().numpy())
+    assert g.min() < -90.0 and g.max() > 90.0
+    _full_check(oracle_lib, w, x, sched, False)
+
+
 def test_identical_experts_closed_form(oracle_lib):
     # Routing-independent closed form: with every expert equal the layer is one FFN.
     w = inputs.moe_weights(256, 16, 4, 128, seed=23)
