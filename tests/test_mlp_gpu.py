@@ -152,3 +152,27 @@ def test_mlp1_full_size(oracle_lib, mlp1, sched, unfused):
     _close(out[rows], ref)
     assert np.isfinite(out).all()
     plan.close()
+
+
+def _draw_mlp(seed):
+    """A seeded dense MLP shape within the plan's limits (H multiple of 128, I of 64)."""
+    rng = np.random.default_rng(5000 + seed)
+    H = int(rng.choice([128, 256, 384, 512, 768, 1024]))
+    I = int(rng.choice([64, 128, 192, 256, 320, 512, 1024]))
+    T = int(rng.choice([int(rng.integers(1, 33)), int(rng.integers(33, 300)), int(rng.integers(300, 900))]))
+    sched = B.ETC_SCHED_DYNAMIC if rng.integers(0, 2) else B.ETC_SCHED_STATIC
+    flags = B.ETC_DEBUG_NO_PAIR if rng.integers(0, 2) else 0
+    return H, I, T, sched, flags
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_mlp_random_shape(oracle_lib, seed):
+    """Seeded (H, I, T), schedule and tile form (CTA pairs or single-CTA) against the oracle:
+    ragged chunks, narrow and wide tiles, one and many chunks."""
+    H, I, T, sched, flags = _draw_mlp(seed)
+    w = inputs.mlp_weights(H, I, seed=700 + seed)
+    x = inputs.tokens(T, H, seed=800 + seed)
+    plan = B.etc_mlp_plan(H, I, t_max=T, sched=sched, debug_flags=flags)
+    out = _run(plan, x.cuda(), w.w_gate_up.cuda(), w.w_down.cuda(), T, False)
+    _close(out, oracle_lib.mlp(x, w.w_gate_up, w.w_down))
+    plan.close()
