@@ -66,3 +66,19 @@ def test_splitk_closed_form_on_gpu():
     A = np.tile(np.arange(1024, dtype=np.float32), (8, 1))
     C = _run(A, 4, B.ETC_SCHED_DYNAMIC)
     assert np.all(C == 1024 * 1023 / 2)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_splitk_random_shape(oracle_lib, seed):
+    """Seeded row counts, split counts and tile widths (n_cols = n_split * tile, tile a
+    multiple of 4 up to 16384) under both schedules, against the oracle."""
+    rng = np.random.default_rng(6000 + seed)
+    n_split = int(rng.choice([1, 2, 3, 4, 5, 8, 16, 64]))
+    tile = 4 * int(rng.integers(1, 4097 if n_split <= 4 else 257))
+    n_rows = int(rng.choice([int(rng.integers(1, 40)), int(rng.integers(40, 3000))]))
+    while n_rows * n_split * tile > 2e7:  # keep the fp64 oracle quick
+        n_rows = max(1, n_rows // 2)
+    sched = B.ETC_SCHED_DYNAMIC if rng.integers(0, 2) else B.ETC_SCHED_STATIC
+    A = inputs.splitk_matrix(n_rows, n_split * tile, seed=6100 + seed).numpy()
+    C = _run(A, n_split, sched)
+    _check(C, A, oracle_lib, n_split)
